@@ -1,0 +1,206 @@
+/*
+ * kk.h - C ABI of the Key-Key Semantic Affinity block selector (sm_103a).
+ *
+ * The method: the page "Key-Key Semantic Affinity: 用 Key 向量替代注意力分数的
+ * KV Cache 重要性评估" (cited as [KK §n]). A paged K cache is summarised per
+ * block by a mean-pooled Key vector v_b, written once ([KK §2.2 step 1],
+ * [KK §5.2 step 2]); each decode step pools the last W tokens' Keys into
+ * v_anchor ([KK §2.2 step 2], [KK §5.2 step 1]), scores every candidate block by
+ * (1 + cos(v_b, v_anchor)) / 2 ([KK §2.2 step 3], [KK §3.2]; the page's own
+ * formula was lost, this is the reading used) and keeps the top K blocks
+ * ([KK §5.2 step 4]).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are device memory owned by the caller; nothing
+ *    here allocates or frees memory. Scratch comes from a caller-provided
+ *    workspace whose size a *_workspace_bytes() function reports.
+ *  - Every call is asynchronous on `stream` and returns a kk_status. Argument
+ *    errors found on the host are returned before anything is launched.
+ *    Errors that depend on device data (a page id out of range, a block table
+ *    whose length disagrees with seq_lens) are recorded in a device error
+ *    word; the offending item is skipped and kk_device_error() reports the
+ *    first such error. No kernel traps.
+ *  - Key caches are bf16 or float32; pooled vectors, anchors and scores are
+ *    float32, accumulated in float32.
+ *  - The first call on a device looks up the device error word's address;
+ *    make that first call outside CUDA stream capture.
+ */
+#ifndef KK_H_
+#define KK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kk_status {
+  KK_OK = 0,
+  KK_ERR_INVALID = 1,     /* bad argument (null pointer, negative size, K or W out of range) */
+  KK_ERR_UNSUPPORTED = 2, /* valid but not handled: head_dim, alignment, strides */
+  KK_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  KK_ERR_BAD_INDEX = 4,   /* (device) a page id, weight-set id or block table entry out of range */
+  KK_ERR_TIMEOUT = 5      /* (device) a bounded wait gave up */
+} kk_status;
+
+typedef enum kk_dtype { KK_F32 = 0, KK_BF16 = 1 } kk_dtype;
+
+/*
+ * Paged K cache layout [KK §1] (fixed-size token blocks managed as pages).
+ * Element (layer l, page p, head h, token t, dim d) is at
+ *   base + l*stride_layer + p*stride_page + h*stride_head + t*stride_token + d
+ * (strides in elements; the dim stride is 1). base and every stride times the
+ * element size must be multiples of 16 bytes, else KK_ERR_UNSUPPORTED.
+ * head_dim must be 32, 64, 128 or 256 (float32: 32, 64 or 128).
+ */
+typedef struct kk_kcache_desc {
+  const void* base; /* device */
+  int32_t dtype;    /* kk_dtype */
+  int32_t num_layers;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_pages;
+  int64_t stride_layer;
+  int64_t stride_page;
+  int64_t stride_head;
+  int64_t stride_token;
+} kk_kcache_desc;
+
+/*
+ * Per-request block tables, CSR style. Request r owns logical blocks
+ * j = 0 .. nb_r-1 with nb_r = offsets[r+1] - offsets[r], which must equal
+ * ceil(seq_lens[r] / block_size); its block j lives in physical page
+ * pages[offsets[r] + j] and holds min(block_size, seq_lens[r] - j*block_size)
+ * valid tokens. max_blocks (host value) bounds every nb_r.
+ */
+typedef struct kk_block_table {
+  const int32_t* pages;    /* device [offsets[R]] */
+  const int32_t* offsets;  /* device [R+1], non-decreasing, offsets[0] = 0 */
+  const int32_t* seq_lens; /* device [R] */
+  int32_t num_requests;    /* R */
+  int32_t max_blocks;      /* host bound of nb_r */
+} kk_block_table;
+
+/* Name of a status code (static string). */
+const char* kk_status_str(kk_status s);
+
+/* Synchronises `stream`, returns the first device-side error recorded since
+ * the last call in *code (KK_OK if none) and clears it. */
+kk_status kk_device_error(cudaStream_t stream, int32_t* code);
+
+/*
+ * kk_pool_blocks - block representation v_b [KK §2.2 step 1], [KK §5.2 step 2-3].
+ * For i < n, with p = pages[i] and m = n_valid[i] (0..block_size):
+ *   vb[p][d] = sum_{l,h} w[l,h] * (1/m) * sum_{t<m} K[l,p,h,t,d]
+ * where w = 1/(L*H) when head_w is NULL, else w = head_w[w_set[i]][l*H+h]
+ * (head_w: device [n_sets][L*H]; w_set: device [n], values < n_sets).
+ * m = 0 writes the zero vector. vb: device [num_pages][head_dim], rows not
+ * named in `pages` are left untouched. Tokens t >= m are never read.
+ */
+kk_status kk_pool_blocks(const kk_kcache_desc* kc, const int32_t* pages, const int32_t* n_valid,
+                         int32_t n, const float* head_w, int32_t n_sets, const int32_t* w_set,
+                         float* vb, cudaStream_t stream);
+
+/*
+ * Head-variance weights [KK §3.3 finding 2], [KK §6.1]: for request r and
+ * each (layer, head), Var = (1/D) sum_d (mean_t K^2 - (mean_t K)^2) over the
+ * request's seq_lens[r] tokens, and head_w_out[r][l*H+h] = Var / sum Var
+ * (uniform 1/(L*H) if every Var is 0). head_w_out: device [R][L*H].
+ * Needs kk_head_variance_workspace_bytes() bytes of device workspace.
+ */
+size_t kk_head_variance_workspace_bytes(const kk_kcache_desc* kc, int32_t total_blocks,
+                                        int32_t num_requests);
+kk_status kk_head_variance(const kk_kcache_desc* kc, const kk_block_table* bt,
+                           int32_t total_blocks, float* head_w_out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Weighted pooling of every block of every request in one pass over K:
+ * the head-variance weights of each request (as kk_head_variance, written to
+ * head_w_out [R][L*H]) and vb[pages[offsets[r]+j]] pooled with them (as
+ * kk_pool_blocks). total_blocks = offsets[R]. Same workspace size as
+ * kk_head_variance.
+ */
+kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table* bt,
+                                  int32_t total_blocks, float* head_w_out, float* vb,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kk_anchor - query anchor [KK §2.2 step 2], [KK §5.2 step 1]:
+ *   va[r][d] = sum_{l,h} w[l,h] * (1/W') * sum_{T-W' <= p < T} K[l, page(p), h, p % bs, d]
+ * with T = seq_lens[r], W' = min(W, T), page(p) = pages[offsets[r] + p / bs],
+ * w uniform 1/(L*H) or head_w[r][l*H+h] (device [R][L*H]). T = 0 gives the
+ * zero vector. 1 <= W <= 1024. va: device [R][head_dim].
+ */
+kk_status kk_anchor(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                    const float* head_w, float* va, cudaStream_t stream);
+
+/*
+ * kk_score - affinity [KK §2.2 step 3], [KK §3.2], [KK §5.2 step 3]:
+ *   scores[offsets[r]+j] = (1 + cos(vb[pages[offsets[r]+j]], va[r])) / 2
+ * cos = 0 when either vector is zero. vb: device [num_pages][D] float32
+ * (num_pages bounds the page ids), va: device [R][D], scores: device
+ * [offsets[R]]. D in {32, 64, 128, 256}.
+ */
+kk_status kk_score(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                   const float* va, float* scores, cudaStream_t stream);
+
+/*
+ * kk_topk - top-K selection [KK §5.2 step 4]. For each request r, among
+ * scores[offsets[r] .. offsets[r+1]) the K largest, ordered by score
+ * descending, equal scores by lower index. idx[r][k] is the logical index
+ * (position within the request's range), top_scores[r][k] (nullable) its
+ * score; slots past the request's count hold -1 and -inf.
+ * offsets: device [R+1]; max_n bounds every range; 1 <= K <= 256.
+ */
+kk_status kk_topk(const float* scores, const int32_t* offsets, int32_t R, int32_t max_n, int32_t K,
+                  int32_t* idx, float* top_scores, cudaStream_t stream);
+
+/* kk_score followed by kk_topk in one launch; `scores` (nullable) receives
+ * the full score vector as kk_score would. */
+kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                        const float* va, int32_t K, int32_t* idx, float* top_scores, float* scores,
+                        cudaStream_t stream);
+
+/*
+ * One decode step of the selector in one launch: kk_anchor, kk_score and
+ * kk_topk [KK §5.2 steps 1-4]. vb: device [num_pages][head_dim] (the
+ * table kk_pool_blocks wrote). va, scores and top_scores are nullable outputs.
+ */
+kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                         const float* head_w, const float* vb, int32_t K, float* va, int32_t* idx,
+                         float* top_scores, float* scores, cudaStream_t stream);
+
+/*
+ * Shared-pool scoring [KK §5.1] (every representation against the anchors
+ * in one matrix product, then a mask): R anchors A (device bf16 bits [R][D])
+ * against N pooled block vectors V (device bf16 bits [N][D]); anchor r may
+ * only pick blocks j whose bit (j % 32) of mask[r][j / 32] is set (device
+ * uint32 [R][ceil(N/32)]). Scores are (1 + cos)/2 from float32 dot products
+ * of the bf16 values; per anchor the top K pool ids (ordered as kk_topk) go
+ * to idx [R][K] and top_scores [R][K] (nullable). D = 128, 1 <= K <= 256.
+ */
+size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K);
+kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,
+                                int32_t R, int32_t N, int32_t D, int32_t K, int32_t* idx,
+                                float* top_scores, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
+ * Coarse representations [KK §5.1] (a coarser level's representation is the
+ * mean of its children's): for request r and group g,
+ *   out[r][g][d] = mean over j in [g*group, min((g+1)*group, nb_r)) of vb[pages[offsets[r]+j]][d]
+ * out: device [R][ceil(max_blocks/group)][D]; groups past a request's last
+ * block are written as zero. D in {32, 64, 128, 256}, group >= 1.
+ */
+kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                          int32_t group, float* out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KK_H_ */

@@ -1,0 +1,237 @@
+"""fp64 CPU oracle for Key-Key Semantic Affinity block scoring.
+
+TEST INFRASTRUCTURE. This module is the slow, plain statement of what the
+hot path computes. Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import it. The library's own code path
+never calls it, and it shares no code with the CUDA sources.
+
+Source: the page "Key-Key Semantic Affinity: 用 Key 向量替代注意力分数的 KV
+Cache 重要性评估" (cited below as [KK §n]):
+
+* [KK §2.2 step 1], [KK §5.2 step 2-3]: a block's representation v_b is the
+  mean of its Key vectors over all tokens of the block, all KV heads and all
+  layers; it is computed once, when the block is written.
+* [KK §2.2 step 2], [KK §5.2 step 1]: the query anchor v_anchor is the mean of
+  the Keys of the most recent W_local tokens.
+* [KK §2.2 step 3], [KK §3.2]: the affinity of a block is the similarity of
+  v_b and v_anchor, normalised. The formula itself is lost from the page; the
+  reading used here is score = (1 + cos(v_b, v_anchor)) / 2, so orthogonal
+  vectors score 0.5, identical directions 1 and opposite directions 0.
+* [KK §5.2 step 4], [KK §5.1]: the K blocks with the highest affinity are
+  selected.
+* [KK §3.3 finding 2], [KK §6.1]: optional weighting of each head by its
+  variance.  Read here as the Key variance of each (layer, KV head):
+  the mean over d of the population variance over the request's tokens,
+  normalised so the weights sum to one.
+* [KK §5.1]: a coarse (Grid / Chunk) representation is the mean of its
+  children's representations.
+
+Every function accumulates in float64. bf16 inputs are decoded exactly
+(bits << 16). Parity of the variance weighting and of the (1+cos)/2 formula
+with the published method is unpinned (the page does not print either);
+everything else here is pinned by tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "decode",
+    "block_keys",
+    "pool_block",
+    "pool_blocks",
+    "head_variance_weights",
+    "anchor",
+    "affinity",
+    "topk",
+    "score_topk",
+    "score_pool_batched",
+    "coarse_means",
+]
+
+
+def decode(x) -> np.ndarray:
+    """Return ``x`` as float64. uint16 arrays are bf16 bit patterns."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def block_keys(kc, page: int, n: int) -> np.ndarray:
+    """Keys of the first ``n`` tokens of physical page ``page``.
+
+    ``kc`` is the paged K cache viewed as [L][P][H][bs][D] (any strides).
+    Returns float64 [L][H][n][D].
+    """
+    return decode(kc[:, page, :, :n, :])
+
+
+def _weights(L: int, H: int, head_w) -> np.ndarray:
+    """Per-(layer, head) weights: uniform 1/(L*H) unless given [KK §5.2 step 3]."""
+    if head_w is None:
+        return np.full((L, H), 1.0 / (L * H))
+    return np.asarray(head_w, dtype=np.float64).reshape(L, H)
+
+
+def pool_block(keys: np.ndarray, head_w=None) -> np.ndarray:
+    """v_b of one block [KK §2.2 step 1], [KK §5.2 step 3].
+
+    keys: float64 [L][H][n][D]. Each (layer, head) contributes the mean of its
+    n token Keys; those means are combined with weights w[l,h] (uniform
+    1/(L*H) when ``head_w`` is None, which is the plain mean over tokens,
+    heads and layers). A block with no valid token pools to the zero vector.
+    """
+    L, H, n, D = keys.shape
+    if n == 0:
+        return np.zeros(D)
+    token_mean = keys.sum(axis=2) / n  # [L][H][D]
+    w = _weights(L, H, head_w)
+    return np.einsum("lh,lhd->d", w, token_mean)
+
+
+def pool_blocks(kc, pages, n_valid, head_w=None, w_set=None) -> np.ndarray:
+    """v_b rows for a list of physical pages; row i belongs to pages[i].
+
+    head_w: None, or [n_sets][L*H] weights; w_set[i] picks the set for row i.
+    """
+    L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+    out = np.zeros((len(pages), D))
+    for i, (p, n) in enumerate(zip(pages, n_valid)):
+        w = None
+        if head_w is not None:
+            w = np.asarray(head_w, dtype=np.float64).reshape(-1, L * H)[w_set[i]]
+        out[i] = pool_block(block_keys(kc, int(p), int(n)), w)
+    return out
+
+
+def request_tokens_of_layer(kc, layer: int, pages_r, seq_len: int, bs: int) -> np.ndarray:
+    """float64 [H][T][D]: every Key of one layer of one request, in token order."""
+    pages_r = np.asarray(pages_r, dtype=np.int64)
+    nb = len(pages_r)
+    if nb == 0 or seq_len == 0:
+        return np.zeros((kc.shape[2], 0, kc.shape[4]))
+    k = decode(kc[layer, pages_r])  # [nb][H][bs][D]
+    k = np.transpose(k, (1, 0, 2, 3)).reshape(k.shape[1], nb * bs, k.shape[3])
+    return k[:, :seq_len, :]
+
+
+def head_variance_weights(kc, pages_r, seq_len: int, bs: int) -> np.ndarray:
+    """Head-variance weights of one request [KK §3.3 finding 2], [KK §6.1].
+
+    For each (layer, KV head): mu_d = mean over the request's T tokens of K_d;
+    Var = (1/D) * sum_d (1/T) * sum_t (K_d - mu_d)^2 (two passes, float64).
+    Weights are Var / sum(Var) over all (layer, head), returned as [L*H];
+    when every Var is 0 (no tokens, or constant Keys) the weights are uniform.
+    """
+    L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+    var = np.zeros((L, H))
+    for layer in range(L):
+        k = request_tokens_of_layer(kc, layer, pages_r, seq_len, bs)  # [H][T][D]
+        if k.shape[1]:
+            mu = k.mean(axis=1, keepdims=True)
+            var[layer] = ((k - mu) ** 2).mean(axis=1).mean(axis=1)
+    if var.sum() == 0:
+        return np.full(L * H, 1.0 / (L * H))
+    return (var / var.sum()).reshape(L * H)
+
+
+def anchor(kc, pages_r, seq_len: int, bs: int, W: int, head_w=None) -> np.ndarray:
+    """v_anchor of one request [KK §2.2 step 2], [KK §5.2 step 1].
+
+    The mean of the Keys of the last min(W, T) tokens, taken per (layer, head)
+    over those tokens and combined with the same per-(layer, head) weights as
+    the block pooling. The tokens are read from the paged cache through the
+    request's block table. A request with no token gives the zero vector.
+    """
+    L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+    w_eff = min(W, seq_len)
+    if w_eff == 0:
+        return np.zeros(D)
+    rows = np.stack(
+        [decode(kc[:, int(pages_r[p // bs]), :, p % bs, :]) for p in range(seq_len - w_eff, seq_len)]
+    )  # [W][L][H][D]
+    token_mean = rows.mean(axis=0)  # [L][H][D]
+    w = _weights(L, H, head_w)
+    return np.einsum("lh,lhd->d", w, token_mean)
+
+
+def affinity(vb: np.ndarray, va: np.ndarray) -> np.ndarray:
+    """score = (1 + cos(v_b, v_anchor)) / 2 per row of ``vb`` [KK §2.2 step 3], [KK §3.2].
+
+    cos is taken as 0 when either vector is zero, so such a block scores 0.5.
+    """
+    vb = np.atleast_2d(decode(vb))
+    va = decode(va)
+    dot = vb @ va
+    nb = np.sqrt((vb * vb).sum(axis=1))
+    na = np.sqrt((va * va).sum())
+    denom = nb * na
+    cos = np.where(denom > 0, dot / np.where(denom > 0, denom, 1.0), 0.0)
+    return (1.0 + cos) / 2.0
+
+
+def topk(scores, K: int):
+    """The K highest scores [KK §5.2 step 4]: order by score descending, ties
+    to the lower index. Slots beyond the number of candidates hold -1 / -inf.
+
+    Returns (idx int64 [K], score float64 [K]).
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    order = np.lexsort((np.arange(len(s)), -s))[:K]
+    idx = np.full(K, -1, dtype=np.int64)
+    val = np.full(K, -np.inf)
+    idx[: len(order)] = order
+    val[: len(order)] = s[order]
+    return idx, val
+
+
+def score_topk(vb_table, pages_r, va, K: int):
+    """Affinity of every block in a request's table, then its top-K.
+
+    vb_table is indexed by physical page; the returned indices are logical
+    (positions in the request's block table).
+    """
+    s = affinity(np.asarray(vb_table)[np.asarray(pages_r, dtype=np.int64)], va)
+    idx, val = topk(s, K)
+    return s, idx, val
+
+
+def score_pool_batched(A, V, mask_words, K: int):
+    """Scores of R anchors against a shared pool of N block vectors, each
+    anchor restricted to the blocks its mask marks, then top-K per anchor
+    [KK §5.1] (all representations against the anchor in one product).
+
+    A: [R][D], V: [N][D] (bf16 bits or floats); mask_words: uint32
+    [R][ceil(N/32)], bit (j % 32) of word j // 32 marks block j.
+    Returns (idx int64 [R][K] pool ids, score float64 [R][K]).
+    """
+    A = decode(A)
+    V = decode(V)
+    R, N = A.shape[0], V.shape[0]
+    mw = np.asarray(mask_words, dtype=np.uint32)
+    idx = np.full((R, K), -1, dtype=np.int64)
+    val = np.full((R, K), -np.inf)
+    for r in range(R):
+        j = np.arange(N)
+        owned = ((mw[r, j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool)
+        cand = j[owned]
+        s = affinity(V[cand], A[r])
+        i_loc, v = topk(s, K)
+        keep = i_loc >= 0
+        idx[r, keep] = cand[i_loc[keep]]
+        val[r] = v
+    return idx, val
+
+
+def coarse_means(vb_logical, group: int) -> np.ndarray:
+    """Coarse representations [KK §5.1]: the mean of ``group`` consecutive
+    block representations; the last group averages whatever blocks remain.
+    """
+    vb_logical = decode(vb_logical)
+    nb = vb_logical.shape[0]
+    ng = (nb + group - 1) // group
+    out = np.zeros((ng, vb_logical.shape[1]))
+    for g in range(ng):
+        out[g] = vb_logical[g * group : min((g + 1) * group, nb)].mean(axis=0)
+    return out

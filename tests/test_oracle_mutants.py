@@ -1,0 +1,190 @@
+"""Plausible mistakes planted in a copy of the CPU oracle must each fail at
+least one pin of tests/test_oracle_pins.py (the mistakes live only here, on
+the CPU, in a namespace copy; the real oracle is untouched)."""
+import types
+
+import numpy as np
+import pytest
+
+from oracle import kk_oracle as ko
+from tests.test_oracle_pins import ALL_CHECKS
+
+
+def _copy():
+    return types.SimpleNamespace(**{k: getattr(ko, k) for k in dir(ko) if not k.startswith("__")})
+
+
+def m_pool_divides_by_heads_only(o):
+    def pool_block(keys, head_w=None):
+        L, H, n, D = keys.shape
+        if n == 0:
+            return np.zeros(D)
+        w = o._weights(L, H, head_w)
+        return np.einsum("lh,lhd->d", w * L, keys.sum(axis=2) / n)
+    o.pool_block = pool_block
+
+
+def m_pool_weights_transposed(o):
+    def _weights(L, H, head_w):
+        if head_w is None:
+            return np.full((L, H), 1.0 / (L * H))
+        return np.asarray(head_w, dtype=np.float64).reshape(H, L).T
+
+    def pool_block(keys, head_w=None):
+        L, H, n, D = keys.shape
+        if n == 0:
+            return np.zeros(D)
+        return np.einsum("lh,lhd->d", _weights(L, H, head_w), keys.sum(axis=2) / n)
+    o.pool_block = pool_block
+
+
+def m_pool_sum_not_mean(o):
+    def pool_block(keys, head_w=None):
+        L, H, n, D = keys.shape
+        if n == 0:
+            return np.zeros(D)
+        return np.einsum("lh,lhd->d", o._weights(L, H, head_w), keys.sum(axis=2))
+    o.pool_block = pool_block
+
+
+def m_affinity_not_halved(o):
+    base = ko.affinity
+    o.affinity = lambda vb, va: 2.0 * base(vb, va)
+
+
+def m_affinity_raw_dot(o):
+    def affinity(vb, va):
+        vb = np.atleast_2d(ko.decode(vb))
+        return (1.0 + vb @ ko.decode(va)) / 2.0
+    o.affinity = affinity
+
+
+def m_affinity_zero_vector_scores_zero(o):
+    def affinity(vb, va):
+        vb = np.atleast_2d(ko.decode(vb))
+        va = ko.decode(va)
+        denom = np.sqrt((vb * vb).sum(axis=1)) * np.sqrt((va * va).sum())
+        return np.where(denom > 0, (1.0 + (vb @ va) / np.where(denom > 0, denom, 1)) / 2.0, 0.0)
+    o.affinity = affinity
+
+
+def m_topk_ties_to_higher_index(o):
+    def topk(scores, K):
+        s = np.asarray(scores, dtype=np.float64)
+        order = np.lexsort((-np.arange(len(s)), -s))[:K]
+        idx = np.full(K, -1, dtype=np.int64)
+        val = np.full(K, -np.inf)
+        idx[: len(order)] = order
+        val[: len(order)] = s[order]
+        return idx, val
+    o.topk = topk
+
+
+def m_topk_ascending(o):
+    base = ko.topk
+    o.topk = lambda scores, K: base(-np.asarray(scores, dtype=np.float64), K)
+
+
+def m_anchor_first_tokens(o):
+    def anchor(kc, pages_r, seq_len, bs, W, head_w=None):
+        L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+        w_eff = min(W, seq_len)
+        if w_eff == 0:
+            return np.zeros(D)
+        rows = np.stack([ko.decode(kc[:, int(pages_r[p // bs]), :, p % bs, :]) for p in range(w_eff)])
+        return np.einsum("lh,lhd->d", o._weights(L, H, head_w), rows.mean(axis=0))
+    o.anchor = anchor
+
+
+def m_anchor_ignores_block_table(o):
+    def anchor(kc, pages_r, seq_len, bs, W, head_w=None):
+        L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+        w_eff = min(W, seq_len)
+        if w_eff == 0:
+            return np.zeros(D)
+        rows = np.stack([ko.decode(kc[:, p // bs, :, p % bs, :]) for p in range(seq_len - w_eff, seq_len)])
+        return np.einsum("lh,lhd->d", o._weights(L, H, head_w), rows.mean(axis=0))
+    o.anchor = anchor
+
+
+def m_variance_one_mean_for_all_dims(o):
+    # (a sample variance, ddof=1, is not a mistake here: the factor T/(T-1)
+    # is shared by every head of a request and cancels in the normalisation)
+    def head_variance_weights(kc, pages_r, seq_len, bs):
+        L, H = kc.shape[0], kc.shape[2]
+        var = np.zeros((L, H))
+        for layer in range(L):
+            k = ko.request_tokens_of_layer(kc, layer, pages_r, seq_len, bs)
+            var[layer] = k.reshape(H, -1).var(axis=1) if k.shape[1] else 0.0
+        return (var / var.sum()).reshape(L * H) if var.sum() else np.full(L * H, 1.0 / (L * H))
+    o.head_variance_weights = head_variance_weights
+
+
+def m_variance_std_not_var(o):
+    def head_variance_weights(kc, pages_r, seq_len, bs):
+        L, H = kc.shape[0], kc.shape[2]
+        var = np.zeros((L, H))
+        for layer in range(L):
+            k = ko.request_tokens_of_layer(kc, layer, pages_r, seq_len, bs)
+            var[layer] = np.sqrt(k.var(axis=1).mean(axis=1))
+        return (var / var.sum()).reshape(L * H) if var.sum() else np.full(L * H, 1.0 / (L * H))
+    o.head_variance_weights = head_variance_weights
+
+
+def m_coarse_last_group_divided_by_group(o):
+    def coarse_means(vb_logical, group):
+        vb_logical = ko.decode(vb_logical)
+        nb = vb_logical.shape[0]
+        ng = (nb + group - 1) // group
+        return np.stack([vb_logical[g * group:(g + 1) * group].sum(axis=0) / group for g in range(ng)])
+    o.coarse_means = coarse_means
+
+
+def m_batched_ignores_mask(o):
+    def score_pool_batched(A, V, mask_words, K):
+        full = np.full_like(np.asarray(mask_words, dtype=np.uint32), 0xFFFFFFFF)
+        return ko.score_pool_batched(A, V, full, K)
+    o.score_pool_batched = score_pool_batched
+
+
+MUTANTS = [
+    m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
+    m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
+    m_topk_ties_to_higher_index, m_topk_ascending, m_anchor_first_tokens,
+    m_anchor_ignores_block_table, m_variance_one_mean_for_all_dims, m_variance_std_not_var,
+    m_coarse_last_group_divided_by_group, m_batched_ignores_mask,
+]
+
+
+def _bind(o):
+    """Re-bind the oracle's composite functions to the mutated namespace."""
+    def pool_blocks(kc, pages, n_valid, head_w=None, w_set=None):
+        L, H, D = kc.shape[0], kc.shape[2], kc.shape[4]
+        out = np.zeros((len(pages), D))
+        for i, (p, n) in enumerate(zip(pages, n_valid)):
+            w = None if head_w is None else np.asarray(head_w, float).reshape(-1, L * H)[w_set[i]]
+            out[i] = o.pool_block(ko.block_keys(kc, int(p), int(n)), w)
+        return out
+
+    def score_topk(vb_table, pages_r, va, K):
+        s = o.affinity(np.asarray(vb_table)[np.asarray(pages_r, dtype=np.int64)], va)
+        idx, val = o.topk(s, K)
+        return s, idx, val
+
+    o.pool_blocks = pool_blocks
+    o.score_topk = score_topk
+    return o
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda m: m.__name__)
+def test_planted_mistake_is_caught(mutant):
+    o = _copy()
+    mutant(o)
+    _bind(o)
+    failed = []
+    for check in ALL_CHECKS:
+        try:
+            check(o)
+        except (AssertionError, ValueError, IndexError, ZeroDivisionError, FloatingPointError):
+            failed.append(check.__name__)
+    assert failed, f"no pin catches {mutant.__name__}"

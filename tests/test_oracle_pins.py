@@ -1,0 +1,315 @@
+"""Pins of the CPU oracle to things other than itself: hand-computed values
+(tests/golden), closed forms, brute force written as plain loops, and
+invariants that follow from the definitions. Each check is written as a
+function of an oracle namespace so that test_oracle_mutants.py can show a
+plausible mistake planted in the oracle fails at least one of them."""
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import kk_oracle as ko
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _f(x):
+    return float("-inf") if x == "-inf" else float(x)
+
+
+# --------------------------------------------------------------------------
+# checks parameterised by the oracle namespace
+# --------------------------------------------------------------------------
+
+
+def check_pool_golden(o):
+    g = gold("pool_tiny.json")
+    K = np.array(g["K"], dtype=np.float64)  # [L][H][n][D]
+    np.testing.assert_allclose(o.pool_block(K), g["vb_uniform"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o.pool_block(K, g["head_w"]), g["vb_weighted"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o.pool_block(K[:, :, :1, :]), g["vb_uniform_n1"], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(o.pool_block(K[:, :, :0, :]), [0.0, 0.0])
+
+
+def check_affinity_golden(o):
+    for c in gold("affinity.json")["cases"]:
+        s = o.affinity(np.array([c["vb"]], float), np.array(c["va"], float))[0]
+        assert abs(s - c["score"]) < 1e-15, c
+
+
+def check_topk_golden(o):
+    g = gold("topk.json")
+    for c in g["cases"]:
+        idx, val = o.topk(g["scores"], c["K"])
+        assert list(idx) == c["idx"]
+        assert [float(v) for v in val] == [_f(v) for v in c["score"]]
+
+
+def _anchor_cache(g):
+    # [L=1][P=2][H=1][bs=2][D=2], invalid slot = NaN
+    kc = np.full((1, 2, 1, 2, 2), np.nan)
+    for p, page in enumerate(g["K"]):
+        for t, row in enumerate(page):
+            if row is not None:
+                kc[0, p, 0, t] = row
+    return kc
+
+
+def check_anchor_golden(o):
+    g = gold("anchor.json")
+    kc = _anchor_cache(g)
+    for c in g["cases"]:
+        va = o.anchor(kc, g["pages_r"], g["seq_len"], 2, c["W"])
+        np.testing.assert_allclose(va, c["va"], rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(o.anchor(kc, g["pages_r"], 0, 2, 4), [0.0, 0.0])
+
+
+def check_variance_golden(o):
+    for c in gold("variance.json")["cases"]:
+        k = np.array(c["K_h_t_d"], float)  # [H][T][D]
+        H, T, D = k.shape
+        kc = k[None, None, :, :, :]  # [L=1][P=1][H][bs=T][D]
+        w = o.head_variance_weights(kc, [0], T, T)
+        np.testing.assert_allclose(w, c["weights"], rtol=1e-14, atol=1e-15)
+
+
+def check_coarse_golden(o):
+    g = gold("coarse.json")
+    np.testing.assert_allclose(o.coarse_means(np.array(g["vb"], float), g["group"]), g["out"], atol=0)
+
+
+def check_batched_golden(o):
+    g = gold("batched.json")
+    idx, val = o.score_pool_batched(np.array(g["A"], float), np.array(g["V"], float),
+                                    np.array(g["mask_words"], np.uint32), g["K"])
+    assert idx.tolist() == g["idx"]
+    np.testing.assert_allclose(val, g["score"], rtol=1e-15)
+
+
+# ---- brute force: plain loops, written independently of the oracle ------
+
+
+def bf_pool(K, n, w=None):
+    L, H, _, D = K.shape
+    out = [0.0] * D
+    for d in range(D):
+        acc = 0.0
+        for l in range(L):
+            for h in range(H):
+                s = 0.0
+                for t in range(n):
+                    s += float(K[l][h][t][d])
+                wl = (1.0 / (L * H)) if w is None else float(w[l * H + h])
+                acc += wl * (s / n if n else 0.0)
+        out[d] = acc
+    return out
+
+
+def bf_cos_score(a, b):
+    dot = sum(float(x) * float(y) for x, y in zip(a, b))
+    na = math.sqrt(sum(float(x) ** 2 for x in a))
+    nb = math.sqrt(sum(float(y) ** 2 for y in b))
+    c = 0.0 if na == 0 or nb == 0 else dot / (na * nb)
+    return (1.0 + c) / 2.0
+
+
+def bf_topk(s, K):
+    order = sorted(range(len(s)), key=lambda j: (-s[j], j))[:K]
+    return order + [-1] * (K - len(order))
+
+
+def check_bruteforce(o, seed=0):
+    rng = random.Random(seed)
+    for _ in range(20):
+        L, H, bs, D = rng.randint(1, 3), rng.randint(1, 3), rng.randint(1, 4), rng.randint(2, 4)
+        P = rng.randint(2, 5)
+        kc = np.array([[[[[rng.randint(-4, 4) for _ in range(D)] for _ in range(bs)] for _ in range(H)]
+                        for _ in range(P)] for _ in range(L)], dtype=np.float64)
+        p, n = rng.randrange(P), rng.randint(0, bs)
+        w = [rng.random() for _ in range(L * H)]
+        blk = kc[:, p, :, :, :]
+        np.testing.assert_allclose(o.pool_blocks(kc, [p], [n])[0], bf_pool(blk, n), atol=1e-12)
+        np.testing.assert_allclose(o.pool_blocks(kc, [p], [n], [w], [0])[0], bf_pool(blk, n, w), atol=1e-12)
+        # anchor through a random block table
+        nbk = rng.randint(1, P)
+        pages_r = rng.sample(range(P), nbk)
+        T = rng.randint((nbk - 1) * bs + 1, nbk * bs)
+        W = rng.randint(1, T + 2)
+        we = min(W, T)
+        want = [0.0] * D
+        for d in range(D):
+            for l in range(L):
+                for h in range(H):
+                    s = 0.0
+                    for q in range(T - we, T):
+                        s += kc[l][pages_r[q // bs]][h][q % bs][d]
+                    want[d] += s / we / (L * H)
+        np.testing.assert_allclose(o.anchor(kc, pages_r, T, bs, W), want, atol=1e-12)
+        # affinity + top-K on random vectors (some zero)
+        vb = [[rng.randint(-3, 3) for _ in range(D)] for _ in range(rng.randint(1, 9))]
+        va = [rng.randint(-3, 3) for _ in range(D)]
+        s_bf = [bf_cos_score(v, va) for v in vb]
+        s_o = o.affinity(np.array(vb, float), np.array(va, float))
+        np.testing.assert_allclose(s_o, s_bf, atol=1e-14)
+        K = rng.randint(1, len(vb) + 2)
+        assert list(o.topk(s_bf, K)[0]) == bf_topk(s_bf, K)
+
+
+def check_batched_bruteforce(o, seed=1):
+    rng = np.random.default_rng(seed)
+    R, N, D, K = 3, 70, 4, 5
+    A = rng.integers(-3, 4, size=(R, D)).astype(float)
+    V = rng.integers(-3, 4, size=(N, D)).astype(float)
+    mask = np.zeros((R, 3), np.uint32)
+    owned = [sorted(rng.choice(N, size=rng.integers(0, 12), replace=False).tolist()) for _ in range(R)]
+    for r, js in enumerate(owned):
+        for j in js:
+            mask[r, j // 32] |= np.uint32(1 << (j % 32))
+    idx, val = o.score_pool_batched(A, V, mask, K)
+    for r in range(R):
+        s = {j: bf_cos_score(V[j], A[r]) for j in owned[r]}
+        order = sorted(s, key=lambda j: (-s[j], j))[:K]
+        assert idx[r].tolist() == order + [-1] * (K - len(order))
+
+
+# ---- invariants ----------------------------------------------------------
+
+
+def small_specs():
+    return [
+        synth.tiny_05b(L=3, seq_lens=[16 * 12 + 5, 16 * 3], num_topics=4),
+        synth.qwen7b(L=2, H=2, D=32, bs=8, seq_lens=[64, 40, 8], num_topics=4, W=5, K=6),
+    ]
+
+
+def check_reblocking(o):
+    # same tokens cut at block size 8 and 32 (topics change every 32 tokens)
+    a = synth.qwen7b(L=2, H=2, D=16, bs=8, seq_lens=[128], span=32, num_topics=4, seed=11)
+    b = synth.qwen7b(L=2, H=2, D=16, bs=32, seq_lens=[128], span=32, num_topics=4, seed=11)
+    ka = synth.view_paged(synth.gen_paged_numpy(a), a)
+    kb = synth.view_paged(synth.gen_paged_numpy(b), b)
+    va = o.pool_blocks(ka, a.pages, a.n_valid)
+    vb = o.pool_blocks(kb, b.pages, b.n_valid)
+    np.testing.assert_allclose(va.reshape(4, 4, -1).mean(axis=1), vb, rtol=1e-12, atol=1e-12)
+    # coarse means of the fine level reproduce the coarse blocks
+    np.testing.assert_allclose(o.coarse_means(va, 4), vb, rtol=1e-12, atol=1e-12)
+    # and the mean over all blocks is the same at both block sizes
+    np.testing.assert_allclose(o.coarse_means(va, 16), o.coarse_means(vb, 4), rtol=1e-12, atol=1e-12)
+
+
+def check_linearity_and_symmetry(o, seed=2):
+    rng = np.random.default_rng(seed)
+    L, H, n, D = 3, 2, 5, 4
+    k1, k2 = rng.standard_normal((2, L, H, n, D))
+    np.testing.assert_allclose(o.pool_block(2.0 * k1 - 3.0 * k2), 2.0 * o.pool_block(k1) - 3.0 * o.pool_block(k2),
+                               rtol=1e-12, atol=1e-12)
+    perm_l, perm_h = rng.permutation(L), rng.permutation(H)
+    np.testing.assert_allclose(o.pool_block(k1[perm_l][:, perm_h]), o.pool_block(k1), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(o.pool_block(k1, [0.7] * (L * H)) / (0.7 * L * H), o.pool_block(k1), rtol=1e-12)
+    # scaling either vector leaves the score unchanged
+    vb, va = rng.standard_normal((5, D)), rng.standard_normal(D)
+    np.testing.assert_allclose(o.affinity(3.5 * vb, 0.25 * va), o.affinity(vb, va), rtol=1e-13)
+    # an equal set of weights is the unweighted mean: scale-free variance weights
+    kc = rng.standard_normal((L, 1, H, n, D))
+    w = o.head_variance_weights(kc, [0], n, n)
+    w2 = o.head_variance_weights(3.0 * kc + 1.0, [0], n, n)
+    np.testing.assert_allclose(w, w2, rtol=1e-12)
+    assert abs(w.sum() - 1.0) < 1e-12
+
+
+def check_page_shuffle(o):
+    a = synth.qwen7b(L=2, H=2, D=16, bs=4, seq_lens=[30, 17], num_topics=3, seed=21)
+    b = synth.qwen7b(L=2, H=2, D=16, bs=4, seq_lens=[30, 17], num_topics=3, seed=21, shuffle_pages=True, extra_pages=5)
+    assert not np.array_equal(a.pages, b.pages[: a.total_blocks])
+    ka = synth.view_paged(synth.gen_paged_numpy(a), a)
+    kb = synth.view_paged(synth.gen_paged_numpy(b), b)
+    for r in range(a.R):
+        T = a.seq_lens[r]
+        la = o.pool_blocks(ka, a.pages_of(r), a.n_valid[a.offsets[r]:a.offsets[r + 1]])
+        lb = o.pool_blocks(kb, b.pages_of(r), b.n_valid[b.offsets[r]:b.offsets[r + 1]])
+        np.testing.assert_array_equal(la, lb)
+        np.testing.assert_array_equal(o.anchor(ka, a.pages_of(r), T, 4, 6), o.anchor(kb, b.pages_of(r), T, 4, 6))
+        np.testing.assert_array_equal(o.head_variance_weights(ka, a.pages_of(r), T, 4),
+                                      o.head_variance_weights(kb, b.pages_of(r), T, 4))
+
+
+def check_planted_topics(o):
+    for spec in small_specs() + [synth.tiny_05b()]:
+        kc = synth.view_paged(synth.gen_paged_numpy(spec), spec)
+        vb_table = np.zeros((spec.num_pages, spec.D))
+        vb_table[spec.pages] = o.pool_blocks(kc, spec.pages, spec.n_valid)
+        for r in range(spec.R):
+            pr = spec.pages_of(r)
+            va = o.anchor(kc, pr, spec.seq_lens[r], spec.bs, spec.W)
+            s, idx, _ = o.score_topk(vb_table, pr, va, spec.K)
+            topic = spec.block_topic[spec.offsets[r]:spec.offsets[r + 1]]
+            same = np.flatnonzero(topic == spec.query_topic[r])
+            m = min(spec.K, len(same))
+            assert set(idx[:m].tolist()) <= set(same.tolist()), (spec.name, r)
+            off = np.flatnonzero(topic != spec.query_topic[r])
+            if len(off):
+                assert s[same].min() > s[off].max()
+
+
+ALL_CHECKS = [
+    check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
+    check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
+    check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,
+    check_planted_topics,
+]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    check(ko)
+
+
+# --------------------------------------------------------------------------
+# the generator itself
+# --------------------------------------------------------------------------
+
+
+def test_splitmix64_published_vector():
+    # SplitMix64 seeded with 0: the first three outputs of the reference
+    # generator (Steele, Lea & Flood 2014).
+    z = [synth._mix64_int(k * synth.GOLDEN) for k in (1, 2, 3)]
+    assert z == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    arr = synth.mix64(np.array([k * synth.GOLDEN & synth.MASK64 for k in (1, 2, 3)], dtype=np.uint64))
+    assert arr.tolist() == z
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = (np.random.default_rng(0).standard_normal(200000) * 37).astype(np.float32)
+    x[:4] = [1.00390625, 1.01171875, -1.00390625, 0.0]  # exact halfway cases: ties to even
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(synth.bf16_rne(x), want)
+
+
+def test_noise_moments_and_exactness():
+    n = synth.noise(synth.stream_key(9, 1), np.arange(400000, dtype=np.uint64))
+    assert abs(float(n.mean())) < 0.01 and abs(float(n.var()) - 1.0) < 0.01
+    assert np.all(np.abs(n) <= 6.0)
+    # every value is an exact multiple of 2^-16 (integer numerator, exact scale)
+    scaled = n.astype(np.float64) * 2.0**17
+    assert np.array_equal(scaled, np.round(scaled))
+
+
+def test_generator_layouts_hold_same_keys():
+    a = synth.qwen7b(L=2, H=3, D=8, bs=4, seq_lens=[9, 4], num_topics=3, seed=5)
+    b = synth.qwen7b(L=2, H=3, D=8, bs=4, seq_lens=[9, 4], num_topics=3, seed=5, layout="LPTHD")
+    ka = synth.view_paged(synth.gen_paged_numpy(a), a)
+    kb = synth.view_paged(synth.gen_paged_numpy(b), b)
+    np.testing.assert_array_equal(ka, kb)
+    # tails of partial blocks are NaN sentinels
+    tail = ka[:, a.pages[2], :, 1:, :]
+    assert np.all(tail == synth.BF16_NAN_BITS)
