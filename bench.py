@@ -1,0 +1,395 @@
+"""Benchmark of the Key-Key block selector hot path on one GB300 (or N replicas).
+
+One step = pool every block of the workload's paged K cache into v_b
+(kk_pool_blocks), then one decode step of the selector for every request
+(kk_select_step: anchor, scores, top-K). Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b]
+    python bench.py --impl reference   # the fp64 CPU oracle on a bounded sample
+
+Under torchrun (N > 1) each rank runs the same workload on its own GPU with
+its own requests (weak scaling, no collective on the data path); the step
+time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "K-pool HBM GB/s (vs ~8 TB/s); blocks scored/s; score+top-K µs/step"
+WORKLOADS = {
+    "tiny": synth.tiny_05b,
+    "7b": synth.qwen7b,
+    "7b-long": synth.qwen7b_long,
+    "write16": lambda: synth.write_stress(16),
+    "write128": lambda: synth.write_stress(128),
+}
+WORKLOAD_NAMES = {
+    "tiny": "0.5B-like paged K: L24 H2 D64 bs16 fp32, 1 x 4096 tokens, W8 K16",
+    "7b": "7B-like paged K: L28 H4 D128 bs128 bf16, 8 x 32768 tokens, W16 K32",
+    "7b-long": "7B-like long context: 32 x 131072 tokens, head-variance weighted, shuffled pages, W32 K64",
+    "write16": "write path: 2^20 tokens of 7B geometry at block size 16",
+    "write128": "write path: 2^20 tokens of 7B geometry at block size 128",
+}
+POOL_SRC = ["kv_cache_block_gb300/csrc/kk_pool.cu", "kv_cache_block_gb300/csrc/kk_device.cuh"]
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per pool launch from the committed ncu summary, if it was
+    taken on the current pool kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"pool_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"pool_source_hash:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != source_hash(POOL_SRC):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg (bounded sample)
+# --------------------------------------------------------------------------
+
+
+def oracle_sample(spec, budget_s: float):
+    """Time the fp64 oracle pooling whole blocks of ``spec`` (drawn with the
+    numpy generator) for about ``budget_s`` seconds, plus one selector step.
+    Returns (GB/s of K pooled, sample description, seconds)."""
+    from oracle import kk_oracle as ko
+
+    # a one-request cache of 4 blocks with the workload's geometry, pooled in turn
+    sub = synth.CacheSpec(name=spec.name + "-sample", L=spec.L, H=spec.H, D=spec.D, bs=spec.bs, dtype=spec.dtype,
+                          seq_lens=[spec.bs * 4], num_topics=spec.num_topics, scale=spec.scale, W=spec.W,
+                          K=spec.K, seed=spec.seed, sigma_range=spec.sigma_range)
+    kc = synth.view_paged(synth.gen_paged_numpy(sub), sub)
+    t0 = time.perf_counter()
+    done_bytes = 0
+    nblk = 0
+    vb = np.zeros((sub.num_pages, sub.D))
+    while True:
+        p = nblk % sub.total_blocks
+        w = None
+        if spec.weighted and nblk == 0:
+            w = ko.head_variance_weights(kc, sub.pages, sub.seq_lens[0], sub.bs)
+        vb[p] = ko.pool_blocks(kc, [p], [sub.n_valid[p]], None if w is None else [w], None if w is None else [0])[0]
+        done_bytes += int(sub.n_valid[p]) * sub.L * sub.H * sub.D * sub.elem_bytes
+        nblk += 1
+        if time.perf_counter() - t0 >= budget_s and nblk >= 4:
+            break
+    va = ko.anchor(kc, sub.pages, sub.seq_lens[0], sub.bs, sub.W)
+    ko.score_topk(vb, sub.pages, va, sub.K)
+    dt = time.perf_counter() - t0
+    desc = (f"{nblk} block poolings (4 distinct blocks in turn) of {spec.bs} tokens x {spec.L} layers x "
+            f"{spec.H} heads x {spec.D} dims, then one 4-block selector step; numpy, one thread")
+    return done_bytes / dt / 1e9, desc, dt
+
+
+# --------------------------------------------------------------------------
+# GPU leg
+# --------------------------------------------------------------------------
+
+
+def run_gpu(args, spec, rank, world, local_rank):
+    import torch
+
+    from kv_cache_block_gb300 import kk
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    storage = synth.gen_paged_cuda(spec, device=dev)
+    i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=dev)  # noqa: E731
+    pages, offsets, seq_lens, n_valid = i32(spec.pages), i32(spec.offsets), i32(spec.seq_lens), i32(spec.n_valid)
+    desc = kk.kcache_desc(storage, kk.KK_F32 if spec.dtype == "f32" else kk.KK_BF16, spec.L, spec.H, spec.D,
+                          spec.bs, spec.num_pages, spec.strides())
+    bt = kk.BlockTable(pages, offsets, seq_lens, max(spec.nb))
+    LH = spec.L * spec.H
+    vb = torch.zeros((spec.num_pages, spec.D), device=dev)
+    idx = torch.zeros((spec.R, spec.K), dtype=torch.int32, device=dev)
+    top = torch.zeros((spec.R, spec.K), device=dev)
+    head_w = torch.zeros((spec.R, LH), device=dev) if spec.weighted else None
+    ws = None
+    if spec.weighted:
+        ws = torch.empty(kk.kk_head_variance_workspace_bytes(desc, spec.total_blocks, spec.R), dtype=torch.uint8,
+                         device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def pool():
+        if spec.weighted:
+            kk.kk_pool_blocks_weighted(desc, bt, spec.total_blocks, head_w, vb, ws)
+        else:
+            kk.kk_pool_blocks(desc, pages, n_valid, vb)
+
+    def select():
+        kk.kk_select_step(desc, bt, spec.W, vb, spec.K, idx, top, head_w=head_w)
+
+    launches_per_step = (4 if spec.weighted else 1) + 1
+
+    for _ in range(max(args.warmup, 3)):
+        pool()
+        select()
+    torch.cuda.synchronize(dev)
+    if kk.kk_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            pool()
+            ev[i][1].record(stream)
+            select()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    pool_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    sel_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # select step alone, back to back (latency of one decode step of the selector)
+    for _ in range(5):
+        select()
+    torch.cuda.synchronize(dev)
+    n_sel = 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_sel):
+        select()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sel_back_to_back_us = e0.elapsed_time(e1) * 1e3 / n_sel
+    # and captured in a CUDA graph
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            select()
+            with torch.cuda.graph(g, stream=s2):
+                for _ in range(20):
+                    select()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = e0.elapsed_time(e1) * 1e3 / 200
+    except Exception as exc:  # noqa: BLE001
+        graph_us = None
+        print(f"cuda graph capture failed: {exc}", file=sys.stderr)
+    if kk.kk_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # end to end through the public API: K from pinned host memory, results back to the host
+    e2e = None
+    if not args.no_e2e:
+        pinned = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        host_k = pinned(storage)
+        host_k.copy_(storage)
+        host_vb, host_idx, host_top = pinned(vb), pinned(idx), pinned(top)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        torch.cuda.synchronize(dev)
+        t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0e.record(stream)
+        for _ in range(e2e_steps):
+            storage.copy_(host_k, non_blocking=True)
+            pool()
+            select()
+            host_vb.copy_(vb, non_blocking=True)
+            host_idx.copy_(idx, non_blocking=True)
+            host_top.copy_(top, non_blocking=True)
+        t1e.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = t0e.elapsed_time(t1e) / e2e_steps
+        h2d = storage.numel() * storage.element_size()
+        d2h = vb.numel() * 4 + idx.numel() * 4 + top.numel() * 4
+        e2e = {"value": spec.k_bytes() / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+        del host_k
+
+    return {
+        "pool_ms": statistics.mean(pool_ms), "select_ms": statistics.mean(sel_ms), "step_ms": statistics.mean(step_ms),
+        "total_ms": total_ms, "wall_s": t_wall, "sel_b2b_us": sel_back_to_back_us, "sel_graph_us": graph_us,
+        "clocks": clocks.summary(), "e2e": e2e, "launches": launches_per_step * args.steps,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="7b")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    spec = WORKLOADS[args.workload]()
+    cfg = {"workload": WORKLOAD_NAMES[args.workload], "requests": spec.R, "blocks": spec.total_blocks,
+           "k_bytes": spec.k_bytes(), "l2": "inputs larger than L2 (no flush needed)" if spec.k_bytes() > 256e6
+           else "inputs fit in L2 (warm)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        K = args.steps
+        vals = []
+        t_all = time.perf_counter()
+        for _ in range(K):
+            v, sample, dt = oracle_sample(spec, min(args.cpu_budget, 240.0 / max(1, K + args.warmup)))
+            vals.append((v, dt))
+        value = statistics.mean(v for v, _ in vals)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dt for _, dt in vals),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t_all}
+        print(json.dumps(line))
+        return
+
+    res = run_gpu(args, spec, rank, world, local_rank)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    kb = spec.k_bytes()
+    value = world * kb * args.steps / (res["total_ms"] * 1e-3) / 1e9
+    achieved = kb / (res["pool_ms"] * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    traffic = profiled_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["total_ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "kk_pool_blocks", "peak_source": peak_kind},
+        "blocks_scored_per_s": spec.total_blocks / (res["select_ms"] * 1e-3),
+        "score_topk_us_per_step": res["select_ms"] * 1e3,
+        "score_topk_us_back_to_back": res["sel_b2b_us"], "score_topk_us_cuda_graph": res["sel_graph_us"],
+        "pool_ms_per_step": res["pool_ms"], "clocks": res["clocks"], "gpu_launches": res["launches"],
+        "e2e": res["e2e"],
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        v, sample, dt = oracle_sample(spec, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                                "seconds": dt}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

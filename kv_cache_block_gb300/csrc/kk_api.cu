@@ -1,0 +1,302 @@
+// C ABI of the selector (include/kk.h): argument checks on the host, then
+// launches. Nothing here allocates device memory.
+#include <mutex>
+
+#include "../../include/kk.h"
+#include "kk_internal.h"
+
+namespace {
+
+__device__ int g_kk_error = 0;  // first device-side error since the last kk_device_error()
+
+// Device address of g_kk_error for the current device (looked up once per device).
+int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static std::mutex mu;
+  static int* ptr[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kk_error) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
+kk_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KK_OK : KK_ERR_CUDA; }
+
+bool dim_supported(int dtype, int D) {
+  if (D != 32 && D != 64 && D != 128 && D != 256) return false;
+  return !(dtype == KK_F32 && D == 256);
+}
+
+kk_status check_kcache(const kk_kcache_desc* kc, kk::KCache* out) {
+  if (!kc || !kc->base) return KK_ERR_INVALID;
+  if (kc->dtype != KK_F32 && kc->dtype != KK_BF16) return KK_ERR_INVALID;
+  if (kc->num_layers <= 0 || kc->num_kv_heads <= 0 || kc->head_dim <= 0 || kc->block_size <= 0 ||
+      kc->num_pages <= 0)
+    return KK_ERR_INVALID;
+  if ((long long)kc->num_layers * kc->num_kv_heads > kk::kMaxLH) return KK_ERR_UNSUPPORTED;
+  if (!dim_supported(kc->dtype, kc->head_dim)) return KK_ERR_UNSUPPORTED;
+  const long long es = kc->dtype == KK_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(kc->base) % 16) return KK_ERR_UNSUPPORTED;
+  const int64_t st[4] = {kc->stride_layer, kc->stride_page, kc->stride_head, kc->stride_token};
+  for (int i = 0; i < 4; ++i)
+    if (st[i] < 0 || (st[i] * es) % 16) return KK_ERR_UNSUPPORTED;
+  *out = kk::KCache{kc->base,       kc->dtype,          kc->num_layers,  kc->num_kv_heads,
+                    kc->head_dim,   kc->block_size,     kc->num_pages,   kc->stride_layer,
+                    kc->stride_page, kc->stride_head,   kc->stride_token};
+  return KK_OK;
+}
+
+kk_status check_table(const kk_block_table* bt, bool need_seq, kk::Table* out) {
+  if (!bt || bt->num_requests < 0 || bt->num_requests > 65535 || bt->max_blocks < 0)
+    return KK_ERR_INVALID;
+  if (bt->num_requests > 0 && (!bt->offsets || !bt->pages || (need_seq && !bt->seq_lens)))
+    return KK_ERR_INVALID;
+  *out = kk::Table{bt->pages, bt->offsets, bt->seq_lens, bt->num_requests, bt->max_blocks};
+  return KK_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct VarWorkspace {
+  float* S;
+  float* Q;
+  double* var;
+};
+
+size_t var_workspace_bytes(int LH, int D, long long total_blocks, int R) {
+  return align256(sizeof(float) * (size_t)total_blocks * LH * D) +
+         align256(sizeof(float) * (size_t)total_blocks * LH) + align256(sizeof(double) * (size_t)R * LH);
+}
+
+VarWorkspace carve(void* ws, int LH, int D, long long total_blocks) {
+  char* p = static_cast<char*>(ws);
+  VarWorkspace w;
+  w.S = reinterpret_cast<float*>(p);
+  p += align256(sizeof(float) * (size_t)total_blocks * LH * D);
+  w.Q = reinterpret_cast<float*>(p);
+  p += align256(sizeof(float) * (size_t)total_blocks * LH);
+  w.var = reinterpret_cast<double*>(p);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kk_status_str(kk_status s) {
+  switch (s) {
+    case KK_OK: return "ok";
+    case KK_ERR_INVALID: return "invalid argument";
+    case KK_ERR_UNSUPPORTED: return "unsupported layout or size";
+    case KK_ERR_CUDA: return "CUDA error";
+    case KK_ERR_BAD_INDEX: return "index out of range in device data";
+    case KK_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+kk_status kk_device_error(cudaStream_t stream, int32_t* code) {
+  if (!code) return KK_ERR_INVALID;
+  if (!error_word()) return KK_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KK_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_kk_error, sizeof(int)) != cudaSuccess) return KK_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_kk_error, &zero, sizeof(int)) != cudaSuccess) return KK_ERR_CUDA;
+  *code = v;
+  return KK_OK;
+}
+
+kk_status kk_pool_blocks(const kk_kcache_desc* kc, const int32_t* pages, const int32_t* n_valid,
+                         int32_t n, const float* head_w, int32_t n_sets, const int32_t* w_set,
+                         float* vb, cudaStream_t stream) {
+  kk::KCache c;
+  kk_status st = check_kcache(kc, &c);
+  if (st != KK_OK) return st;
+  if (n < 0) return KK_ERR_INVALID;
+  if (n == 0) return KK_OK;
+  if (!pages || !n_valid || !vb) return KK_ERR_INVALID;
+  if (head_w && (!w_set || n_sets <= 0)) return KK_ERR_INVALID;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_pool_direct(c, pages, n_valid, n, head_w, n_sets, w_set, vb, err, stream));
+}
+
+size_t kk_head_variance_workspace_bytes(const kk_kcache_desc* kc, int32_t total_blocks,
+                                        int32_t num_requests) {
+  if (!kc || total_blocks < 0 || num_requests < 0) return 0;
+  return var_workspace_bytes(kc->num_layers * kc->num_kv_heads, kc->head_dim, total_blocks,
+                             num_requests);
+}
+
+static kk_status variance_common(const kk_kcache_desc* kc, const kk_block_table* bt,
+                                 int32_t total_blocks, float* head_w_out, float* vb, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  kk::KCache c;
+  kk::Table t;
+  kk_status st = check_kcache(kc, &c);
+  if (st != KK_OK) return st;
+  if ((st = check_table(bt, true, &t)) != KK_OK) return st;
+  if (total_blocks < 0 || !head_w_out) return KK_ERR_INVALID;
+  if (t.R == 0) return KK_OK;
+  const int LH = c.L * c.H;
+  if (!ws || ws_bytes < var_workspace_bytes(LH, c.D, total_blocks, t.R)) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  VarWorkspace w = carve(ws, LH, c.D, total_blocks);
+  cudaError_t e = kk::launch_pool_slices(c, t, w.S, w.Q, err, stream);
+  if (e == cudaSuccess) e = kk::launch_head_var(c, t, w.S, w.Q, w.var, err, stream);
+  if (e == cudaSuccess) e = kk::launch_finalize_weights(c, t, w.var, head_w_out, stream);
+  if (e == cudaSuccess && vb) e = kk::launch_combine(c, t, w.S, head_w_out, vb, err, stream);
+  return from_cuda(e);
+}
+
+kk_status kk_head_variance(const kk_kcache_desc* kc, const kk_block_table* bt,
+                           int32_t total_blocks, float* head_w_out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  return variance_common(kc, bt, total_blocks, head_w_out, nullptr, workspace, workspace_bytes,
+                         stream);
+}
+
+kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table* bt,
+                                  int32_t total_blocks, float* head_w_out, float* vb,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!vb) return KK_ERR_INVALID;
+  return variance_common(kc, bt, total_blocks, head_w_out, vb, workspace, workspace_bytes, stream);
+}
+
+static kk_status step_common(kk::StepParams& p, cudaStream_t stream) {
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  p.err = err;
+  return from_cuda(kk::launch_step(p, stream));
+}
+
+kk_status kk_anchor(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                    const float* head_w, float* va, cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = check_kcache(kc, &p.kc);
+  if (st != KK_OK) return st;
+  if ((st = check_table(bt, true, &p.bt)) != KK_OK) return st;
+  if (W < 1 || W > kk::kMaxW || !va) return KK_ERR_INVALID;
+  p.W = W;
+  p.head_w = head_w;
+  p.va_out = va;
+  p.D = p.kc.D;
+  p.flags = kk::kStepAnchor;
+  return step_common(p, stream);
+}
+
+static kk_status score_args(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                            const float* va, kk::StepParams* p) {
+  kk_status st = check_table(bt, false, &p->bt);
+  if (st != KK_OK) return st;
+  if (!vb || !va || num_pages <= 0) return KK_ERR_INVALID;
+  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
+  p->vb = vb;
+  p->vb_rows = num_pages;
+  p->D = D;
+  p->va_in = va;
+  return KK_OK;
+}
+
+kk_status kk_score(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                   const float* va, float* scores, cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = score_args(vb, D, num_pages, bt, va, &p);
+  if (st != KK_OK) return st;
+  if (!scores) return KK_ERR_INVALID;
+  p.scores_out = scores;
+  p.flags = kk::kStepScore;
+  return step_common(p, stream);
+}
+
+kk_status kk_topk(const float* scores, const int32_t* offsets, int32_t R, int32_t max_n, int32_t K,
+                  int32_t* idx, float* top_scores, cudaStream_t stream) {
+  if (R < 0 || R > 65535 || max_n < 0 || K < 1 || K > kk::kMaxK) return KK_ERR_INVALID;
+  if (R == 0) return KK_OK;
+  if (!scores || !offsets || !idx) return KK_ERR_INVALID;
+  kk::StepParams p = {};
+  p.bt = kk::Table{nullptr, offsets, nullptr, R, max_n};
+  p.D = 128;
+  p.scores_in = scores;
+  p.K = K;
+  p.idx_out = idx;
+  p.top_out = top_scores;
+  p.flags = kk::kStepTopK | kk::kStepTopKFromScores;
+  return step_common(p, stream);
+}
+
+kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                        const float* va, int32_t K, int32_t* idx, float* top_scores, float* scores,
+                        cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = score_args(vb, D, num_pages, bt, va, &p);
+  if (st != KK_OK) return st;
+  if (K < 1 || K > kk::kMaxK || !idx) return KK_ERR_INVALID;
+  p.K = K;
+  p.idx_out = idx;
+  p.top_out = top_scores;
+  p.scores_out = scores;
+  p.flags = kk::kStepScore | kk::kStepTopK;
+  return step_common(p, stream);
+}
+
+kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                         const float* head_w, const float* vb, int32_t K, float* va, int32_t* idx,
+                         float* top_scores, float* scores, cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = check_kcache(kc, &p.kc);
+  if (st != KK_OK) return st;
+  if ((st = check_table(bt, true, &p.bt)) != KK_OK) return st;
+  if (W < 1 || W > kk::kMaxW || K < 1 || K > kk::kMaxK || !vb || !idx) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
+  p.W = W;
+  p.head_w = head_w;
+  p.va_out = va;
+  p.vb = vb;
+  p.vb_rows = p.kc.num_pages;
+  p.D = p.kc.D;
+  p.K = K;
+  p.idx_out = idx;
+  p.top_out = top_scores;
+  p.scores_out = scores;
+  p.flags = kk::kStepAnchor | kk::kStepScore | kk::kStepTopK;
+  return step_common(p, stream);
+}
+
+size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {
+  (void)R;
+  (void)N;
+  (void)K;
+  return 0;
+}
+
+kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,
+                                int32_t R, int32_t N, int32_t D, int32_t K, int32_t* idx,
+                                float* top_scores, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  (void)A; (void)V; (void)mask; (void)R; (void)N; (void)D; (void)K; (void)idx;
+  (void)top_scores; (void)workspace; (void)workspace_bytes; (void)stream;
+  return KK_ERR_UNSUPPORTED;
+}
+
+kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                          int32_t group, float* out, cudaStream_t stream) {
+  kk::Table t;
+  kk_status st = check_table(bt, false, &t);
+  if (st != KK_OK) return st;
+  if (!vb || !out || group < 1 || num_pages <= 0) return KK_ERR_INVALID;
+  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_coarse(vb, D, num_pages, t, group, out, err, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Host-side launch interface between the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kk {
+
+constexpr int kMaxLH = 1024;       // layers * KV heads
+constexpr int kMaxW = 1024;        // anchor tokens
+constexpr int kMaxK = 256;         // top-K
+constexpr int kMaxCluster = 16;    // CTAs per request in the step kernel
+constexpr int kMergeSlots = 2048;  // cluster size * K
+
+enum ErrorCode { kErrBadIndex = 4, kErrTimeout = 5 };
+
+struct KCache {
+  const void* base;
+  int dtype;  // 0 f32, 1 bf16
+  int L, H, D, bs, num_pages;
+  long long sL, sP, sH, sT;  // element strides
+};
+
+struct Table {
+  const int* pages;
+  const int* offsets;
+  const int* seq_lens;
+  int R, max_blocks;
+};
+
+// kk_pool.cu
+cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_valid, int n,
+                               const float* head_w, int n_sets, const int* w_set, float* vb,
+                               int* err, cudaStream_t s);
+cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, float* S, float* Q, int* err,
+                               cudaStream_t s);
+cudaError_t launch_head_var(const KCache& kc, const Table& bt, const float* S, const float* Q,
+                            double* var, int* err, cudaStream_t s);
+cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, const double* var,
+                                    float* head_w_out, cudaStream_t s);
+cudaError_t launch_combine(const KCache& kc, const Table& bt, const float* S, const float* head_w,
+                           float* vb, int* err, cudaStream_t s);
+
+// kk_step.cu
+enum StepFlags {
+  kStepAnchor = 1,           // pool the anchor from the K cache
+  kStepScore = 2,            // score blocks against the anchor
+  kStepTopK = 4,             // select the top K
+  kStepTopKFromScores = 8,   // keys come from a score array
+};
+
+struct StepParams {
+  KCache kc;
+  Table bt;
+  int W;
+  const float* head_w;  // [R][L*H] or null
+  const float* va_in;   // [R][D] or null
+  float* va_out;        // [R][D] or null
+  const float* vb;      // [vb_rows][D]
+  int vb_rows;
+  int D;
+  const float* scores_in;  // [offsets[R]] (top-K only mode)
+  float* scores_out;       // [offsets[R]] or null
+  int K;
+  int* idx_out;      // [R][K]
+  float* top_out;    // [R][K] or null
+  int flags;
+  int* err;
+};
+cudaError_t launch_step(const StepParams& p, cudaStream_t s);
+
+// kk_coarse.cu
+cudaError_t launch_coarse(const float* vb, int D, int num_pages, const Table& bt, int group,
+                          float* out, int* err, cudaStream_t s);
+
+}  // namespace kk

@@ -1,0 +1,159 @@
+"""The five workloads at full size, called exactly as bench.py calls them.
+The oracle checks sampled outputs it can compute one by one (sampled blocks,
+sampled requests, sampled coarse groups); properties that hold at any size
+(planted-topic ranking, reblocking) cover the rest."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import kk_oracle as ko
+from tests.helpers import DeviceCache, assert_scores_close, assert_topk_valid, assert_vec_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kk(cuda):
+    from kv_cache_block_gb300 import kk as mod
+
+    return mod
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _pool_all(kk, dev):
+    sp = dev.spec
+    vb = torch.zeros((sp.num_pages, sp.D), device="cuda")
+    kk.kk_pool_blocks(dev.desc, dev.pages, dev.n_valid, vb)
+    assert kk.kk_device_error() == 0
+    return vb
+
+
+def _check_sampled_blocks(dev, vb, blocks, head_w=None):
+    sp = dev.spec
+    pages = sp.pages[blocks]
+    kc = dev.host_pages(pages)
+    want = ko.pool_blocks(kc, np.arange(len(pages)), sp.n_valid[blocks],
+                          None if head_w is None else [head_w], None if head_w is None else [0] * len(pages))
+    assert_vec_close(vb.cpu().numpy()[pages], want, f"{sp.name} sampled vb")
+
+
+def _check_request_step(dev, r, va_gpu, scores_gpu, idx_gpu, top_gpu, K, head_w=None):
+    sp = dev.spec
+    kc_r, local = dev.host_request(r)
+    T = sp.seq_lens[r]
+    va_o = ko.anchor(kc_r, local, T, sp.bs, sp.W, head_w)
+    assert_vec_close(va_gpu, va_o, f"{sp.name} va r={r}")
+    nb = len(local)
+    w = None if head_w is None else [head_w]
+    vb_o = ko.pool_blocks(kc_r, local, sp.n_valid[sp.offsets[r]:sp.offsets[r + 1]], w,
+                          None if w is None else [0] * nb)
+    s_o = ko.affinity(vb_o, va_o)
+    assert_scores_close(scores_gpu, s_o, f"{sp.name} scores r={r}")
+    assert_topk_valid(idx_gpu, top_gpu, s_o, K, f"{sp.name} top-K r={r}")
+
+
+def _check_planted(dev, idx):
+    sp = dev.spec
+    for r in range(sp.R):
+        topic = sp.block_topic[sp.offsets[r]:sp.offsets[r + 1]]
+        same = set(np.flatnonzero(topic == sp.query_topic[r]).tolist())
+        m = min(sp.K, len(same))
+        assert set(idx[r][:m].tolist()) <= same, f"{sp.name} r={r}: planted topic not ranked first"
+
+
+def _step(kk, dev, vb, head_w=None):
+    sp = dev.spec
+    idx = torch.zeros((sp.R, sp.K), dtype=torch.int32, device="cuda")
+    top = torch.zeros((sp.R, sp.K), device="cuda")
+    va = torch.zeros((sp.R, sp.D), device="cuda")
+    scores = torch.zeros(sp.total_blocks, device="cuda")
+    kk.kk_select_step(dev.desc, dev.bt, sp.W, vb, sp.K, idx, top, va=va, scores=scores, head_w=head_w)
+    assert kk.kk_device_error() == 0
+    return idx.cpu().numpy(), top.cpu().numpy(), va.cpu().numpy(), scores.cpu().numpy()
+
+
+def test_tiny_05b_whole_path(kk):
+    dev = DeviceCache(synth.tiny_05b())
+    sp = dev.spec
+    vb = _pool_all(kk, dev)
+    kc = dev.host_view()
+    assert_vec_close(vb.cpu().numpy()[sp.pages], ko.pool_blocks(kc, sp.pages, sp.n_valid), "vb")
+    idx, top, va, scores = _step(kk, dev, vb)
+    _check_request_step(dev, 0, va[0], scores, idx[0], top[0], sp.K)
+    _check_planted(dev, idx)
+
+
+def test_qwen7b_full(kk):
+    dev = DeviceCache(synth.qwen7b())
+    sp = dev.spec
+    vb = _pool_all(kk, dev)
+    rng = np.random.default_rng(1)
+    _check_sampled_blocks(dev, vb, np.unique(np.concatenate([[0, sp.total_blocks - 1],
+                                                              rng.choice(sp.total_blocks, 30, replace=False)])))
+    idx, top, va, scores = _step(kk, dev, vb)
+    for r in (0, sp.R - 1):
+        _check_request_step(dev, r, va[r], scores[sp.offsets[r]:sp.offsets[r + 1]], idx[r], top[r], sp.K)
+    _check_planted(dev, idx)
+    del dev, vb
+    _free()
+
+
+def test_qwen7b_long_weighted_full(kk):
+    dev = DeviceCache(synth.qwen7b_long())
+    sp = dev.spec
+    LH = sp.L * sp.H
+    ws = torch.empty(kk.kk_head_variance_workspace_bytes(dev.desc, sp.total_blocks, sp.R), dtype=torch.uint8,
+                     device="cuda")
+    w_out = torch.zeros((sp.R, LH), device="cuda")
+    vb = torch.zeros((sp.num_pages, sp.D), device="cuda")
+    kk.kk_pool_blocks_weighted(dev.desc, dev.bt, sp.total_blocks, w_out, vb, ws)
+    assert kk.kk_device_error() == 0
+    del ws
+    _free()
+    idx, top, va, scores = _step(kk, dev, vb, head_w=w_out)
+    r = 5
+    kc_r, local = dev.host_request(r)
+    w_o = ko.head_variance_weights(kc_r, local, sp.seq_lens[r], sp.bs)
+    assert_vec_close(w_out.cpu().numpy()[r], w_o, "head weights")
+    del kc_r
+    _check_request_step(dev, r, va[r], scores[sp.offsets[r]:sp.offsets[r + 1]], idx[r], top[r], sp.K, w_o)
+    _check_planted(dev, idx)
+    del dev, vb
+    _free()
+
+
+@pytest.mark.parametrize("bs", [16, 128])
+def test_write_stress_pool_and_coarse(kk, bs):
+    dev = DeviceCache(synth.write_stress(bs))
+    sp = dev.spec
+    vb = _pool_all(kk, dev)
+    rng = np.random.default_rng(bs)
+    _check_sampled_blocks(dev, vb, np.unique(np.concatenate([[0, sp.total_blocks - 1],
+                                                              rng.choice(sp.total_blocks, 24, replace=False)])))
+    for group in (64, 512):
+        ng = (sp.nb[0] + group - 1) // group
+        out = torch.zeros((1, ng, sp.D), device="cuda")
+        kk.kk_coarse_means(vb, dev.bt, group, out)
+        assert kk.kk_device_error() == 0
+        g = int(rng.integers(0, ng))
+        blocks = np.arange(g * group, min((g + 1) * group, sp.nb[0]))
+        kc = dev.host_pages(sp.pages[blocks])
+        vb_o = ko.pool_blocks(kc, np.arange(len(blocks)), sp.n_valid[blocks])
+        assert_vec_close(out.cpu().numpy()[0, g], ko.coarse_means(vb_o, group)[0], f"coarse {group} g={g}")
+    if bs == 16:
+        # reblocking: eight 16-token blocks average to the 128-token block over the same tokens
+        test_write_stress_pool_and_coarse.vb16 = vb.cpu().numpy()
+    else:
+        vb16 = getattr(test_write_stress_pool_and_coarse, "vb16", None)
+        if vb16 is not None:
+            fine = vb16.reshape(-1, 8, sp.D).mean(axis=1)
+            assert_vec_close(fine, vb.cpu().numpy(), "reblocking 16 -> 128")
+    del dev, vb
+    _free()
