@@ -14,6 +14,7 @@ time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -159,11 +160,9 @@ def oracle_sample(spec, budget_s: float):
     done_bytes = 0
     nblk = 0
     vb = np.zeros((sub.num_pages, sub.D))
+    w = ko.head_variance_weights(kc, sub.pages, sub.seq_lens[0], sub.bs) if spec.weighted else None
     while True:
         p = nblk % sub.total_blocks
-        w = None
-        if spec.weighted and nblk == 0:
-            w = ko.head_variance_weights(kc, sub.pages, sub.seq_lens[0], sub.bs)
         vb[p] = ko.pool_blocks(kc, [p], [sub.n_valid[p]], None if w is None else [w], None if w is None else [0])[0]
         done_bytes += int(sub.n_valid[p]) * sub.L * sub.H * sub.D * sub.elem_bytes
         nblk += 1
@@ -336,9 +335,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--requests", type=int, default=0, help="override the number of requests (profiling runs)")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
     spec = WORKLOADS[args.workload]()
+    if args.requests:
+        spec = dataclasses.replace(spec, seq_lens=spec.seq_lens[:1] * args.requests)
     cfg = {"workload": WORKLOAD_NAMES[args.workload], "requests": spec.R, "blocks": spec.total_blocks,
            "k_bytes": spec.k_bytes(), "l2": "inputs larger than L2 (no flush needed)" if spec.k_bytes() > 256e6
            else "inputs fit in L2 (warm)"}
