@@ -97,17 +97,14 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {
   return x;
 }
 
-// Number of entries of a descending list of distinct keys that exceed `key`.
-__device__ __forceinline__ int count_greater(const uint64_t* list, int n, uint64_t key) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (list[mid] > key)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  return lo;
+// Number of entries greater than `key` (> 0) in a descending list of distinct
+// keys stored in `cap` slots (cap a power of two), unused slots holding 0.
+// Branch-free with a fixed number of steps, so searches in several lists can
+// be interleaved by the compiler instead of running as serial chains.
+__device__ __forceinline__ int count_greater_pow2(const uint64_t* list, int cap, uint64_t key) {
+  int pos = 0;
+  for (int step = cap >> 1; step > 0; step >>= 1) pos += (list[pos + step] > key) ? step : 0;
+  return (list[0] > key) ? pos + 1 : 0;
 }
 
 // ---- thread-block clusters (distributed shared memory) --------------------
@@ -148,5 +145,54 @@ __device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+// ---- mbarrier and bulk (TMA) copies --------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Makes an initialised mbarrier visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for phase `parity` of the barrier for at most `limit_ns` nanoseconds.
+// Returns false on timeout; never spins unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory; completes as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
 
 }  // namespace kk

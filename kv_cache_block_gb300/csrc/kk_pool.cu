@@ -69,20 +69,30 @@ __device__ __forceinline__ void slice_sum(const char* rowp, long long tok_bytes,
   }
 }
 
+// One CTA per block, or (direct mode) a cluster of S CTAs per block that
+// split the block's (layer, head) slices and sum their partial vectors in the
+// leader CTA through distributed shared memory; S > 1 only when there are too
+// few blocks to fill the GPU evenly.
 template <typename T, int D, bool kSlices>
 __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
   constexpr int EPV = Vec16<T>::kElems;
   constexpr int V16 = D / EPV;
   static_assert(V16 >= 1 && V16 <= 32 && (32 % V16) == 0, "row must be 16..512 bytes");
   constexpr int ES = elem_bytes<T>();
-  __shared__ float s_w[kMaxLH];
+  constexpr int kMaxSplit = 8;
+  __shared__ float s_w[kSlices ? 1 : kMaxLH];
   __shared__ float s_red[kWarps][D];
+  __shared__ float s_part[kSlices ? 1 : kMaxSplit][D];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int vec = lane % V16, tl = lane / V16;
   const int LH = a.L * a.H;
+  const int S = kSlices ? 1 : (int)cluster_size();
+  const int crank = S > 1 ? (int)cluster_rank() : 0;
+  if (S > 1) cluster_arrive_relaxed();
 
-  int page, n, g = 0, wsel = 0;
+  int page = 0, n = 0, g = 0, wsel = 0;
+  bool valid = true;
   if (kSlices) {
     const int r = blockIdx.y, j = blockIdx.x;
     const int off = a.offsets[r];
@@ -96,21 +106,22 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
     g = off + j;
     page = a.bt_pages[g];
     n = min(a.bs, T_r - j * a.bs);
-  } else {
-    page = a.pages[blockIdx.x];
-    n = a.n_valid[blockIdx.x];
-    if (a.head_w && a.w_set) wsel = a.w_set[blockIdx.x];
-    if (n < 0 || n > a.bs || (a.head_w && (wsel < 0 || wsel >= a.n_sets))) {
+    if (page < 0 || page >= a.num_pages) {
       if (threadIdx.x == 0) flag_error(a.err, kErrBadIndex);
       return;
     }
-  }
-  if (page < 0 || page >= a.num_pages) {
-    if (threadIdx.x == 0) flag_error(a.err, kErrBadIndex);
-    return;
-  }
-
-  if (!kSlices) {
+  } else {
+    const int i = blockIdx.x / S;
+    page = a.pages[i];
+    n = a.n_valid[i];
+    if (a.head_w && a.w_set) wsel = a.w_set[i];
+    valid = !(n < 0 || n > a.bs || page < 0 || page >= a.num_pages ||
+              (a.head_w && (wsel < 0 || wsel >= a.n_sets)));
+    if (!valid) {
+      if (threadIdx.x == 0 && crank == 0) flag_error(a.err, kErrBadIndex);
+      n = 0;
+      page = 0;
+    }
     for (int s = threadIdx.x; s < LH; s += kThreads)
       s_w[s] = a.head_w ? a.head_w[(long long)wsel * LH + s] : 1.f;
     __syncthreads();
@@ -122,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
 #pragma unroll
   for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
 
-  for (int s = warp; s < LH; s += kWarps) {
+  for (int s = crank + S * warp; s < LH; s += S * kWarps) {
     const int l = s / a.H, h = s - l * a.H;
     const char* rowp = page_base + ((long long)l * a.sL + (long long)h * a.sH) * ES;
     float ps[EPV], q;
@@ -158,12 +169,43 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
     for (int e = 0; e < EPV; ++e) s_red[warp][vec * EPV + e] = acc[e];
   }
   __syncthreads();
-  const float scale = (n == 0) ? 0.f : (a.head_w ? 1.f / (float)n : 1.f / ((float)n * (float)LH));
-  for (int d = threadIdx.x; d < D; d += kThreads) {
-    float v = 0.f;
+  float part[(D + kThreads - 1) / kThreads];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) v += s_red[w][d];
-    a.vb[(long long)page * D + d] = v * scale;
+  for (int k = 0; k < (D + kThreads - 1) / kThreads; ++k) {
+    const int d = threadIdx.x + k * kThreads;
+    float v = 0.f;
+    if (d < D) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += s_red[w][d];
+    }
+    part[k] = v;
+  }
+  if (S > 1) {
+    cluster_wait_acquire();  // every CTA of the cluster has started
+#pragma unroll
+    for (int k = 0; k < (D + kThreads - 1) / kThreads; ++k) {
+      const int d = threadIdx.x + k * kThreads;
+      if (d < D) st_cluster_f32(map_to_rank(smem_u32(&s_part[crank][d]), 0), part[k]);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (crank != 0) return;
+#pragma unroll
+    for (int k = 0; k < (D + kThreads - 1) / kThreads; ++k) {
+      const int d = threadIdx.x + k * kThreads;
+      if (d < D) {
+        float v = 0.f;
+        for (int q = 0; q < S; ++q) v += s_part[q][d];
+        part[k] = v;
+      }
+    }
+  }
+  if (!valid) return;
+  const float scale = (n == 0) ? 0.f : (a.head_w ? 1.f / (float)n : 1.f / ((float)n * (float)LH));
+#pragma unroll
+  for (int k = 0; k < (D + kThreads - 1) / kThreads; ++k) {
+    const int d = threadIdx.x + k * kThreads;
+    if (d < D) a.vb[(long long)page * D + d] = part[k] * scale;
   }
 }
 
@@ -259,13 +301,26 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* S, const
   }
 }
 
+template <typename T, int D, bool kSlices>
+cudaError_t launch_pool(const PoolArgs& a, dim3 grid, int split, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pool_kernel<T, D, kSlices>, a);
+}
+
 template <bool kSlices>
-cudaError_t dispatch_pool(const KCache& kc, const PoolArgs& a, dim3 grid, cudaStream_t s) {
-#define KK_POOL_CASE(TT, DD)                                                  \
-  if (kc.D == DD) {                                                           \
-    pool_kernel<TT, DD, kSlices><<<grid, kThreads, 0, s>>>(a);                \
-    return cudaGetLastError();                                                \
-  }
+cudaError_t dispatch_pool(const KCache& kc, const PoolArgs& a, dim3 grid, int split, cudaStream_t s) {
+#define KK_POOL_CASE(TT, DD) \
+  if (kc.D == DD) return launch_pool<TT, DD, kSlices>(a, grid, split, s);
   if (kc.dtype == 1) {
     KK_POOL_CASE(bf16_t, 32)
     KK_POOL_CASE(bf16_t, 64)
@@ -308,7 +363,11 @@ cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_
   a.n_sets = n_sets;
   a.w_set = w_set;
   a.vb = vb;
-  return dispatch_pool<false>(kc, a, dim3(n), s);
+  // Split each block over a cluster of 2 CTAs only when there are too few
+  // blocks to fill the GPU (fewer than 1024); measured on GB300, larger
+  // clusters or splits of many blocks lose bandwidth to cluster scheduling.
+  const int split = (n < 1024 && kc.L * kc.H >= 16) ? 2 : 1;
+  return dispatch_pool<false>(kc, a, dim3((unsigned)n * split), split, s);
 }
 
 cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, float* S, float* Q, int* err,
@@ -321,7 +380,7 @@ cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, float* S, floa
   a.max_blocks = bt.max_blocks;
   a.S = S;
   a.Q = Q;
-  return dispatch_pool<true>(kc, a, dim3(bt.max_blocks, bt.R), s);
+  return dispatch_pool<true>(kc, a, dim3(bt.max_blocks, bt.R), 1, s);
 }
 
 cudaError_t launch_head_var(const KCache& kc, const Table& bt, const float* S, const float* Q,

@@ -4,10 +4,13 @@
 // §3.2), and keep the top K (§5.2 step 4).
 //
 // A request is served by one thread-block cluster of CL CTAs. The CTAs split
-// the anchor's (layer, head) slices and the request's blocks; partial anchors
-// and partial top-K lists travel through distributed shared memory, so a whole
-// step is one launch with no global scratch. Every stage can be switched off,
-// which gives kk_anchor, kk_score, kk_topk and kk_score_topk from the same code.
+// the anchor's (layer, head) slices and the request's blocks. A CTA starts by
+// bulk-copying (TMA) the v_b rows of its blocks into shared memory, so that
+// gather overlaps the anchor. Partial anchors, and each CTA's sorted top-K
+// list, are exchanged through distributed shared memory; every CTA then ranks
+// its own candidates in the union and writes them. A whole step is one launch
+// with no global scratch. Every stage can be switched off, which gives
+// kk_anchor, kk_score, kk_topk and kk_score_topk from the same code.
 #include <mutex>
 
 #include "kk_device.cuh"
@@ -20,9 +23,11 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kThreads;  // candidates per top-K tile
 constexpr int kUnroll = 8;
+constexpr int kStage = 64;  // v_b rows staged in shared memory by bulk copies
 
 template <int D>
 struct StepSmem {
+  float stage[kStage][D];      // v_b rows of the CTA's first blocks (bulk copies)
   float part[kMaxCluster][D];  // anchor partial of each CTA of the cluster
   float wpart[kWarps][D];
   float va[D];
@@ -35,33 +40,31 @@ struct StepSmem {
   uint64_t run[2][kMaxK];
   uint64_t merge[kMergeSlots];
   int mcount[kMaxCluster];
+  uint64_t bar;  // completion of the staged bulk copies
 };
 
-// D floats per row: each lane holds D/32 of them.
+// D floats per row: each lane holds D/32 of them (plain loads: the row may be
+// in global or shared memory).
 template <int D>
 struct RowSlice {
   static constexpr int kPer = D / 32;
   float v[kPer];
   __device__ __forceinline__ void load(const float* row, int lane) {
-    const float* p = row + lane * kPer;
+    const float* q = row + lane * kPer;
     if (kPer == 8) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+      const float4 a = reinterpret_cast<const float4*>(q)[0];
+      const float4 b = reinterpret_cast<const float4*>(q)[1];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
       v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else if (kPer == 4) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+      const float4 a = reinterpret_cast<const float4*>(q)[0];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     } else if (kPer == 2) {
-      const float2 a = __ldg(reinterpret_cast<const float2*>(p));
+      const float2 a = reinterpret_cast<const float2*>(q)[0];
       v[0] = a.x; v[1] = a.y;
     } else {
-      v[0] = __ldg(p);
+      v[0] = q[0];
     }
-  }
-  __device__ __forceinline__ void load_shared(const float* row, int lane) {
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) v[e] = row[lane * kPer + e];
   }
   __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -76,8 +79,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   StepSmem<D>& sm = *reinterpret_cast<StepSmem<D>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,6 +92,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
   const bool do_topk = p.flags & kStepTopK;
   const bool from_scores = p.flags & kStepTopKFromScores;
   const int K = p.K;
+  const int Kp = K <= 1 ? 1 : 1 << (32 - __clz(K - 1));  // next power of two >= K
 
   // The first remote shared-memory access must follow a cluster barrier that
   // every CTA has arrived at; arrive now, wait just before that access.
@@ -113,17 +117,16 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
     nb = 0;
     T_r = 0;
   }
+  const int chunk = (nb + CL - 1) / CL;
+  const int j0 = min(nb, crank * chunk);
+  const int j1 = min(nb, j0 + chunk);
 
-  // ---- stage 1: anchor -----------------------------------------------------
+  // ---- prefetch: one round of page-id loads for the anchor's token rows and
+  // the first tile's blocks, then bulk copies of that tile's v_b rows -------
   constexpr bool kAnchorFits = D <= 32 * Vec16<T>::kElems;  // a row is at most 32 vectors
+  const int w_eff = min(p.W, T_r);
   if (kAnchorFits && do_anchor) {
-    constexpr int EPV = Vec16<T>::kElems;
-    constexpr int V16 = kAnchorFits ? D / EPV : 32;
-    constexpr int RPW = 32 / V16;
     constexpr int ES = elem_bytes<T>();
-    const int vec = lane % V16, tl = lane / V16;
-    const int LH = p.kc.L * p.kc.H;
-    const int w_eff = min(p.W, T_r);
     for (int i = tid; i < w_eff; i += kThreads) {
       const int pos = T_r - w_eff + i;
       const int pgid = p.bt.pages[off + pos / p.kc.bs];
@@ -135,8 +138,47 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
       }
     }
     if (p.head_w)
-      for (int s = tid; s < LH; s += kThreads) sm.w[s] = p.head_w[(long long)r * LH + s];
-    __syncthreads();
+      for (int s = tid; s < p.kc.L * p.kc.H; s += kThreads)
+        sm.w[s] = p.head_w[(long long)r * p.kc.L * p.kc.H + s];
+  }
+  const int nstage = do_score ? min(kStage, j1 - j0) : 0;
+  if (do_score) {
+    const int t0count = min(kTile, j1 - j0);
+    int pg = -1;
+    if (tid < t0count) {
+      pg = p.bt.pages[off + j0 + tid];
+      if (pg < 0 || pg >= p.vb_rows) {
+        flag_error(p.err, kErrBadIndex);
+        pg = -1;
+      }
+    }
+    sm.pg[tid] = pg;
+    if (tid == 0) {
+      mbar_init(&sm.bar, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (do_score) {
+    if (warp == 0 && nstage > 0) {
+      int valid = 0;
+      for (int i = lane; i < nstage; i += 32) valid += sm.pg[i] >= 0;
+      valid = __reduce_add_sync(kFull, valid);
+      if (lane == 0) mbar_arrive_expect_tx(&sm.bar, (uint32_t)(valid * D * sizeof(float)));
+      __syncwarp();
+      for (int i = lane; i < nstage; i += 32)
+        if (sm.pg[i] >= 0) bulk_g2s(&sm.stage[i][0], p.vb + (long long)sm.pg[i] * D, D * sizeof(float), &sm.bar);
+    }
+  }
+
+  // ---- stage 1: anchor -----------------------------------------------------
+  if (kAnchorFits && do_anchor) {
+    constexpr int EPV = Vec16<T>::kElems;
+    constexpr int V16 = kAnchorFits ? D / EPV : 32;
+    constexpr int RPW = 32 / V16;
+    constexpr int ES = elem_bytes<T>();
+    const int vec = lane % V16, tl = lane / V16;
+    const int LH = p.kc.L * p.kc.H;
 
     float acc[EPV];
 #pragma unroll
@@ -211,25 +253,31 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
   }
 
   // ---- stage 2: scores and the CTA's top-K over its share of the blocks --
+  // Running top-K list: sm.run[cur][0..Kp), descending, zero-padded.
   int run_n = 0, cur = 0;
+  if (do_topk)
+    for (int i = tid; i < Kp; i += kThreads) sm.run[0][i] = 0ull;
   if (do_score || from_scores) {
-    const int chunk = (nb + CL - 1) / CL;
-    const int j0 = min(nb, crank * chunk);
-    const int j1 = min(nb, j0 + chunk);
     RowSlice<D> a;
     float na2 = 0.f;
+    bool staged_ok = true;
     if (do_score) {
-      a.load_shared(sm.va, lane);
+      a.load(sm.va, lane);
       float t = 0.f;
 #pragma unroll
       for (int e = 0; e < RowSlice<D>::kPer; ++e) t = fmaf(a.v[e], a.v[e], t);
       na2 = warp_sum(t);
+      if (nstage > 0 && !mbar_wait_bounded(&sm.bar, 0, kWaitLimitNs)) {
+        staged_ok = false;
+        if (tid == 0) flag_error(p.err, kErrTimeout);
+      }
     }
     const float na = sqrtf(na2);
     for (int tile0 = j0; tile0 < j1; tile0 += kTile) {
       const int tcount = min(kTile, j1 - tile0);
+      const bool first = tile0 == j0;
       if (do_score) {
-        {
+        if (!first) {
           int pg = -1;
           if (tid < tcount) {
             pg = p.bt.pages[off + tile0 + tid];
@@ -239,22 +287,25 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
             }
           }
           sm.pg[tid] = pg;
+          __syncthreads();
         }
-        __syncthreads();
-        // warp w scores tile slots [32w, 32w + 32)
-        for (int i0 = 0; i0 < 32; i0 += kUnroll) {
+        // warp w scores tile slots w, w + 8, w + 16, ...; kUnroll rows in flight
+        for (int base = warp; base < tcount; base += kWarps * kUnroll) {
           RowSlice<D> b[kUnroll];
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u) {
-            const int pg = sm.pg[warp * 32 + i0 + u];
-            if (pg >= 0)
-              b[u].load(p.vb + (long long)pg * D, lane);
-            else
-              b[u].zero();
+            // always load (row 0 for empty slots, masked below): no branch, so
+            // all kUnroll rows are in flight together
+            const int slot = base + u * kWarps;
+            const int pg = slot < tcount ? sm.pg[slot] : -1;
+            const bool staged = first && slot < nstage;
+            const float* row = (staged || pg < 0) ? &sm.stage[staged ? slot : 0][0] : p.vb + (long long)pg * D;
+            b[u].load(row, lane);
+            if (pg < 0 || (staged && !staged_ok)) b[u].zero();
           }
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u) {
-            const int slot = warp * 32 + i0 + u;
+            const int slot = base + u * kWarps;
             float dot = 0.f, n2 = 0.f;
 #pragma unroll
             for (int e = 0; e < RowSlice<D>::kPer; ++e) {
@@ -263,18 +314,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
             }
             dot = warp_sum(dot);
             n2 = warp_sum(n2);
-            if (lane == 0) {
-              uint64_t key = 0;
-              if (slot < tcount) {
-                float cosv = 0.f;
-                if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
-                cosv = fminf(1.f, fmaxf(-1.f, cosv));
-                const float sc = fmaf(0.5f, cosv, 0.5f);
-                const int j = tile0 + slot;
-                if (p.scores_out) p.scores_out[off + j] = sc;
-                if (sm.pg[slot] >= 0) key = make_key(sc, (uint32_t)j);
-              }
-              sm.keys[slot] = key;
+            if (lane == 0 && slot < tcount) {
+              float cosv = 0.f;
+              if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
+              cosv = fminf(1.f, fmaxf(-1.f, cosv));
+              const float sc = fmaf(0.5f, cosv, 0.5f);
+              const int j = tile0 + slot;
+              if (p.scores_out) p.scores_out[off + j] = sc;
+              sm.keys[slot] = sm.pg[slot] >= 0 ? make_key(sc, (uint32_t)j) : 0ull;
             }
           }
         }
@@ -282,13 +329,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
         const int j = tile0 + tid;
         sm.keys[tid] = (tid < tcount) ? make_key(p.scores_in[off + j], (uint32_t)j) : 0ull;
       }
-      if (!do_topk) {
-        __syncthreads();
-        continue;
-      }
       __syncthreads();
-      // merge this tile into the running top-K list (sorted, descending)
-      uint64_t key = sm.keys[tid];
+      if (!do_topk) continue;
+      // merge this tile into the running list
+      uint64_t key = tid < tcount ? sm.keys[tid] : 0ull;
       const uint64_t thr = (run_n == K) ? sm.run[cur][K - 1] : 0ull;
       if (key <= thr) key = 0ull;
       if (!__syncthreads_or(key != 0ull)) continue;
@@ -296,20 +340,35 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
       sm.wl[warp][lane] = key;
       const int cnt = __popc(__ballot_sync(kFull, key != 0ull));
       if (lane == 0) sm.wn[warp] = cnt;
-      __syncthreads();
       const int nxt = cur ^ 1;
+      for (int i = tid; i < Kp; i += kThreads) sm.run[nxt][i] = 0ull;
+      __syncthreads();
+      // rank in the union = number of larger keys in every list (own list included)
       if (key != 0ull) {
-        int rank = lane + count_greater(sm.run[cur], run_n, key);
+        int pos[kWarps];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-          if (w != warp) rank += count_greater(sm.wl[w], sm.wn[w], key);
+        for (int w = 0; w < kWarps; ++w) pos[w] = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1)
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) pos[w] += (sm.wl[w][pos[w] + step] > key) ? step : 0;
+        int rank = count_greater_pow2(sm.run[cur], Kp, key);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) rank += (sm.wl[w][0] > key) ? pos[w] + 1 : 0;
         if (rank < K) sm.run[nxt][rank] = key;
       }
       if (tid < run_n) {
         const uint64_t x = sm.run[cur][tid];
+        int pos[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) pos[w] = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1)
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) pos[w] += (sm.wl[w][pos[w] + step] > x) ? step : 0;
         int rank = tid;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) rank += count_greater(sm.wl[w], sm.wn[w], x);
+        for (int w = 0; w < kWarps; ++w) rank += (sm.wl[w][0] > x) ? pos[w] + 1 : 0;
         if (rank < K) sm.run[nxt][rank] = x;
       }
       int total = run_n;
@@ -337,26 +396,32 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
         cluster_wait_acquire();
         start_waited = true;
       }
-      for (int i = tid; i < run_n; i += kThreads)
-        st_cluster_u64(map_to_rank(smem_u32(&sm.merge[crank * K + i]), 0), sm.run[cur][i]);
-      if (tid == 0) st_cluster_s32(map_to_rank(smem_u32(&sm.mcount[crank]), 0), run_n);
+      // all-gather: every CTA receives every CTA's zero-padded sorted list
+      for (int f = tid; f < CL * Kp; f += kThreads) {
+        const int dst = f / Kp, i = f - dst * Kp;
+        st_cluster_u64(map_to_rank(smem_u32(&sm.merge[crank * Kp + i]), dst), sm.run[cur][i]);
+      }
+      if (tid < CL) st_cluster_s32(map_to_rank(smem_u32(&sm.mcount[crank]), tid), run_n);
       cluster_arrive_release();
       cluster_wait_acquire();
+      // Each CTA ranks its own candidates in the union: a group of CL lanes
+      // per candidate, one lane per list, counts summed with shuffles.
+      const int list = lane & (CL - 1);
+      const int per_warp = 32 / CL;
+      for (int c0 = warp * per_warp; c0 < run_n; c0 += kWarps * per_warp) {
+        const int c = c0 + lane / CL;
+        const bool have = c < run_n;
+        const uint64_t k = have ? sm.merge[crank * Kp + c] : ~0ull;
+        int cnt = count_greater_pow2(&sm.merge[list * Kp], Kp, k);
+        for (int o = 1; o < CL; o <<= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+        if (have && list == 0 && cnt < K) {
+          idx_out[cnt] = (int)key_index(k);
+          if (top_out) top_out[cnt] = key_score(k);
+        }
+      }
       if (crank == 0) {
         int total = 0;
         for (int q = 0; q < CL; ++q) total += sm.mcount[q];
-        for (int f = tid; f < CL * K; f += kThreads) {
-          const int q = f / K, i = f - q * K;
-          if (i >= sm.mcount[q]) continue;
-          const uint64_t k = sm.merge[q * K + i];
-          int rank = i;
-          for (int o = 0; o < CL; ++o)
-            if (o != q) rank += count_greater(&sm.merge[o * K], sm.mcount[o], k);
-          if (rank < K) {
-            idx_out[rank] = (int)key_index(k);
-            if (top_out) top_out[rank] = key_score(k);
-          }
-        }
         for (int i = total + tid; i < K; i += kThreads) {
           idx_out[i] = -1;
           if (top_out) top_out[i] = -__int_as_float(0x7f800000);
@@ -370,23 +435,28 @@ __global__ void __launch_bounds__(kThreads) step_kernel(StepParams p) {
 // Per-device launch setup of one instantiation: dynamic shared memory above
 // 48 KB, non-portable cluster sizes, and the largest cluster size (<= 16)
 // that the occupancy calculator says can be co-scheduled.
+struct ClusterCaps {
+  int active[kMaxCluster + 1];  // co-resident clusters of each size (0 = cannot launch)
+};
+
 template <typename T, int D>
-cudaError_t setup_device(int* max_cluster) {
+cudaError_t setup_device(ClusterCaps* caps) {
   static std::mutex mu;
-  static int cached[64] = {};  // 0 = not set up yet
+  static bool ready[64] = {};
+  static ClusterCaps cached[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cached[dev]) {
+  if (!ready[dev]) {
     const int smem = (int)sizeof(StepSmem<D>);
     e = cudaFuncSetAttribute(step_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(step_kernel<T, D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    int best = 1;
-    for (int cl = kMaxCluster; cl > 1; cl >>= 1) {
+    ClusterCaps c = {};
+    for (int cl = 1; cl <= kMaxCluster; cl <<= 1) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cl, 1);
       cfg.blockDim = dim3(kThreads);
@@ -399,24 +469,40 @@ cudaError_t setup_device(int* max_cluster) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, step_kernel<T, D>, &cfg) == cudaSuccess && n > 0) {
-        best = cl;
-        break;
-      }
-      (void)cudaGetLastError();  // clear a sticky-free error from an unsupported size
+      if (cudaOccupancyMaxActiveClusters(&n, step_kernel<T, D>, &cfg) != cudaSuccess) n = 0;
+      (void)cudaGetLastError();  // an unsupported size is not an error here
+      c.active[cl] = n;
     }
-    cached[dev] = best;
+    cached[dev] = c;
+    ready[dev] = true;
   }
-  *max_cluster = cached[dev];
+  *caps = cached[dev];
   return cudaSuccess;
 }
 
+// CTAs per request: the largest cluster size (<= 16) at which all R
+// requests' clusters are resident at once, limited by the merge buffer
+// (CL * K) and by the work (at least 16 blocks per CTA); with more requests
+// than that, single-CTA requests.
+int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
+  const int per_cta_min = 16;
+  const int Kp = p.K <= 1 ? 1 : 1 << (32 - __builtin_clz(p.K - 1));
+  int best = 1;
+  for (int cl = 2; cl <= kMaxCluster; cl <<= 1) {
+    if (caps.active[cl] < p.bt.R) break;
+    if (cl * Kp > kMergeSlots / 2) break;
+    if ((long long)cl * per_cta_min > (long long)p.bt.max_blocks + per_cta_min) break;
+    best = cl;
+  }
+  return best;
+}
+
 template <typename T, int D>
-cudaError_t launch_typed(const StepParams& p, int CL, cudaStream_t s) {
-  int max_cl = 1;
-  cudaError_t e = setup_device<T, D>(&max_cl);
+cudaError_t launch_typed(const StepParams& p, cudaStream_t s) {
+  ClusterCaps caps;
+  cudaError_t e = setup_device<T, D>(&caps);
   if (e != cudaSuccess) return e;
-  while (CL > max_cl) CL >>= 1;
+  const int CL = pick_cluster(p, caps);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, p.bt.R);
   cfg.blockDim = dim3(kThreads);
@@ -432,25 +518,13 @@ cudaError_t launch_typed(const StepParams& p, int CL, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, step_kernel<T, D>, p);
 }
 
-// CTAs per request: enough CTAs to cover the GPU's 152 SMs about twice,
-// at most 16, and no more than the merge buffer (CL * K) or the work allows.
-int pick_cluster(const StepParams& p) {
-  int CL = 1;
-  const int per_cta_min = 16;  // blocks scored by a CTA, at least
-  while (CL < kMaxCluster && (long long)p.bt.R * CL < 2 * 152 && 2 * CL * p.K <= kMergeSlots &&
-         (long long)2 * CL * per_cta_min <= (long long)p.bt.max_blocks + per_cta_min)
-    CL *= 2;
-  return CL;
-}
-
 }  // namespace
 
 cudaError_t launch_step(const StepParams& p, cudaStream_t s) {
   if (p.bt.R == 0) return cudaSuccess;
-  const int CL = pick_cluster(p);
   const bool bf16 = (p.flags & kStepAnchor) && p.kc.dtype == 1;
-#define KK_STEP_CASE(DD)                                                          \
-  if (p.D == DD) return bf16 ? launch_typed<bf16_t, DD>(p, CL, s) : launch_typed<float, DD>(p, CL, s);
+#define KK_STEP_CASE(DD) \
+  if (p.D == DD) return bf16 ? launch_typed<bf16_t, DD>(p, s) : launch_typed<float, DD>(p, s);
   KK_STEP_CASE(32)
   KK_STEP_CASE(64)
   KK_STEP_CASE(128)
