@@ -129,6 +129,30 @@ kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table
                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Allocation-free form of kk_pool_blocks_weighted (the page describes no such
+ * variant; it exists for callers). Some callers cannot call cudaMalloc: a
+ * serving engine that reserves nearly all device memory for its paged KV cache
+ * at start-up and hands none out afterwards, or a plugin running inside such
+ * an engine's write path, where an allocation would fail or stall the device.
+ * This entry point takes only the inputs and outputs of
+ * kk_pool_blocks_weighted and keeps its scratch in a 32 MiB array that the
+ * library owns on each GPU that loads it (held until the process exits).
+ * - The scratch needed is kk_head_variance_workspace_bytes(kc, total_blocks,
+ *   R); above 32 MiB the call returns KK_ERR_UNSUPPORTED and launches nothing.
+ * - It allocates nothing: no cudaMalloc or cudaFree, no allocating library
+ *   call. The first call on a device looks up the array's device address (and
+ *   the error word's); make that first call before any stream capture.
+ * - Every call shares the one array. Calls that overlap on the GPU (on two
+ *   streams, or from two threads) race on it and give wrong results; order
+ *   them on one stream. Nothing needs clearing between calls: each call
+ *   writes every scratch byte before reading it.
+ * Results are the same as kk_pool_blocks_weighted's.
+ */
+kk_status kk_pool_blocks_weighted_static(const kk_kcache_desc* kc, const kk_block_table* bt,
+                                         int32_t total_blocks, float* head_w_out, float* vb,
+                                         cudaStream_t stream);
+
+/*
  * kk_anchor - query anchor [KK §2.2 step 2], [KK §5.2 step 1]:
  *   va[r][d] = sum_{l,h} w[l,h] * (1/W') * sum_{T-W' <= p < T} K[l, page(p), h, p % bs, d]
  * with T = seq_lens[r], W' = min(W, T), page(p) = pages[offsets[r] + p / bs],

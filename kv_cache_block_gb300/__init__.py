@@ -9,7 +9,7 @@ import importlib
 
 _BINDING = (
     "BlockTable", "KKError", "kcache_desc", "kk_anchor", "kk_coarse_means", "kk_device_error",
-    "kk_head_variance", "kk_head_variance_workspace_bytes", "kk_pool_blocks", "kk_pool_blocks_weighted",
+    "kk_head_variance", "kk_head_variance_workspace_bytes", "kk_pool_blocks", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static",
     "kk_score", "kk_score_pool_batched", "kk_score_pool_batched_workspace_bytes", "kk_score_topk",
     "kk_select_step", "kk_topk",
 )

@@ -300,3 +300,21 @@ kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const k
 }
 
 }  // extern "C"
+
+// Internal helpers for the allocation-free weighted pool (kk_static.cu): the
+// same argument checks as kk_pool_blocks_weighted, and the device error word.
+namespace kk {
+
+kk_status check_weighted_args(const kk_kcache_desc* kc, const kk_block_table* bt,
+                              int32_t total_blocks, const float* head_w_out, const float* vb,
+                              KCache* c, Table* t) {
+  kk_status st = check_kcache(kc, c);
+  if (st != KK_OK) return st;
+  if ((st = check_table(bt, true, t)) != KK_OK) return st;
+  if (total_blocks < 0 || !head_w_out || !vb) return KK_ERR_INVALID;
+  return KK_OK;
+}
+
+int* device_error_word() { return error_word(); }
+
+}  // namespace kk

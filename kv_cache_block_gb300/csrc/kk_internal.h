@@ -68,6 +68,9 @@ struct StepParams {
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 
+// kk_api.cu (used by kk_static.cu)
+int* device_error_word();
+
 // kk_coarse.cu
 cudaError_t launch_coarse(const float* vb, int D, int num_pages, const Table& bt, int group,
                           float* out, int* err, cudaStream_t s);

@@ -67,6 +67,7 @@ def _load():
         "kk_head_variance_workspace_bytes": (SZ, [KC, I32, I32]),
         "kk_head_variance": (ctypes.c_int, [KC, BT, I32, P, P, SZ, P]),
         "kk_pool_blocks_weighted": (ctypes.c_int, [KC, BT, I32, P, P, P, SZ, P]),
+        "kk_pool_blocks_weighted_static": (ctypes.c_int, [KC, BT, I32, P, P, P]),
         "kk_anchor": (ctypes.c_int, [KC, BT, I32, P, P, P]),
         "kk_score": (ctypes.c_int, [P, I32, I32, BT, P, P, P]),
         "kk_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
@@ -89,7 +90,7 @@ _lib = _load()
 #: the C entry points declared in include/kk.h
 EXPORTS = (
     "kk_status_str", "kk_device_error", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
-    "kk_head_variance", "kk_pool_blocks_weighted", "kk_anchor", "kk_score", "kk_topk",
+    "kk_head_variance", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static", "kk_anchor", "kk_score", "kk_topk",
     "kk_score_topk", "kk_select_step", "kk_score_pool_batched_workspace_bytes",
     "kk_score_pool_batched", "kk_coarse_means",
 )
@@ -186,6 +187,14 @@ def kk_pool_blocks_weighted(kc, bt: BlockTable, total_blocks: int, head_w_out, v
         ctypes.byref(kc), ctypes.byref(bt.c), total_blocks, _ptr(head_w_out, torch.float32, "head_w_out"),
         _ptr(vb, torch.float32, "vb"), _ptr(workspace, name="workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kk_pool_blocks_weighted_static(kc, bt: BlockTable, total_blocks: int, head_w_out, vb, stream=None):
+    """kk_pool_blocks_weighted without a workspace argument: for callers that
+    cannot allocate device memory (scratch is a 32 MiB array the library owns)."""
+    _check("kk_pool_blocks_weighted_static", _lib.kk_pool_blocks_weighted_static(
+        ctypes.byref(kc), ctypes.byref(bt.c), total_blocks, _ptr(head_w_out, torch.float32, "head_w_out"),
+        _ptr(vb, torch.float32, "vb"), _stream(stream)))
 
 
 def kk_anchor(kc, bt: BlockTable, W: int, va, head_w=None, stream=None):
