@@ -272,19 +272,27 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
 }
 
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {
-  (void)R;
-  (void)N;
   (void)K;
-  return 0;
+  if (R < 0 || N < 0) return 0;
+  return kk::batched_workspace_bytes(R, N);
 }
 
 kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,
                                 int32_t R, int32_t N, int32_t D, int32_t K, int32_t* idx,
                                 float* top_scores, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
-  (void)A; (void)V; (void)mask; (void)R; (void)N; (void)D; (void)K; (void)idx;
-  (void)top_scores; (void)workspace; (void)workspace_bytes; (void)stream;
-  return KK_ERR_UNSUPPORTED;
+  if (R < 0 || N < 0 || K < 1 || K > kk::kMaxK) return KK_ERR_INVALID;
+  if (R == 0) return KK_OK;
+  if (D != 128) return KK_ERR_UNSUPPORTED;
+  if (!idx || !workspace || (N > 0 && (!A || !V || !mask))) return KK_ERR_INVALID;
+  if (workspace_bytes < kk::batched_workspace_bytes(R, N)) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(V) % 16 ||
+      reinterpret_cast<uintptr_t>(workspace) % 256)
+    return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_score_pool_batched(A, V, mask, R, N, K, idx, top_scores, workspace,
+                                                 err, stream));
 }
 
 kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,

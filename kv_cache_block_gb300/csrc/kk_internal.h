@@ -68,6 +68,12 @@ struct StepParams {
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 
+// kk_batched.cu
+size_t batched_workspace_bytes(int R, int N);
+cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask, int R,
+                                      int N, int K, int* idx, float* top, void* ws, int* err,
+                                      cudaStream_t s);
+
 // kk_api.cu (used by kk_static.cu)
 int* device_error_word();
 

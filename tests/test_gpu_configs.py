@@ -157,3 +157,30 @@ def test_write_stress_pool_and_coarse(kk, bs):
             assert_vec_close(fine, vb.cpu().numpy(), "reblocking 16 -> 128")
     del dev, vb
     _free()
+
+
+def test_shared_pool_full(kk):
+    from tests.test_gpu_parity import check_batched_against_oracle
+
+    v_spec, a_spec, mask, K = synth.shared_pool()
+    V = synth.gen_rows_cuda(v_spec)
+    A = synth.gen_rows_cuda(a_spec)
+    R, N = A.shape[0], V.shape[0]
+    Mt = torch.from_numpy(mask.view(np.int32)).cuda()
+    ws = torch.empty(kk.kk_score_pool_batched_workspace_bytes(R, N, K), dtype=torch.uint8, device="cuda")
+    idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    top = torch.zeros((R, K), device="cuda")
+    kk.kk_score_pool_batched(A, V, Mt, K, idx, top, ws)
+    assert kk.kk_device_error() == 0
+    A_h = A.cpu().numpy().view(np.uint16)
+    V_h = V.cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(A_h, synth.gen_rows_numpy(a_spec))  # generator bits, GPU == numpy
+    idx_h, top_h = idx.cpu().numpy(), top.cpu().numpy()
+    check_batched_against_oracle(A_h, V_h, mask, K, idx_h, top_h)
+    # planted topics: the owned blocks of the anchor's topic come first
+    j = np.arange(N)
+    for r in range(R):
+        owned = np.flatnonzero((mask[r, j // 32] >> (j % 32).astype(np.uint32)) & 1)
+        same = set(owned[v_spec.topics[owned] == a_spec.topics[r]].tolist())
+        m = min(K, len(same))
+        assert set(idx_h[r][:m].tolist()) <= same, f"row {r}"

@@ -269,3 +269,43 @@ def test_bad_indices_are_reported_not_faulted(kk):
     # and the library stays usable
     kk.kk_pool_blocks(dev.desc, dev.pages, dev.n_valid, vb)
     assert kk.kk_device_error() == 0
+
+
+def _pool_inputs(R, N, owned, seed):
+    v = synth.RowsSpec(N=N, D=128, num_topics=8, scale=1.5, sigma=0.05, seed=seed, stream=2, dtype="bf16")
+    a = synth.RowsSpec(N=R, D=128, num_topics=8, scale=1.5, sigma=0.15, seed=seed, stream=3, dtype="bf16",
+                       centroid_seed=seed)
+    return synth.gen_rows_numpy(a), synth.gen_rows_numpy(v), synth.owned_mask(R, N, owned, seed + 1)
+
+
+def check_batched_against_oracle(A, V, mask, K, idx, top, rows=None):
+    R, N = A.shape[0], V.shape[0]
+    j = np.arange(N)
+    for r in (range(R) if rows is None else rows):
+        owned = np.flatnonzero((mask[r, j // 32] >> (j % 32).astype(np.uint32)) & 1)
+        s_o = ko.affinity(V[owned], A[r])
+        pos = {int(b): p for p, b in enumerate(owned)}
+        g = idx[r]
+        assert all(int(b) in pos for b in g if b >= 0), f"row {r}: picked a block it does not own"
+        g_pos = np.array([pos[int(b)] if b >= 0 else -1 for b in g])
+        assert_topk_valid(g_pos, top[r], s_o, K, f"batched row {r}")
+
+
+@pytest.mark.parametrize("R,N,K,owned", [(5, 300, 7, 40), (130, 1000, 16, 300), (3, 129, 256, 129),
+                                         (1, 64, 1, 0), (200, 4096, 128, 1024), (129, 257, 33, 250)])
+def test_score_pool_batched_small(kk, R, N, K, owned):
+    A, V, mask = _pool_inputs(R, N, owned, seed=R + N)
+    At = torch.from_numpy(A.view(np.int16)).cuda()
+    Vt = torch.from_numpy(V.view(np.int16)).cuda()
+    Mt = torch.from_numpy(mask.view(np.int32)).cuda()
+    ws = torch.empty(kk.kk_score_pool_batched_workspace_bytes(R, N, K), dtype=torch.uint8, device="cuda")
+    results = []
+    for _ in range(2):  # a second call must not see the first call's candidate lists
+        idx = torch.full((R, K), 7, dtype=torch.int32, device="cuda")
+        top = torch.zeros((R, K), device="cuda")
+        kk.kk_score_pool_batched(At, Vt, Mt, K, idx, top, ws)
+        assert kk.kk_device_error() == 0
+        results.append((idx.cpu().numpy(), top.cpu().numpy()))
+    np.testing.assert_array_equal(results[0][0], results[1][0])
+    np.testing.assert_array_equal(results[0][1], results[1][1])
+    check_batched_against_oracle(A, V, mask, K, *results[0])
