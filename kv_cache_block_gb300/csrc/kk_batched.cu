@@ -3,11 +3,11 @@
 // masked): R anchors against N pooled block vectors, each anchor restricted to
 // the blocks its mask marks, top K per anchor.
 //
-// Kernel 1 is a tcgen05 GEMM tile: TMA loads a 128-anchor x 128-dim tile of A
-// and a 128-block tile of V into shared memory (128-byte swizzle), one thread
-// issues eight 128x128x16 bf16 MMAs into a TMEM fp32 accumulator, and four
-// epilogue warps read it back (tcgen05.ld), divide by the norms (computed from
-// the same shared-memory tiles), apply the ownership mask and write each
+// Kernel 1 is a persistent tcgen05 GEMM: TMA streams 128-block tiles of V
+// (128-byte swizzle) past a resident 128-anchor tile of A, one thread issues
+// eight 128x128x16 bf16 MMAs per tile into one of two TMEM fp32 accumulators,
+// and four epilogue warps read them back (tcgen05.ld), divide by the norms
+// (computed from the same shared-memory tiles), apply the ownership mask and write each
 // owned candidate as a 64-bit key (score, pool id) into the anchor's segment
 // for this tile, with the segment's count (no atomics: one writer each).
 // Kernel 2 selects each anchor's top K from its list by radix select over the
@@ -15,6 +15,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kk_device.cuh"
@@ -27,10 +28,15 @@ namespace {
 constexpr int kBM = 128;  // anchors per tile
 constexpr int kBN = 128;  // pool blocks per tile
 constexpr int kD = 128;   // head_dim (two 64-element swizzle boxes)
-constexpr int kBoxBytes = 128 * 128;  // 128 rows x 128 bytes
-constexpr int kGemmThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr uint32_t kTmemCols = 128;
-constexpr int kGemmSmem = 4 * kBoxBytes + 2 * 128 * 4 + 64 + 1024;  // tiles, norms, barriers, alignment
+constexpr int kBoxBytes = 128 * 128;   // 128 rows x 128 bytes
+constexpr int kTileBytes = 2 * kBoxBytes;
+constexpr int kStages = 4;             // V tiles in flight
+constexpr int kEpiWarps = 8;           // two per TMEM lane quarter, 64 columns each
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kGemmThreads = 64 + kEpiThreads;  // warp 0 TMA, warp 1 MMA, then the epilogue
+constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
+constexpr int kStageFloats = kEpiWarps * 32 * 33;  // per-lane 32-column dump, padded
+constexpr int kGemmSmem = kTileBytes * (1 + kStages) + kStageFloats * 4 + 8 * 128 * 4 + 256 + 1024;
 
 struct GemmArgs {
   const uint32_t* mask;
@@ -40,27 +46,56 @@ struct GemmArgs {
   int* err;
 };
 
+// Persistent, warp-specialised: CTA c owns M-tile (c % MT) of the anchors and
+// N-tiles p, p + P, p + 2P, ... (p = c / MT, P = CTAs per M-tile). Warp 0
+// streams V tiles through a kStages-deep TMA ring; warp 1 issues the MMAs of
+// tile j into TMEM accumulator j % 2; eight epilogue warps take the V-row
+// norms from the ring (then release the stage) and drain the other
+// accumulator, so the epilogue of tile j overlaps the loads and MMAs of tile
+// j + 1. Each epilogue warp drains 64 columns of its 32 TMEM lanes (anchors)
+// without branches: every column's score is formed in registers and only
+// owned columns are stored, at slots given by a popcount prefix of the mask.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     score_pool_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmV,
                       GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sA = base;                   // two boxes of A: dims 0-63, 64-127
-  unsigned char* sV = base + 2 * kBoxBytes;   // two boxes of V
-  float* s_na = reinterpret_cast<float*>(base + 4 * kBoxBytes);
-  float* s_nv = s_na + 128;
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(s_nv + 128);
-  uint64_t* bar_mma = bar_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  unsigned char* sA = base;               // A tile: two boxes (dims 0-63, 64-127)
+  unsigned char* sV = base + kTileBytes;  // kStages V tiles
+  float* s_dump = reinterpret_cast<float*>(base + kTileBytes * (1 + kStages));  // [warp][lane][33]
+  float* s_part = s_dump + kStageFloats;  // [2 halves][128] sums of squares
+  float* s_inv_a = s_part + 256;          // [128] 1 / ||A row||
+  float* s_inv_v = s_inv_a + 128;         // [2 buffers][128] 1 / ||V row||
+  float* s_part_a = s_inv_v + 256;        // [2 halves][128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(s_part_a + 256);
+  uint64_t* bar_a = bar;                         // A tile landed
+  uint64_t* full = bar + 1;                      // [kStages] V tile landed
+  uint64_t* empty = full + kStages;              // [kStages] V tile released (MMA + epilogue warps)
+  uint64_t* acc_full = empty + kStages;          // [2] accumulator ready
+  uint64_t* acc_empty = acc_full + 2;            // [2] accumulator drained (epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+  const int MT = (g.R + kBM - 1) / kBM;
+  const int P = max(1, (int)gridDim.x / MT);
+  const int m = blockIdx.x % MT, p = blockIdx.x / MT;
+  if (p >= P) return;
+  const int ntiles = p < g.tiles ? (g.tiles - p + P - 1) / P : 0;
+  if (ntiles == 0) return;
+  const int m0 = m * kBM;
 
   if (tid == 0) {
-    mbar_init(bar_full, 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(bar_a, 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1 + kEpiWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -72,118 +107,192 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  volatile int* abort_flag = s_abort;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    flag_error(g.err, code);
+  };
 
-  if (warp == 0 && lane == 0) {
-    mbar_arrive_expect_tx(bar_full, 4 * kBoxBytes);
-    tma_load_2d(sA, &tmA, 0, m0, bar_full);
-    tma_load_2d(sA + kBoxBytes, &tmA, 64, m0, bar_full);
-    tma_load_2d(sV, &tmV, 0, n0, bar_full);
-    tma_load_2d(sV + kBoxBytes, &tmV, 64, n0, bar_full);
-  } else if (warp == 1 && lane == 0) {
-    if (mbar_wait_bounded(bar_full, 0, kWaitLimitNs)) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-      const uint32_t a0 = smem_u32(sA), v0 = smem_u32(sV);
-#pragma unroll
-      for (int k = 0; k < kD / 16; ++k) {
-        const uint32_t off = (uint32_t)((k >> 2) * kBoxBytes + (k & 3) * 32);
-        mma_bf16(tmem, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(v0 + off), idesc, k > 0);
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_a, kTileBytes);
+      tma_load_2d(sA, &tmA, 0, m0, bar_a);
+      tma_load_2d(sA + kBoxBytes, &tmA, 64, m0, bar_a);
+      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !mbar_wait_bounded(&empty[st], ((j / kStages) & 1) ^ 1, kWaitLimitNs)) {
+          fail(kErrTimeout);
+          break;
+        }
+        const int n0 = (p + j * P) * kBN;
+        unsigned char* dst = sV + st * kTileBytes;
+        mbar_arrive_expect_tx(&full[st], kTileBytes);
+        tma_load_2d(dst, &tmV, 0, n0, &full[st]);
+        tma_load_2d(dst + kBoxBytes, &tmV, 64, n0, &full[st]);
       }
-      mma_commit(bar_mma);
-    } else {
-      atomicExch(s_abort, 1);
-      flag_error(g.err, kErrTimeout);
-      mbar_arrive(bar_mma);  // release the epilogue
     }
-  } else if (warp >= 2) {
-    const int e = tid - 64;  // 0..127: norm row, then TMEM lane owner below
-    const int q4 = warp & 3;            // TMEM lane quarter of this warp
-    const int row = q4 * 32 + lane;     // anchor row within the tile
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      if (!mbar_wait_bounded(bar_a, 0, kWaitLimitNs)) fail(kErrTimeout);
+      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+        const int st = j % kStages, b = j & 1;
+        if (!mbar_wait_bounded(&full[st], (j / kStages) & 1, kWaitLimitNs) ||
+            (j >= 2 && !mbar_wait_bounded(&acc_empty[b], ((j >> 1) & 1) ^ 1, kWaitLimitNs))) {
+          fail(kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA), v0 = smem_u32(sV + st * kTileBytes);
+        const uint32_t d = tmem + (uint32_t)(b * kBN);
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * kBoxBytes + (k & 3) * 32);
+          mma_bf16(d, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(v0 + off), idesc, k > 0);
+        }
+        mma_commit(&empty[st]);
+        mma_commit(&acc_full[b]);
+      }
+    }
+  } else {
+    const int ew = warp - 2;             // epilogue warp 0..7
+    const int half = ew >> 2;            // which 64 columns this warp drains
+    const int q4 = warp & 3;             // TMEM lane quarter of this warp
+    const int row = q4 * 32 + lane;      // anchor row (TMEM lane) this thread drains
     const int r = m0 + row;
-    // Ownership bits of this anchor's 128 columns (limited to columns < N)
-    // and the row's write offset, both independent of the tiles: fetched
-    // first so their latency hides behind the loads and the MMAs.
-    uint32_t w[4];
-    int total = 0;
+    const int nrow = ew * 32 + lane;     // norm work item: row nrow & 127, half nrow >> 7
+    const int nr = nrow & 127, nh = nrow >> 7;
+    // half of the squared norm of a 128-dim bf16 row stored as two 128-byte
+    // swizzled rows: box `nh`, eight 16-byte chunks (rotated by lane to spread
+    // banks; the order of a sum of squares does not matter)
+    auto half_sq = [&](const unsigned char* tile) {
+      float acc = 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int wi = n0 / 32 + c;
-      uint32_t x = 0;
-      if (r < g.R && wi < g.mask_words) x = g.mask[(long long)r * g.mask_words + wi];
-      const int lim = g.N - wi * 32;  // valid columns in this word
-      if (lim < 32) x &= lim <= 0 ? 0u : ((1u << lim) - 1u);
-      w[c] = x;
-      total += __popc(x);
-    }
-    if (r < g.R) g.counts[(long long)r * g.tiles + blockIdx.x] = total;
-    if (mbar_wait_bounded(bar_full, 0, kWaitLimitNs)) {
-      // squared norms of A row e and V row e (16-byte chunks rotated by lane
-      // to spread banks; the order of a sum of squares does not matter)
-      float na = 0.f, nv = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int cc = (c + lane) & 15;
-        const int off = (cc >> 3) * kBoxBytes + e * 128 + (cc & 7) * 16;
-        const uint4 a = *reinterpret_cast<const uint4*>(sA + off);
-        const uint4 v = *reinterpret_cast<const uint4*>(sV + off);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, vw[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 8; ++c) {
+        const int cc = (c + lane) & 7;
+        const uint4 x = *reinterpret_cast<const uint4*>(tile + nh * kBoxBytes + nr * 128 + cc * 16);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float a_lo = bf16_lo(aw[q]), a_hi = bf16_hi(aw[q]);
-          const float v_lo = bf16_lo(vw[q]), v_hi = bf16_hi(vw[q]);
-          na = fmaf(a_lo, a_lo, fmaf(a_hi, a_hi, na));
-          nv = fmaf(v_lo, v_lo, fmaf(v_hi, v_hi, nv));
+          const float lo = bf16_lo(xw[q]), hi = bf16_hi(xw[q]);
+          acc = fmaf(lo, lo, fmaf(hi, hi, acc));
         }
       }
-      s_na[e] = sqrtf(na);
-      s_nv[e] = sqrtf(nv);
-    } else {
-      atomicExch(s_abort, 1);
-      flag_error(g.err, kErrTimeout);
-    }
-    named_sync(1, 128);
-    bool mma_ok = mbar_wait_bounded(bar_mma, 0, kWaitLimitNs);
-    if (!mma_ok) flag_error(g.err, kErrTimeout);
-    // tcgen05.ld is warp-collective: the whole warp takes one decision
-    mma_ok = __all_sync(kFull, mma_ok && *s_abort == 0);
-    tc_fence_after();
-    if (mma_ok) {
-      uint64_t* out = g.cand + ((long long)r * g.tiles + blockIdx.x) * kBN;
-      int k = 0;
-      const float na = s_na[row];
-      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16);
-      // The MMAs have consumed the V tile, so its shared memory stages each
-      // lane's 32 accumulator columns; only the owned columns are then visited
-      // (mask bits are sparse), by index into shared memory.
-      // 4 warps x 32 lanes x 33 floats = 16.9 KB of the 32 KB V tile; each lane
-      // writes and reads only its own row, so no synchronisation is needed
-      float* stage = reinterpret_cast<float*>(sV) + ((warp - 2) * 32 + lane) * 33;
-      uint32_t acc[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, acc[c]);  // whole warp, one wait
-      tmem_wait_ld();
+      return acc;
+    };
+    auto inv_norm = [](float sq) { return sq > 0.f ? 1.f / sqrtf(sq) : 0.f; };
+    bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
+    if (!ok) fail(kErrTimeout);
+    s_part_a[nh * 128 + nr] = ok ? half_sq(sA) : 0.f;
+    named_sync(1, kEpiThreads);
+    if (nrow < 128) s_inv_a[nrow] = inv_norm(s_part_a[nrow] + s_part_a[128 + nrow]);
+    named_sync(1, kEpiThreads);
+    const float inv_a = s_inv_a[row];
+    // ownership bits of this anchor's 128 columns of tile jj (limited to
+    // columns < N); fetched two tiles ahead so their latency stays hidden
+    auto mask_words = [&](int jj, uint32_t (&w)[4]) {
+      const int n0 = (p + jj * P) * kBN;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const int wi = n0 / 32 + c;
+        uint32_t x = 0;
+        if (jj < ntiles && r < g.R && wi < g.mask_words) x = g.mask[(long long)r * g.mask_words + wi];
+        w[c] = x;
+      }
+    };
+    auto limit_cols = [&](int n0, uint32_t (&w)[4]) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) stage[i] = __uint_as_float(acc[c][i]);
-        uint32_t x = w[c];
+      for (int c = 0; c < 4; ++c) {
+        const int lim = g.N - (n0 / 32 + c) * 32;
+        if (lim < 32) w[c] &= lim <= 0 ? 0u : ((1u << lim) - 1u);
+      }
+    };
+    uint32_t w_next[4], w_after[4];
+    mask_words(0, w_next);
+    mask_words(1, w_after);
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kStages, b = j & 1;
+      const int tile = p + j * P, n0 = tile * kBN;
+      uint32_t w[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        w[c] = w_next[c];
+        w_next[c] = w_after[c];
+      }
+      mask_words(j + 2, w_after);
+      limit_cols(n0, w);
+      // V-row norms of this tile, then release the ring stage. The epilogue
+      // warps leave the loop together (a lone warp leaving would strand the
+      // others at the named barrier).
+      ok = !*abort_flag && mbar_wait_bounded(&full[st], (j / kStages) & 1, kWaitLimitNs);
+      s_part[nh * 128 + nr] = ok ? half_sq(sV + st * kTileBytes) : 0.f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      if (named_sync_or(1, kEpiThreads, !ok)) {
+        if (!ok) fail(kErrTimeout);
+        break;
+      }
+      if (nrow < 128) s_inv_v[b * 128 + nrow] = inv_norm(s_part[nrow] + s_part[128 + nrow]);
+      ok = mbar_wait_bounded(&acc_full[b], (j >> 1) & 1, kWaitLimitNs);
+      if (named_sync_or(1, kEpiThreads, !ok)) {  // tcgen05.ld below is warp-collective too
+        if (!ok) fail(kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      uint32_t acc[2][32];
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(b * kBN + half * 64);
+      tmem_ld32(taddr, acc[0]);
+      tmem_ld32(taddr + 32, acc[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);  // the accumulator may be reused
+      if (r < g.R && half == 0)
+        g.counts[(long long)r * g.tiles + tile] = __popc(w[0]) + __popc(w[1]) + __popc(w[2]) + __popc(w[3]);
+      uint64_t* out = g.cand + ((long long)r * g.tiles + tile) * kBN;
+      int k = half ? __popc(w[0]) + __popc(w[1]) : 0;
+      const float* inv_v = s_inv_v + b * 128 + half * 64;
+      // Owned columns are sparse: dump the 32 accumulators of a chunk to this
+      // lane's shared-memory row (stride 33: no bank conflicts) and visit only
+      // the set mask bits.
+      float* dump = s_dump + (ew * 32 + lane) * 33;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dump[i] = __uint_as_float(acc[c][i]);
+        uint32_t x = half ? w[2 + c] : w[c];
+        // the first four owned columns as independent slots (they overlap),
+        // then the rare remainder one by one
+        int ib[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ib[u] = x ? __ffs(x) - 1 : -1;
+          x &= x - 1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (ib[u] >= 0) {
+            const int i = ib[u];
+            float cosv = dump[i] * inv_a * inv_v[c * 32 + i];
+            cosv = fminf(1.f, fmaxf(-1.f, cosv));
+            out[k + u] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + half * 64 + c * 32 + i));
+          }
+        }
+        k += (ib[0] >= 0) + (ib[1] >= 0) + (ib[2] >= 0) + (ib[3] >= 0);
         while (x) {
           const int i = __ffs(x) - 1;
           x &= x - 1;
-          const int col = c * 32 + i;
-          const float nv = s_nv[col];
-          float cosv = (na > 0.f && nv > 0.f) ? stage[i] / (na * nv) : 0.f;
+          float cosv = dump[i] * inv_a * inv_v[c * 32 + i];
           cosv = fminf(1.f, fmaxf(-1.f, cosv));
-          out[k++] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + col));
+          out[k++] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + half * 64 + c * 32 + i));
         }
       }
     }
   }
 
-  // teardown: nothing may still read TMEM or wait on copies
+  // teardown: every role has left its loop; no MMA or TMEM read is pending
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *s_abort) (void)mbar_wait_bounded(bar_full, 0, kWaitLimitNs);  // copies in flight
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -209,7 +318,7 @@ __device__ __forceinline__ void for_each_key(bool staged, int n, const uint64_t*
     }
   } else {
     for (int t = warp; t < tiles; t += kSelThreads / 32) {
-      const int c = cnt[t];
+      const int c = min(max(cnt[t], 0), kBN);
       for (int j0 = 0; j0 < c; j0 += 32) {
         const int j = j0 + lane;
         const bool active = j < c;
@@ -517,6 +626,14 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
+  return n;
+}
+
 cudaError_t setup_gemm() {
   static std::mutex mu;
   static bool ready[64] = {};
@@ -557,12 +674,14 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
     CUtensorMap ma, mv;
     if (!make_map(&ma, A, R) || !make_map(&mv, V, N)) return cudaErrorInvalidValue;
     GemmArgs g{mask, R, N, (N + 31) / 32, tiles, counts, cand, err};
-    dim3 grid(tiles, (R + kBM - 1) / kBM);
-    score_pool_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
+    // one CTA per SM, split evenly across the M-tiles of the anchors
+    const int MT = (R + kBM - 1) / kBM;
+    const int P = std::max(1, std::min(tiles, sm_count() / MT));
+    score_pool_kernel<<<MT * P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  select_rows_kernel<<<R, kSelThreads, sizeof(uint64_t) * kSelStage, s>>>(cand, counts, tiles, K, idx, top,
-                                                                          err);
+  select_rows_kernel<<<R, kSelThreads, sizeof(uint64_t) * kSelStage, s>>>(cand, counts, tiles, K, idx,
+                                                                          top, err);
   return cudaGetLastError();
 }
 
