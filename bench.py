@@ -56,6 +56,32 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_spec(spec, rank: int):
+    """The shard of one rank under weak scaling: the workload's geometry and
+    sizes, with requests of its own (every input drawn from a seed offset by
+    the rank). Rank 0 keeps the workload's own seed."""
+    return spec if rank == 0 else dataclasses.replace(spec, seed=spec.seed + 7919 * rank)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of ``x`` over the ranks of the default process group (``x``
+    itself without one)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(units_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processed ``units_per_rank`` per step;
+    the job took the slowest rank's ``max_ms`` for ``steps`` steps."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -87,34 +113,45 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms. The sampler
+    is started (first sample seen) before the caller's timed region; only the
+    samples taken inside the window passed to ``window`` are summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (perf_counter seconds, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            deadline = time.perf_counter() + 5.0
+            while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
 
     def __exit__(self, *exc):
         if self.proc:
+            time.sleep(2.0 * self.PERIOD_MS / 1e3)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -122,24 +159,37 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) != 6:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[2:]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.lines, self.t0, self.t1)
+
+
+def summarize_clocks(lines, t0=None, t1=None):
+    """Median SM clock, max clock and throttle reasons of the samples taken in
+    [t0, t1] (all samples when no window is given). When the window is shorter
+    than the sampling period and holds none, the first sample after it is
+    used and ``in_window`` says so."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    parsed = []
+    for t, line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) != 6:
+            continue
+        try:
+            sm, mx = float(parts[0]), float(parts[1])
+        except ValueError:
+            continue
+        parsed.append((t, sm, mx, [n for n, v in zip(names, parts[2:]) if v.lower() == "active"]))
+    in_window = True
+    sel = parsed
+    if t0 is not None and t1 is not None:
+        sel = [x for x in parsed if t0 <= x[0] <= t1]
+        if not sel:
+            in_window = False
+            sel = [x for x in parsed if x[0] > t1][:1]
+    if not sel:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    reasons = sorted({n for x in sel for n in x[3]})
+    return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+            "reasons": reasons, "samples": len(sel), "in_window": in_window}
 
 
 # --------------------------------------------------------------------------
@@ -234,7 +284,7 @@ def run_gpu(args, spec, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local_rank) as clocks:
-        t_wall = time.perf_counter()
+        t_start = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(stream)
             pool()
@@ -242,17 +292,14 @@ def run_gpu(args, spec, rank, world, local_rank):
             select()
             ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
+        t_end = time.perf_counter()
+        clocks.window(t_start, t_end)
     if world > 1:
         torch.distributed.barrier()
     pool_ms = [a.elapsed_time(b) for a, b, _ in ev]
     sel_ms = [b.elapsed_time(c) for _, b, c in ev]
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][2]), dev)
 
     # select step alone, back to back (latency of one decode step of the selector)
     for _ in range(5):
@@ -321,7 +368,7 @@ def run_gpu(args, spec, rank, world, local_rank):
 
     return {
         "pool_ms": statistics.mean(pool_ms), "select_ms": statistics.mean(sel_ms), "step_ms": statistics.mean(step_ms),
-        "total_ms": total_ms, "wall_s": t_wall, "sel_b2b_us": sel_back_to_back_us, "sel_graph_us": graph_us,
+        "total_ms": total_ms, "wall_s": t_end - t_start, "sel_b2b_us": sel_back_to_back_us, "sel_graph_us": graph_us,
         "clocks": clocks.summary(), "e2e": e2e, "launches": launches_per_step * args.steps,
     }
 
@@ -352,12 +399,14 @@ def run_pool_gpu(args, local_rank):
         raise RuntimeError("device error during warm-up")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clocks:
+        t_start = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 255)
             ev[i][0].record(stream)
             kk.kk_score_pool_batched(A, V, Mt, K, idx, top, ws)
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
+        clocks.window(t_start, time.perf_counter())
     ms = [a.elapsed_time(b) for a, b in ev]
     # warm (inputs L2-resident) for comparison
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -377,7 +426,7 @@ def run_pool_gpu(args, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="7b")
@@ -425,7 +474,7 @@ def main():
         vals = []
         t_all = time.perf_counter()
         for _ in range(K):
-            v, sample, dt = oracle_sample(spec, min(args.cpu_budget, 240.0 / max(1, K + args.warmup)))
+            v, sample, dt = oracle_sample(spec, min(args.cpu_budget, 120.0 / max(1, K + args.warmup)))
             vals.append((v, dt))
         value = statistics.mean(v for v, _ in vals)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -438,12 +487,12 @@ def main():
         print(json.dumps(line))
         return
 
-    res = run_gpu(args, spec, rank, world, local_rank)
+    res = run_gpu(args, rank_spec(spec, rank), rank, world, local_rank)
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
     kb = spec.k_bytes()
-    value = world * kb * args.steps / (res["total_ms"] * 1e-3) / 1e9
+    value = weak_value(kb, args.steps, world, res["total_ms"]) / 1e9
     achieved = kb / (res["pool_ms"] * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     traffic = profiled_traffic(args.workload)
