@@ -49,7 +49,8 @@ WORKLOAD_NAMES = {
     "write16": "write path: 2^20 tokens of 7B geometry at block size 16",
     "write128": "write path: 2^20 tokens of 7B geometry at block size 128",
 }
-POOL_SRC = ["kv_cache_block_gb300/csrc/kk_pool.cu", "kv_cache_block_gb300/csrc/kk_device.cuh"]
+POOL_SRC = ["kv_cache_block_gb300/csrc/kk_pool_tma.cu", "kv_cache_block_gb300/csrc/kk_tcgen05.cuh",
+            "kv_cache_block_gb300/csrc/kk_device.cuh"]
 
 
 def dist_env():

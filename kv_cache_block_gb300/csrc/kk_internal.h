@@ -74,6 +74,17 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
                                       int N, int K, int* idx, float* top, void* ws, int* err,
                                       cudaStream_t s);
 
+// kk_host.cu
+void* tensor_map_encoder();  // cuTensorMapEncodeTiled (driver ABI 12.0), or null
+int sm_count();              // SMs of the current device
+
+// kk_pool_tma.cu: the persistent TMA pool for many blocks; returns
+// cudaErrorNotSupported (nothing launched) when the cache layout or the block
+// count does not suit it, and the caller falls back to launch_pool_direct.
+cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_valid, int n,
+                            const float* head_w, int n_sets, const int* w_set, float* vb, int* err,
+                            cudaStream_t s);
+
 // kk_api.cu (used by kk_static.cu)
 int* device_error_word();
 

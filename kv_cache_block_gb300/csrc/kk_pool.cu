@@ -356,6 +356,9 @@ cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_
                                const float* head_w, int n_sets, const int* w_set, float* vb,
                                int* err, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  // at least one block per SM: the persistent TMA pipeline (kk_pool_tma.cu)
+  const cudaError_t e = launch_pool_tma(kc, pages, n_valid, n, head_w, n_sets, w_set, vb, err, s);
+  if (e != cudaErrorNotSupported) return e;
   PoolArgs a = base_args(kc, err);
   a.pages = pages;
   a.n_valid = n_valid;

@@ -1,0 +1,380 @@
+// Block pooling of many blocks at once ("Key-Key Semantic Affinity" page,
+// §2.2 step 1 and §5.2 steps 2-3; per-(layer, head) weights per §3.3 finding
+// 2): the same v_b as pool_kernel in kk_pool.cu, from a persistent kernel
+// built for writes of hundreds to many thousands of blocks.
+//
+// One CTA per SM owns a contiguous, balanced range of whole blocks. Warp 0
+// streams each block's Keys through a ring of shared-memory stages with tiled
+// TMA loads of a 5-D view of the paged cache (dims, token, head, page, layer,
+// the last four in order of stride); eight consumer warps sum every stage's
+// rows. The bytes in flight per SM are set by the ring (six 32 KB stages), not
+// by how many CTAs are resident, so the SMs that still hold blocks at the end
+// of a launch draw the bandwidth the finished ones no longer use.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kk_device.cuh"
+#include "kk_internal.h"
+#include "kk_tcgen05.cuh"
+
+namespace kk {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = 32 + kConsumers;
+constexpr int kStageBytes = 32768;
+constexpr int kStages = 6;
+constexpr int kRowsPerThread = kStageBytes / (kConsumers * 16);  // 16-byte vectors per thread per stage
+constexpr int kMaxD = 256;
+constexpr int kTmaSmem = 1024 + kStages * kStageBytes + kMaxLH * 4 + 2 * kConsumerWarps * kMaxD * 4 +
+                         2 * kStages * 8 + 16;
+
+// The four strided axes of a K cache; each sits at one of the tensor map's
+// positions 1..4 (position 0 is the contiguous axis of the D dims).
+enum Dim { kTok = 0, kHead = 1, kPage = 2, kLayer = 3 };
+
+struct PoolTmaArgs {
+  const int* pages;
+  const int* n_valid;
+  const float* head_w;  // [n_sets][L*H] or null (uniform)
+  int n_sets;
+  const int* w_set;
+  float* vb;
+  int n;
+  int L, H, bs, num_pages;
+  int tb, hb, lb;     // tokens, heads and layers per box (tb | bs, hb | H, lb | L)
+  int nhb, nlb;       // boxes per block along heads and layers
+  int pos[4];         // tensor-map position (1..4) of each Dim
+  int ext[5];         // box extent at each tensor-map position
+  int* err;
+};
+
+struct BlockMeta {
+  int page, n, wsel;
+  bool ok;
+};
+
+__device__ __forceinline__ BlockMeta block_meta(const PoolTmaArgs& a, long long i) {
+  BlockMeta m;
+  m.page = a.pages[i];
+  m.n = a.n_valid[i];
+  m.wsel = (a.head_w && a.w_set) ? a.w_set[i] : 0;
+  m.ok = !(m.n < 0 || m.n > a.bs || m.page < 0 || m.page >= a.num_pages ||
+           (a.head_w && (m.wsel < 0 || m.wsel >= a.n_sets)));
+  return m;
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Value of tensor-map position p (1..4) for box coordinates given per Dim.
+__device__ __forceinline__ int coord_at(const PoolTmaArgs& a, int p, int tok, int head, int page, int layer) {
+  return a.pos[kTok] == p ? tok : a.pos[kHead] == p ? head : a.pos[kPage] == p ? page : layer;
+}
+
+template <typename T, int D, bool kWeighted>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    pool_tma_kernel(const __grid_constant__ CUtensorMap tm, const PoolTmaArgs a) {
+  constexpr int ES = elem_bytes<T>();
+  constexpr int EPV = Vec16<T>::kElems;
+  constexpr int V16 = D / EPV;              // 16-byte vectors per row
+  constexpr int RSTEP = kConsumers / V16;   // rows covered by one pass of the consumers
+  static_assert(V16 >= 1 && V16 <= 32 && (32 % V16) == 0, "row must be 16..512 bytes");
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = base;
+  float* s_w = reinterpret_cast<float*>(base + kStages * kStageBytes);  // [L*H] weights of the block
+  float* s_red = s_w + kMaxLH;                                          // [2][warps][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_red + 2 * kConsumerWarps * kMaxD);
+  uint64_t* empty = full + kStages;
+  int* s_abort = reinterpret_cast<int*>(empty + kStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long b0 = (long long)a.n * blockIdx.x / gridDim.x;
+  const long long b1 = (long long)a.n * (blockIdx.x + 1) / gridDim.x;
+  const int LH = a.L * a.H;
+  const uint32_t box_bytes = (uint32_t)(a.tb * a.hb * a.lb * D * ES);
+
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumerWarps);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = s_abort;
+
+  if (warp == 0) {
+    // ---- producer: one thread issues every box of the CTA's blocks --------
+    if (lane == 0) {
+      uint32_t k = 0;  // boxes issued
+      bool alive = true;
+      BlockMeta nx = b0 < b1 ? block_meta(a, b0) : BlockMeta{0, 0, 0, false};
+      for (long long i = b0; i < b1 && alive; ++i) {
+        const BlockMeta m = nx;
+        if (i + 1 < b1) nx = block_meta(a, i + 1);
+        if (!m.ok) continue;
+        const int nt = (m.n + a.tb - 1) / a.tb;
+        for (int lbi = 0; lbi < a.nlb && alive; ++lbi)
+          for (int hbi = 0; hbi < a.nhb && alive; ++hbi)
+            for (int tbi = 0; tbi < nt; ++tbi) {
+              const int st = (int)(k % kStages);
+              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, kWaitLimitNs)) ||
+                  *abort_flag) {
+                if (!*abort_flag) flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+                alive = false;
+                break;
+              }
+              const int ct = tbi * a.tb, ch = hbi * a.hb, cl = lbi * a.lb;
+              mbar_arrive_expect_tx(&full[st], box_bytes);
+              tma_load_5d(stages + st * kStageBytes, &tm, 0, coord_at(a, 1, ct, ch, m.page, cl),
+                          coord_at(a, 2, ct, ch, m.page, cl), coord_at(a, 3, ct, ch, m.page, cl),
+                          coord_at(a, 4, ct, ch, m.page, cl), &full[st]);
+              ++k;
+            }
+      }
+      // no copy may still be writing shared memory when the CTA exits
+      for (uint32_t j = k > (uint32_t)kStages ? k - kStages : 0; j < k; ++j)
+        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, kWaitLimitNs)) {
+          flag_error(a.err, kErrTimeout);
+          break;
+        }
+    }
+    return;
+  }
+
+  // ---- consumers ------------------------------------------------------------
+  const int ct = tid - 32, cw = ct >> 5;
+  const int col = ct % V16, r0 = ct / V16;
+  const int rows = a.tb * a.hb * a.lb;
+  // this thread's rows of a box: token offset and (layer, head) offset of each
+  int t_off[kRowsPerThread], s_off[kRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kRowsPerThread; ++j) {
+    int rr = r0 + j * RSTEP, q[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+    for (int p = 1; p <= 4; ++p) {
+      q[p] = rr % a.ext[p];
+      rr /= a.ext[p];
+    }
+    int qt = 0, qh = 0, ql = 0;
+#pragma unroll
+    for (int p = 1; p <= 4; ++p) {
+      if (a.pos[kTok] == p) qt = q[p];
+      if (a.pos[kHead] == p) qh = q[p];
+      if (a.pos[kLayer] == p) ql = q[p];
+    }
+    const bool in_box = r0 + j * RSTEP < rows;
+    t_off[j] = in_box ? qt : a.bs;  // rows past the box are never valid tokens
+    s_off[j] = in_box ? ql * a.H + qh : 0;
+  }
+  const uint32_t stage0 = smem_u32(stages) + (uint32_t)(r0 * D * ES + col * 16);
+  uint32_t k = 0;
+  int nred = 0;
+  // Every consumer thread walks the same blocks and boxes and meets the same
+  // named barriers whatever happens; after a failed wait a warp only stops
+  // touching the ring (the error word says why).
+  bool alive = true;
+  BlockMeta nx = b0 < b1 ? block_meta(a, b0) : BlockMeta{0, 0, 0, false};
+  for (long long i = b0; i < b1; ++i) {
+    const BlockMeta m = nx;
+    if (i + 1 < b1) nx = block_meta(a, i + 1);
+    if (!m.ok) {
+      if (ct == 0) flag_error(a.err, kErrBadIndex);
+      continue;
+    }
+    if (kWeighted) {
+      named_sync(1, kConsumers);  // the previous block's weights are no longer read
+      for (int s = ct; s < LH; s += kConsumers) s_w[s] = a.head_w[(long long)m.wsel * LH + s];
+      named_sync(1, kConsumers);
+    }
+    float acc[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+    const int nt = (m.n + a.tb - 1) / a.tb;
+    for (int lbi = 0; lbi < a.nlb; ++lbi)
+      for (int hbi = 0; hbi < a.nhb; ++hbi)
+        for (int tbi = 0; tbi < nt; ++tbi, ++k) {
+          if (!alive) continue;
+          const int st = (int)(k % kStages);
+          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, kWaitLimitNs);
+          ok = __all_sync(kFull, ok);
+          if (!ok) {
+            if (lane == 0 && !*abort_flag) flag_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+            alive = false;
+            continue;
+          }
+          const uint32_t sp = stage0 + (uint32_t)(st * kStageBytes);
+          const int tleft = m.n - tbi * a.tb;  // valid tokens from this box's first
+          const int sbase = lbi * a.lb * a.H + hbi * a.hb;
+          uint4 v[kRowsPerThread];
+#pragma unroll
+          for (int j = 0; j < kRowsPerThread; ++j)
+            v[j] = (r0 + j * RSTEP < rows) ? lds16(sp + (uint32_t)(j * RSTEP * D * ES)) : make_uint4(0, 0, 0, 0);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+          for (int j = 0; j < kRowsPerThread; ++j) {
+            if (t_off[j] < tleft) {
+              float f[EPV];
+              Vec16<T>::unpack(v[j], f);
+              const float w = kWeighted ? s_w[sbase + s_off[j]] : 1.f;
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+            }
+          }
+        }
+    // sum the lanes that share a dim range, then the warps
+#pragma unroll
+    for (int e = 0; e < EPV; ++e)
+#pragma unroll
+      for (int o = V16; o < 32; o <<= 1) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
+    float* red = s_red + (nred & 1) * kConsumerWarps * D;
+    if (lane < V16) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) red[cw * D + col * EPV + e] = acc[e];
+    }
+    named_sync(1, kConsumers);
+    if (!*abort_flag) {
+      const float scale = m.n == 0 ? 0.f : (kWeighted ? 1.f / (float)m.n : 1.f / ((float)m.n * (float)LH));
+      for (int d = ct; d < D; d += kConsumers) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) s += red[w * D + d];
+        a.vb[(long long)m.page * D + d] = s * scale;
+      }
+    }
+    ++nred;
+  }
+}
+
+template <typename T, int D, bool kWeighted>
+cudaError_t launch_t(const CUtensorMap& tm, const PoolTmaArgs& a, int grid, cudaStream_t s) {
+  static std::mutex mu;
+  static bool ready[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      e = cudaFuncSetAttribute(pool_tma_kernel<T, D, kWeighted>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTmaSmem);
+      if (e != cudaSuccess) return e;
+      ready[dev] = true;
+    }
+  }
+  pool_tma_kernel<T, D, kWeighted><<<grid, kTmaThreads, kTmaSmem, s>>>(tm, a);
+  return cudaGetLastError();
+}
+
+template <typename T, bool kWeighted>
+cudaError_t dispatch_d(int D, const CUtensorMap& tm, const PoolTmaArgs& a, int grid, cudaStream_t s) {
+  switch (D) {
+    case 32: return launch_t<T, 32, kWeighted>(tm, a, grid, s);
+    case 64: return launch_t<T, 64, kWeighted>(tm, a, grid, s);
+    case 128: return launch_t<T, 128, kWeighted>(tm, a, grid, s);
+    case 256: return sizeof(T) == 2 ? launch_t<bf16_t, 256, kWeighted>(tm, a, grid, s) : cudaErrorNotSupported;
+    default: return cudaErrorNotSupported;
+  }
+}
+
+int largest_divisor_at_most(int x, int cap) {
+  for (int d = std::min(x, cap); d > 1; --d)
+    if (x % d == 0) return d;
+  return 1;
+}
+
+}  // namespace
+
+cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_valid, int n,
+                            const float* head_w, int n_sets, const int* w_set, float* vb, int* err,
+                            cudaStream_t s) {
+  const int sms = sm_count();
+  if (n < sms) return cudaErrorNotSupported;  // too few blocks for one per SM: the cluster path splits them
+  const int ES = kc.dtype == 1 ? 2 : 4;
+  const long long row_bytes = (long long)kc.D * ES;
+  if (kc.D > kMaxD || row_bytes % 16 != 0 || row_bytes > 512 || (reinterpret_cast<uintptr_t>(kc.base) & 15))
+    return cudaErrorNotSupported;
+  // the four non-contiguous dims, sorted by stride (token, head, page, layer order on ties)
+  const long long stride[4] = {kc.sT * ES, kc.sH * ES, kc.sP * ES, kc.sL * ES};
+  for (long long b : stride)
+    if (b <= 0 || b % 16 != 0 || b >= (1ll << 40)) return cudaErrorNotSupported;
+  // box: tokens first, then whole heads, then whole layers, up to one stage
+  const int rows_cap = std::min<long long>(kStageBytes / row_bytes, 1 << 30);
+  int tb = kc.bs;
+  if (tb > rows_cap) {
+    if ((kc.bs & (kc.bs - 1)) != 0) return cudaErrorNotSupported;
+    tb = rows_cap;  // a power of two dividing bs
+  }
+  if (tb > 256) tb = 256;
+  if (kc.bs % tb != 0) return cudaErrorNotSupported;
+  const int hb = tb == kc.bs ? largest_divisor_at_most(kc.H, std::min(256, rows_cap / tb)) : 1;
+  const int lb = (tb == kc.bs && hb == kc.H) ? largest_divisor_at_most(kc.L, std::min(256, rows_cap / (tb * hb))) : 1;
+
+  PoolTmaArgs a = {};
+  a.pages = pages;
+  a.n_valid = n_valid;
+  a.head_w = head_w;
+  a.n_sets = n_sets;
+  a.w_set = w_set;
+  a.vb = vb;
+  a.n = n;
+  a.L = kc.L;
+  a.H = kc.H;
+  a.bs = kc.bs;
+  a.num_pages = kc.num_pages;
+  a.tb = tb;
+  a.hb = hb;
+  a.lb = lb;
+  a.nhb = kc.H / hb;
+  a.nlb = kc.L / lb;
+  a.err = err;
+  const long long extent[4] = {kc.bs, kc.H, kc.num_pages, kc.L};
+  const int box[4] = {tb, hb, 1, lb};
+  int order[4] = {kTok, kHead, kPage, kLayer};
+  std::stable_sort(order, order + 4, [&](int x, int y) { return stride[x] < stride[y]; });
+  cuuint64_t dims[5] = {(cuuint64_t)kc.D, 0, 0, 0, 0};
+  cuuint64_t strides[4] = {};
+  cuuint32_t bdim[5] = {(cuuint32_t)kc.D, 0, 0, 0, 0};
+  a.ext[0] = kc.D;
+  for (int p = 1; p <= 4; ++p) {
+    const int d = order[p - 1];
+    a.pos[d] = p;
+    dims[p] = (cuuint64_t)extent[d];
+    strides[p - 1] = (cuuint64_t)stride[d];
+    bdim[p] = (cuuint32_t)box[d];
+    a.ext[p] = box[d];
+  }
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tm;
+  if (encode(&tm, kc.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
+             const_cast<void*>(kc.base), dims, strides, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorNotSupported;
+  const int grid = std::min(n, sms);
+  if (kc.dtype == 1)
+    return head_w ? dispatch_d<bf16_t, true>(kc.D, tm, a, grid, s) : dispatch_d<bf16_t, false>(kc.D, tm, a, grid, s);
+  return head_w ? dispatch_d<float, true>(kc.D, tm, a, grid, s) : dispatch_d<float, false>(kc.D, tm, a, grid, s);
+}
+
+}  // namespace kk

@@ -108,7 +108,7 @@ class CacheSpec:
     shuffle_pages: bool = False
     span: int = 0  # tokens per topic segment; 0 -> bs
     extra_pages: int = 0  # unused physical pages in the pool
-    layout: str = "LPHTD"  # or "LPTHD" (token-major inside a page)
+    layout: str = "LPHTD"  # or "LPTHD" (token-major inside a page), "PLHTD" (page-major)
 
     # ---- derived -------------------------------------------------------
     def __post_init__(self):
@@ -185,6 +185,8 @@ class CacheSpec:
             return (P * H * bs * D, H * bs * D, bs * D, D)
         if self.layout == "LPTHD":
             return (P * bs * H * D, bs * H * D, D, H * D)
+        if self.layout == "PLHTD":
+            return (H * bs * D, L * H * bs * D, bs * D, D)
         raise ValueError(self.layout)
 
     def storage_elems(self) -> int:

@@ -101,6 +101,8 @@ class DeviceCache:
         idx = torch.as_tensor(np.asarray(pages, dtype=np.int64), device=self.storage.device)
         if sp.layout == "LPHTD":
             t = self.storage.view(L, P, H, bs, D).index_select(1, idx)
+        elif sp.layout == "PLHTD":
+            t = self.storage.view(P, L, H, bs, D).index_select(0, idx).transpose(0, 1)
         else:
             t = self.storage.view(L, P, bs, H, D).index_select(1, idx).transpose(2, 3)
         arr = t.contiguous().cpu().numpy()
