@@ -206,6 +206,11 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
  * uint32 [R][ceil(N/32)]). Scores are (1 + cos)/2 from float32 dot products
  * of the bf16 values; per anchor the top K pool ids (ordered as kk_topk) go
  * to idx [R][K] and top_scores [R][K] (nullable). D = 128, 1 <= K <= 256.
+ * workspace: caller-owned device memory, 256-byte aligned, of at least
+ * kk_score_pool_batched_workspace_bytes(R, N, K) bytes (about 8 * R * N plus
+ * counts); the size depends on the SM count of the current device, so query
+ * it with the device that will run the call current. Concurrent calls need
+ * separate workspaces.
  */
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K);
 kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,

@@ -30,31 +30,72 @@ constexpr int kBN = 128;  // pool blocks per tile
 constexpr int kD = 128;   // head_dim (two 64-element swizzle boxes)
 constexpr int kBoxBytes = 128 * 128;   // 128 rows x 128 bytes
 constexpr int kTileBytes = 2 * kBoxBytes;
-constexpr int kStages = 4;             // V tiles in flight
-constexpr int kEpiWarps = 8;           // two per TMEM lane quarter, 64 columns each
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kGemmThreads = 64 + kEpiThreads;  // warp 0 TMA, warp 1 MMA, then the epilogue
-constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
-constexpr int kStageFloats = kEpiWarps * 32 * 33;  // per-lane 32-column dump, padded
-constexpr int kGemmSmem = kTileBytes * (1 + kStages) + kStageFloats * 4 + 8 * 128 * 4 + 256 + 1024;
+constexpr int kStages = 3;             // V tiles in flight
+constexpr int kGroups = 4;             // epilogue groups, each drains whole tiles
+constexpr int kAccs = kGroups;         // TMEM accumulators (128 columns each), one per group
+constexpr int kGroupThreads = 128;     // four warps: one per TMEM lane quarter
+constexpr int kEpiThreads = kGroups * kGroupThreads;
+constexpr int kGemmThreads = 64 + kEpiThreads;  // warp 0 TMA, warp 1 MMA, then the epilogue groups
+constexpr uint32_t kTmemCols = kAccs * kBN;
+constexpr int kDumpStride = 36;  // floats per lane row of the dump: 16-byte rows, no bank conflicts
+constexpr int kDumpFloats = kEpiThreads * kDumpStride;
+constexpr int kGemmSmem =
+    1024 + kTileBytes * (1 + kStages) + kDumpFloats * 4 + kGroups * 2 * kBN * 4 + 256;
 
 struct GemmArgs {
   const uint32_t* mask;
   int R, N, mask_words, tiles;
-  int* counts;      // [R][tiles] owned candidates of each anchor in each 128-block tile
-  uint64_t* cand;   // [R][tiles][128] candidate keys, segment per (anchor, tile)
+  int* counts;      // [R][P] owned candidates of each anchor in each CTA's tiles
+  uint64_t* cand;   // [R][P][cap] candidate keys, one segment per (anchor, CTA)
+  long long cap;    // 128 x the most tiles a CTA takes
+  int mask_vec;     // mask rows allow 16-byte loads of a tile's four words
   int* err;
 };
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Sum of squares of one 128-dim bf16 row held as two 128-byte swizzled rows
+// (one per box); the swizzle only permutes 16-byte chunks inside a row, and
+// the order of a sum of squares does not matter. The chunk order is rotated
+// by the row so that the eight rows a quarter-warp reads hit eight different
+// bank groups; four chains for ILP.
+__device__ __forceinline__ float row_sq(const unsigned char* tile, int row) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int pc = (c + row) & 7;
+      const uint4 x = *reinterpret_cast<const uint4*>(tile + h * kBoxBytes + row * 128 + pc * 16);
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = bf16_lo(xw[q]), hi = bf16_hi(xw[q]);
+        acc[q] = fmaf(lo, lo, fmaf(hi, hi, acc[q]));
+      }
+    }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Persistent, warp-specialised: CTA c owns M-tile (c % MT) of the anchors and
-// N-tiles p, p + P, p + 2P, ... (p = c / MT, P = CTAs per M-tile). Warp 0
-// streams V tiles through a kStages-deep TMA ring; warp 1 issues the MMAs of
-// tile j into TMEM accumulator j % 2; eight epilogue warps take the V-row
-// norms from the ring (then release the stage) and drain the other
-// accumulator, so the epilogue of tile j overlaps the loads and MMAs of tile
-// j + 1. Each epilogue warp drains 64 columns of its 32 TMEM lanes (anchors)
-// without branches: every column's score is formed in registers and only
-// owned columns are stored, at slots given by a popcount prefix of the mask.
+// N-tiles p, p + P, p + 2P, ... (p = c / MT, P = CTAs per M-tile), split into
+// four contiguous ranges, one per epilogue group of four warps, each group
+// with its own TMEM accumulator. Warp 0 streams V tiles through a
+// kStages-deep TMA ring and warp 1 issues the MMAs, both visiting the ranges
+// round robin, so four tiles drain at once. A group computes its tile's V-row
+// norms from the ring (then releases the stage), reads the accumulator (one
+// anchor row per thread, tcgen05.ld), and writes each owned column as a
+// 64-bit key (score, pool id) into the anchor's segment for this CTA, in tile
+// order; the last group writes the segment's length. No atomics: every slot
+// has one writer.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     score_pool_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmV,
                       GemmArgs g) {
@@ -63,19 +104,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sA = base;               // A tile: two boxes (dims 0-63, 64-127)
   unsigned char* sV = base + kTileBytes;  // kStages V tiles
-  float* s_dump = reinterpret_cast<float*>(base + kTileBytes * (1 + kStages));  // [warp][lane][33]
-  float* s_part = s_dump + kStageFloats;  // [2 halves][128] sums of squares
-  float* s_inv_a = s_part + 256;          // [128] 1 / ||A row||
-  float* s_inv_v = s_inv_a + 128;         // [2 buffers][128] 1 / ||V row||
-  float* s_part_a = s_inv_v + 256;        // [2 halves][128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(s_part_a + 256);
-  uint64_t* bar_a = bar;                         // A tile landed
-  uint64_t* full = bar + 1;                      // [kStages] V tile landed
-  uint64_t* empty = full + kStages;              // [kStages] V tile released (MMA + epilogue warps)
-  uint64_t* acc_full = empty + kStages;          // [2] accumulator ready
-  uint64_t* acc_empty = acc_full + 2;            // [2] accumulator drained (epilogue warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  float* s_dump = reinterpret_cast<float*>(base + kTileBytes * (1 + kStages));  // [thread][36]
+  float* s_inv_v = s_dump + kDumpFloats;  // [group][2 buffers][128] 1 / ||V row||
+  uint64_t* bar = reinterpret_cast<uint64_t*>(s_inv_v + kGroups * 2 * kBN);
+  uint64_t* bar_a = bar;                  // A tile landed
+  uint64_t* full = bar + 1;               // [kStages] V tile landed
+  uint64_t* empty = full + kStages;       // [kStages] V tile released (MMA + the tile's group)
+  uint64_t* acc_full = empty + kStages;   // [kAccs] accumulator ready
+  uint64_t* acc_empty = acc_full + kAccs; // [kAccs] accumulator drained (the tile's group)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + kAccs);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
+
+  // the select kernel may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int MT = (g.R + kBM - 1) / kBM;
@@ -90,11 +131,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(bar_a, 1);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full[st], 1);
-      mbar_init(&empty[st], 1 + kEpiWarps);
+      mbar_init(&empty[st], 1 + kGroupThreads / 32);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccs; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
+      mbar_init(&acc_empty[b], kGroupThreads / 32);
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -113,14 +154,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     flag_error(g.err, code);
   };
 
+  // The CTA's local tiles 0 .. ntiles-1 (global tile p + j * P) are split
+  // into four contiguous ranges, one per epilogue group, and each group has
+  // its own TMEM accumulator. The producer and the MMA issuer visit the
+  // ranges round robin (sequence k: group k % 4, its (k / 4)-th tile), so
+  // four tiles drain at once; q counts the tiles issued (its ring stage).
+  auto range_lo = [&](int gg) { return gg * ntiles / kGroups; };
+  auto range_len = [&](int gg) { return (gg + 1) * ntiles / kGroups - gg * ntiles / kGroups; };
+
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_a, kTileBytes);
       tma_load_2d(sA, &tmA, 0, m0, bar_a);
       tma_load_2d(sA + kBoxBytes, &tmA, 64, m0, bar_a);
-      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait_bounded(&empty[st], ((j / kStages) & 1) ^ 1, kWaitLimitNs)) {
+      for (int k = 0, q = 0; q < ntiles && !*abort_flag; ++k) {
+        const int gg = k % kGroups, i = k / kGroups;
+        if (i >= range_len(gg)) continue;
+        const int j = range_lo(gg) + i;
+        const int st = q % kStages;
+        if (q >= kStages && !mbar_wait_bounded(&empty[st], ((q / kStages) & 1) ^ 1, kWaitLimitNs)) {
           fail(kErrTimeout);
           break;
         }
@@ -129,165 +181,162 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive_expect_tx(&full[st], kTileBytes);
         tma_load_2d(dst, &tmV, 0, n0, &full[st]);
         tma_load_2d(dst + kBoxBytes, &tmV, 64, n0, &full[st]);
+        ++q;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
       if (!mbar_wait_bounded(bar_a, 0, kWaitLimitNs)) fail(kErrTimeout);
-      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-        const int st = j % kStages, b = j & 1;
-        if (!mbar_wait_bounded(&full[st], (j / kStages) & 1, kWaitLimitNs) ||
-            (j >= 2 && !mbar_wait_bounded(&acc_empty[b], ((j >> 1) & 1) ^ 1, kWaitLimitNs))) {
+      for (int k = 0, q = 0; q < ntiles && !*abort_flag; ++k) {
+        const int gg = k % kGroups, i = k / kGroups;
+        if (i >= range_len(gg)) continue;
+        const int st = q % kStages;
+        if (!mbar_wait_bounded(&full[st], (q / kStages) & 1, kWaitLimitNs) ||
+            (i >= 1 && !mbar_wait_bounded(&acc_empty[gg], (i - 1) & 1, kWaitLimitNs))) {
           fail(kErrTimeout);
           break;
         }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA), v0 = smem_u32(sV + st * kTileBytes);
-        const uint32_t d = tmem + (uint32_t)(b * kBN);
+        const uint32_t d = tmem + (uint32_t)(gg * kBN);
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const uint32_t off = (uint32_t)((k >> 2) * kBoxBytes + (k & 3) * 32);
-          mma_bf16(d, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(v0 + off), idesc, k > 0);
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
+          mma_bf16(d, desc_kmajor_sw128(a0 + off), desc_kmajor_sw128(v0 + off), idesc, kk > 0);
         }
         mma_commit(&empty[st]);
-        mma_commit(&acc_full[b]);
+        mma_commit(&acc_full[gg]);
+        ++q;
       }
     }
   } else {
-    const int ew = warp - 2;             // epilogue warp 0..7
-    const int half = ew >> 2;            // which 64 columns this warp drains
-    const int q4 = warp & 3;             // TMEM lane quarter of this warp
-    const int row = q4 * 32 + lane;      // anchor row (TMEM lane) this thread drains
+    const int et = tid - 64;
+    const int grp = et / kGroupThreads;       // epilogue group
+    const int q4 = warp & 3;                  // TMEM lane quarter this warp may access
+    const int row = q4 * 32 + lane;           // anchor row (TMEM lane) of this thread
     const int r = m0 + row;
-    const int nrow = ew * 32 + lane;     // norm work item: row nrow & 127, half nrow >> 7
-    const int nr = nrow & 127, nh = nrow >> 7;
-    // half of the squared norm of a 128-dim bf16 row stored as two 128-byte
-    // swizzled rows: box `nh`, eight 16-byte chunks (rotated by lane to spread
-    // banks; the order of a sum of squares does not matter)
-    auto half_sq = [&](const unsigned char* tile) {
-      float acc = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int cc = (c + lane) & 7;
-        const uint4 x = *reinterpret_cast<const uint4*>(tile + nh * kBoxBytes + nr * 128 + cc * 16);
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = bf16_lo(xw[q]), hi = bf16_hi(xw[q]);
-          acc = fmaf(lo, lo, fmaf(hi, hi, acc));
-        }
-      }
-      return acc;
-    };
+    const int bar_id = 1 + grp;               // named barrier of the group
+    float* inv_v_grp = s_inv_v + grp * 2 * kBN;
+    const uint32_t dump = smem_u32(s_dump + et * kDumpStride);
+    const int lo = range_lo(grp), len = range_len(grp);
     auto inv_norm = [](float sq) { return sq > 0.f ? 1.f / sqrtf(sq) : 0.f; };
-    bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
-    if (!ok) fail(kErrTimeout);
-    s_part_a[nh * 128 + nr] = ok ? half_sq(sA) : 0.f;
-    named_sync(1, kEpiThreads);
-    if (nrow < 128) s_inv_a[nrow] = inv_norm(s_part_a[nrow] + s_part_a[128 + nrow]);
-    named_sync(1, kEpiThreads);
-    const float inv_a = s_inv_a[row];
-    // ownership bits of this anchor's 128 columns of tile jj (limited to
-    // columns < N); fetched two tiles ahead so their latency stays hidden
+    // ownership bits of this anchor's 128 columns of the CTA's local tile jj
+    // (limited to columns < N): one 16-byte load when the rows allow it
+    const uint32_t* mrow = g.mask + (long long)(r < g.R ? r : 0) * g.mask_words;
     auto mask_words = [&](int jj, uint32_t (&w)[4]) {
-      const int n0 = (p + jj * P) * kBN;
+      const int wi0 = (p + jj * P) * (kBN / 32);
+      if (g.mask_vec && jj < ntiles && r < g.R) {
+        const uint4 x = *reinterpret_cast<const uint4*>(mrow + wi0);
+        w[0] = x.x;
+        w[1] = x.y;
+        w[2] = x.z;
+        w[3] = x.w;
+      } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int wi = n0 / 32 + c;
-        uint32_t x = 0;
-        if (jj < ntiles && r < g.R && wi < g.mask_words) x = g.mask[(long long)r * g.mask_words + wi];
-        w[c] = x;
+        for (int c = 0; c < 4; ++c)
+          w[c] = (jj < ntiles && r < g.R && wi0 + c < g.mask_words) ? mrow[wi0 + c] : 0u;
       }
-    };
-    auto limit_cols = [&](int n0, uint32_t (&w)[4]) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int lim = g.N - (n0 / 32 + c) * 32;
+        const int lim = g.N - (wi0 + c) * 32;
         if (lim < 32) w[c] &= lim <= 0 ? 0u : ((1u << lim) - 1u);
       }
     };
-    uint32_t w_next[4], w_after[4];
-    mask_words(0, w_next);
-    mask_words(1, w_after);
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kStages, b = j & 1;
+    auto owned = [](const uint32_t (&w)[4]) { return __popc(w[0]) + __popc(w[1]) + __popc(w[2]) + __popc(w[3]); };
+    // The anchor's keys from this CTA's tiles fill one segment in local tile
+    // order: this group's keys start after the owned columns of the tiles of
+    // the groups before it.
+    uint64_t* seg = g.cand + ((long long)r * P + p) * g.cap;
+    int pre = 0;
+    for (int j0 = 0; j0 < lo; j0 += 4) {
+      uint32_t wb[4][4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) mask_words(j0 + x < lo ? j0 + x : ntiles, wb[x]);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) pre += owned(wb[x]);
+    }
+    uint32_t w_next[4];
+    mask_words(len > 0 ? lo : ntiles, w_next);
+    bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
+    if (!ok) fail(kErrTimeout);
+    const float inv_a = ok ? inv_norm(row_sq(sA, row)) : 0.f;
+    for (int i = 0; i < len; ++i) {
+      const int j = lo + i;
+      // this tile's place in the issue sequence: tiles of earlier rounds,
+      // then those of the groups before this one in round i
+      int q = 0;
+#pragma unroll
+      for (int gg = 0; gg < kGroups; ++gg) q += min(range_len(gg), i + (gg < grp ? 1 : 0));
+      const int st = q % kStages;
       const int tile = p + j * P, n0 = tile * kBN;
       uint32_t w[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        w[c] = w_next[c];
-        w_next[c] = w_after[c];
-      }
-      mask_words(j + 2, w_after);
-      limit_cols(n0, w);
-      // V-row norms of this tile, then release the ring stage. The epilogue
-      // warps leave the loop together (a lone warp leaving would strand the
-      // others at the named barrier).
-      ok = !*abort_flag && mbar_wait_bounded(&full[st], (j / kStages) & 1, kWaitLimitNs);
-      s_part[nh * 128 + nr] = ok ? half_sq(sV + st * kTileBytes) : 0.f;
+      for (int c = 0; c < 4; ++c) w[c] = w_next[c];
+      mask_words(i + 1 < len ? j + 1 : ntiles, w_next);
+      // V-row norms of this tile (one row per thread), then release the
+      // ring stage. The group leaves the loop together (a lone warp leaving
+      // would strand the others at the named barrier).
+      ok = !*abort_flag && mbar_wait_bounded(&full[st], (q / kStages) & 1, kWaitLimitNs);
+      float* inv_v = inv_v_grp + (i & 1) * kBN;
+      inv_v[row] = ok ? inv_norm(row_sq(sV + st * kTileBytes, row)) : 0.f;
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (named_sync_or(1, kEpiThreads, !ok)) {
-        if (!ok) fail(kErrTimeout);
-        break;
-      }
-      if (nrow < 128) s_inv_v[b * 128 + nrow] = inv_norm(s_part[nrow] + s_part[128 + nrow]);
-      ok = mbar_wait_bounded(&acc_full[b], (j >> 1) & 1, kWaitLimitNs);
-      if (named_sync_or(1, kEpiThreads, !ok)) {  // tcgen05.ld below is warp-collective too
+      ok = ok && mbar_wait_bounded(&acc_full[grp], i & 1, kWaitLimitNs);
+      if (named_sync_or(bar_id, kGroupThreads, !ok)) {  // also orders the inv_v writes before the reads
         if (!ok) fail(kErrTimeout);
         break;
       }
       tc_fence_after();
-      uint32_t acc[2][32];
-      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(b * kBN + half * 64);
-      tmem_ld32(taddr, acc[0]);
-      tmem_ld32(taddr + 32, acc[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);  // the accumulator may be reused
-      if (r < g.R && half == 0)
-        g.counts[(long long)r * g.tiles + tile] = __popc(w[0]) + __popc(w[1]) + __popc(w[2]) + __popc(w[3]);
-      uint64_t* out = g.cand + ((long long)r * g.tiles + tile) * kBN;
-      int k = half ? __popc(w[0]) + __popc(w[1]) : 0;
-      const float* inv_v = s_inv_v + b * 128 + half * 64;
-      // Owned columns are sparse: dump the 32 accumulators of a chunk to this
-      // lane's shared-memory row (stride 33: no bank conflicts) and visit only
-      // the set mask bits.
-      float* dump = s_dump + (ew * 32 + lane) * 33;
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(grp * kBN);
+      uint64_t* out = seg + pre;
+      int k = 0;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t acc[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), acc);
+        tmem_wait_ld();
+        if (c == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[grp]);  // the accumulator may be reused
+        }
+        uint32_t x = w[c];
+        if (x == 0u) continue;
+        // owned columns are sparse: dump the chunk to this thread's row of
+        // shared memory and visit only the set bits, the first four as
+        // independent slots (their loads and math overlap), then the rare
+        // remainder one by one
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dump[i] = __uint_as_float(acc[c][i]);
-        uint32_t x = half ? w[2 + c] : w[c];
-        // the first four owned columns as independent slots (they overlap),
-        // then the rare remainder one by one
+        for (int e = 0; e < 32; e += 4) sts128(dump + e * 4, acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
         int ib[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           ib[u] = x ? __ffs(x) - 1 : -1;
           x &= x - 1;
         }
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = ib[u] >= 0 ? lds_f32(dump + ib[u] * 4) * inv_v[c * 32 + ib[u]] : 0.f;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (ib[u] >= 0) {
-            const int i = ib[u];
-            float cosv = dump[i] * inv_a * inv_v[c * 32 + i];
-            cosv = fminf(1.f, fmaxf(-1.f, cosv));
-            out[k + u] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + half * 64 + c * 32 + i));
+            const float cosv = fminf(1.f, fmaxf(-1.f, v[u] * inv_a));
+            out[k + u] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + ib[u]));
           }
         }
         k += (ib[0] >= 0) + (ib[1] >= 0) + (ib[2] >= 0) + (ib[3] >= 0);
         while (x) {
-          const int i = __ffs(x) - 1;
+          const int e = __ffs(x) - 1;
           x &= x - 1;
-          float cosv = dump[i] * inv_a * inv_v[c * 32 + i];
-          cosv = fminf(1.f, fmaxf(-1.f, cosv));
-          out[k++] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + half * 64 + c * 32 + i));
+          const float cosv = fminf(1.f, fmaxf(-1.f, lds_f32(dump + e * 4) * inv_v[c * 32 + e] * inv_a));
+          out[k++] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + e));
         }
       }
+      pre += owned(w);
     }
+    // the last group's range ends at the CTA's last tile: its end is the total
+    if (grp == kGroups - 1 && r < g.R) g.counts[(long long)r * P + p] = pre;
   }
 
   // teardown: every role has left its loop; no MMA or TMEM read is pending
@@ -299,69 +348,85 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-// ---- per-anchor top-K by radix select ------------------------------------
+// ---- per-anchor top-K ----------------------------------------------------
 constexpr int kSelThreads = 256;
-constexpr int kSelStage = 6144;  // keys of a row held in shared memory (48 KB)
+constexpr int kSelStage = 6144;                    // keys of a row held in shared memory (48 KB)
+constexpr int kRegKeys = kSelStage / kSelThreads;  // and then in registers, 24 per thread
+constexpr int kMaxSegs = 1024;                     // segments (GEMM CTAs per M-tile) of a row
+constexpr int kBuckets = 2048;                     // linear buckets over a row's score range
+constexpr int kTieCap = 512;                       // boundary-bucket keys ranked exactly
 
-// Visits every candidate key of row r, warp-uniformly (every lane of a warp
-// runs the same iterations; `active` marks real keys), either from the
-// shared-memory copy or, for rows too long for it, from the tile segments.
+struct SelArgs {
+  const uint64_t* cand;  // [R][segs][cap] keys, segment per (anchor, GEMM CTA)
+  const int* counts;     // [R][segs]
+  int segs;
+  long long cap;
+  int K;
+  int* idx;
+  float* top;
+  int* err;
+};
+
+// Visits every candidate key of a row straight from its segments,
+// warp-uniformly (every lane of a warp runs the same iterations; `active`
+// marks real keys): the path for rows longer than the shared-memory copy.
 template <typename F>
-__device__ __forceinline__ void for_each_key(bool staged, int n, const uint64_t* s_keys, const int* cnt,
-                                             const uint64_t* seg, int tiles, F&& fn) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (staged) {
-    for (int i0 = 0; i0 < n; i0 += kSelThreads) {
-      const int i = i0 + tid;
-      const bool active = i < n;
-      fn(active, active ? s_keys[i] : 0ull);
-    }
-  } else {
-    for (int t = warp; t < tiles; t += kSelThreads / 32) {
-      const int c = min(max(cnt[t], 0), kBN);
-      for (int j0 = 0; j0 < c; j0 += 32) {
-        const int j = j0 + lane;
-        const bool active = j < c;
-        fn(active, active ? seg[(long long)t * kBN + j] : 0ull);
-      }
+__device__ __forceinline__ void for_each_segment_key(const SelArgs& a, const int* s_cnt, const uint64_t* row, F&& fn) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int p = warp; p < a.segs; p += kSelThreads / 32) {
+    const int c = s_cnt[p];
+    for (int j0 = 0; j0 < c; j0 += 32) {
+      const int j = j0 + lane;
+      const bool active = j < c;
+      fn(active, active ? row[p * a.cap + j] : 0ull);
     }
   }
 }
 
-constexpr int kBuckets = 2048;  // linear buckets over a row's score range
-constexpr int kMaxTiles = 2048; // tiles of a row whose offsets are staged (N <= 262144)
-constexpr int kTieCap = 512;    // boundary-bucket keys ranked exactly
-
-__global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t* cand, const int* counts,
-                                                                  int tiles, int K, int* idx_out,
-                                                                  float* top_out, int* err) {
+// One CTA per anchor. The row's segments are copied into shared memory with
+// warp-wide coalesced loads, then into registers (24 keys a thread). One pass
+// of linear buckets over the row's score range finds the bucket holding the
+// K-th key; keys above it are selected, the boundary bucket's keys are ranked
+// exactly; the K winners are sorted (warp bitonic lists + merge ranks). Rows
+// longer than the shared-memory copy take the same passes over the segments,
+// with a radix select on the 64-bit keys when a bucket holds too many ties.
+__global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs a) {
   extern __shared__ __align__(16) uint64_t s_keys[];  // [kSelStage]
   __shared__ int hist[kBuckets];
+  __shared__ int s_cnt[kMaxSegs];
+  __shared__ int s_off[kMaxSegs];
   __shared__ int s_bin, s_above;
   __shared__ int s_sel_n, s_tie_n;
   __shared__ int s_wsum[kSelThreads / 32];
-  __shared__ int s_off[kMaxTiles + 1];
   __shared__ uint64_t s_lo[kSelThreads / 32], s_hi[kSelThreads / 32];
   __shared__ uint64_t s_sel[kMaxK];
   __shared__ uint64_t s_tie[kTieCap];
   __shared__ uint64_t s_wl[kSelThreads / 32][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
-  const int* cnt = counts + (long long)r * tiles;
-  const uint64_t* seg = cand + (long long)r * tiles * kBN;
+  const int K = a.K;
+  const uint64_t* row = a.cand + (long long)r * a.segs * a.cap;
 
-  // ---- row length and per-tile offsets: each thread sums a contiguous run
-  // of tiles, an exclusive scan over the block gives the run's start, and the
-  // run's tile offsets go to shared memory (rows of up to kMaxTiles tiles)
-  const int tpt = (tiles + kSelThreads - 1) / kSelThreads;
-  const int t_begin = min(tiles, tid * tpt), t_end = min(tiles, t_begin + tpt);
+  for (int b = tid; b < kBuckets; b += kSelThreads) hist[b] = 0;
+  if (tid == 0) {
+    s_sel_n = 0;
+    s_tie_n = 0;
+  }
+  // the candidates come from the GEMM grid launched just before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- segment counts and their offsets in the row's compact copy: each
+  // thread scans a run of up to four segments, then the block
+  const int spt = (a.segs + kSelThreads - 1) / kSelThreads;  // <= 4
+  const int s_begin = min(a.segs, tid * spt), s_end = min(a.segs, s_begin + spt);
   int mine = 0;
-  for (int t = t_begin; t < t_end; ++t) {
-    int c = cnt[t];
-    if (c < 0 || c > kBN) {
-      flag_error(err, kErrBadIndex);
-      c = min(max(c, 0), kBN);
+  for (int p = s_begin; p < s_end; ++p) {
+    int c = a.counts[(long long)r * a.segs + p];
+    if (c < 0 || c > a.cap) {
+      flag_error(a.err, kErrBadIndex);
+      c = c < 0 ? 0 : (int)a.cap;
     }
+    s_cnt[p] = c;
     mine += c;
   }
   int incl = mine;
@@ -378,43 +443,52 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
     if (w < warp) base += s_wsum[w];
     n += s_wsum[w];
   }
-  const bool staged = n <= kSelStage && tiles <= kMaxTiles;
-  if (staged) {
-    int o = base;
-    for (int t = t_begin; t < t_end; ++t) {
-      s_off[t] = o;
-      o += min(max(cnt[t], 0), kBN);
-    }
-    if (tid == 0) s_off[tiles] = n;
+  for (int p = s_begin; p < s_end; ++p) {
+    s_off[p] = base;
+    base += s_cnt[p];
   }
+  const bool staged = n <= kSelStage;
   __syncthreads();
 
-  // ---- stage the row compactly: key i lives in the last tile whose offset
-  // is <= i (binary search), 16 independent loads per thread; and the key range
+  // ---- the compact copy: warp w takes segments w, w + 8, ...; two segments
+  // and 64 keys of each per round of loads (a segment holds about N / segs
+  // owned candidates, here ~54)
+  if (staged) {
+    for (int p0 = warp; p0 < a.segs; p0 += 2 * (kSelThreads / 32)) {
+      const int p1 = p0 + kSelThreads / 32;
+      const int c0 = s_cnt[p0], c1 = p1 < a.segs ? s_cnt[p1] : 0;
+      const uint64_t* g0 = row + p0 * a.cap;
+      const uint64_t* g1 = row + p1 * a.cap;
+      const uint64_t v0 = lane < c0 ? g0[lane] : 0ull, v1 = lane + 32 < c0 ? g0[lane + 32] : 0ull;
+      const uint64_t v2 = lane < c1 ? g1[lane] : 0ull, v3 = lane + 32 < c1 ? g1[lane + 32] : 0ull;
+      const int o0 = s_off[p0], o1 = p1 < a.segs ? s_off[p1] : 0;
+      if (lane < c0) s_keys[o0 + lane] = v0;
+      if (lane + 32 < c0) s_keys[o0 + lane + 32] = v1;
+      if (lane < c1) s_keys[o1 + lane] = v2;
+      if (lane + 32 < c1) s_keys[o1 + lane + 32] = v3;
+      for (int j = 64 + lane; j < c0; j += 32) s_keys[o0 + j] = g0[j];
+      for (int j = 64 + lane; j < c1; j += 32) s_keys[o1 + j] = g1[j];
+    }
+    __syncthreads();
+  }
+
+  // ---- this thread's keys (staged rows) and the row's key range
+  uint64_t key[kRegKeys];
   uint64_t lo = ~0ull, hi = 0ull;
   if (staged) {
-    for (int i0 = 0; i0 < n; i0 += kSelThreads * 16) {
-      uint64_t v[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = i0 + u * kSelThreads + tid;
-        int t = 0;
-        for (int step = kMaxTiles / 2; step > 0; step >>= 1)
-          if (t + step <= tiles && s_off[t + step] <= i) t += step;
-        v[u] = i < n ? seg[(long long)t * kBN + (i - s_off[t])] : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = i0 + u * kSelThreads + tid;
-        if (i < n) {
-          s_keys[i] = v[u];
-          lo = v[u] < lo ? v[u] : lo;
-          hi = v[u] > hi ? v[u] : hi;
-        }
+    for (int u = 0; u < kRegKeys; ++u) {
+      const int i = tid + u * kSelThreads;
+      key[u] = i < n ? s_keys[i] : 0ull;
+      if (i < n) {
+        lo = key[u] < lo ? key[u] : lo;
+        hi = key[u] > hi ? key[u] : hi;
       }
     }
   } else {
-    for_each_key(false, n, s_keys, cnt, seg, tiles, [&](bool active, uint64_t k) {
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) key[u] = 0ull;
+    for_each_segment_key(a, s_cnt, row, [&](bool active, uint64_t k) {
       if (active) {
         lo = k < lo ? k : lo;
         hi = k > hi ? k : hi;
@@ -423,18 +497,13 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t a = __shfl_xor_sync(kFull, lo, o), b = __shfl_xor_sync(kFull, hi, o);
-    lo = a < lo ? a : lo;
-    hi = b > hi ? b : hi;
+    const uint64_t x = __shfl_xor_sync(kFull, lo, o), y = __shfl_xor_sync(kFull, hi, o);
+    lo = x < lo ? x : lo;
+    hi = y > hi ? y : hi;
   }
   if (lane == 0) {
     s_lo[warp] = lo;
     s_hi[warp] = hi;
-  }
-  for (int b = tid; b < kBuckets; b += kSelThreads) hist[b] = 0;
-  if (tid == 0) {
-    s_sel_n = 0;
-    s_tie_n = 0;
   }
   __syncthreads();
   lo = s_lo[0];
@@ -445,6 +514,15 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
     hi = s_hi[w] > hi ? s_hi[w] : hi;
   }
   const int m = min(K, n);
+  // visits every key of the row warp-uniformly: registers, or the segments
+  auto visit = [&](auto&& fn) {
+    if (staged) {
+#pragma unroll
+      for (int u = 0; u < kRegKeys; ++u) fn(tid + u * kSelThreads < n, key[u]);
+    } else {
+      for_each_segment_key(a, s_cnt, row, fn);
+    }
+  };
 
   // ---- bucket pass: linear buckets over the score part of the keys (a
   // non-decreasing function of the key, so keys above the boundary bucket
@@ -456,7 +534,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
   };
   bool fast = m > 0 && s_hi32 != s_lo32;
   if (fast) {
-    for_each_key(staged, n, s_keys, cnt, seg, tiles, [&](bool active, uint64_t k) {
+    visit([&](bool active, uint64_t k) {
       if (active) atomicAdd(&hist[bucket(k)], 1);
     });
     __syncthreads();
@@ -484,17 +562,63 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
     }
     __syncthreads();
     const int bstar = s_bin;
-    for_each_key(staged, n, s_keys, cnt, seg, tiles, [&](bool active, uint64_t k) {
-      if (!active) return;
-      const int b = bucket(k);
-      if (b > bstar) {
-        const int p = atomicAdd(&s_sel_n, 1);
-        if (p < kMaxK) s_sel[p] = k;
-      } else if (b == bstar) {
-        const int p = atomicAdd(&s_tie_n, 1);
-        if (p < kTieCap) s_tie[p] = k;
+    // keys above the boundary bucket to s_sel, the boundary bucket's to
+    // s_tie; one shared-memory atomic per warp and list, a lane's slot is
+    // the count of the keys of lower lanes (and earlier rounds) before it
+    const unsigned below_me = (1u << lane) - 1u;
+    if (staged) {
+      // this thread's keys above / in the boundary bucket as bit masks, a
+      // warp scan of their counts, one atomic per warp and list
+      uint32_t m_above = 0, m_tie = 0;
+#pragma unroll
+      for (int u = 0; u < kRegKeys; ++u) {
+        const int b = tid + u * kSelThreads < n ? bucket(key[u]) : -1;
+        m_above |= (b > bstar ? 1u : 0u) << u;
+        m_tie |= (b == bstar ? 1u : 0u) << u;
       }
-    });
+      const int c_above = __popc(m_above), c_tie = __popc(m_tie);
+      int x_above = c_above, x_tie = c_tie;  // inclusive scans over the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(kFull, x_above, o), yt = __shfl_up_sync(kFull, x_tie, o);
+        if (lane >= o) {
+          x_above += ya;
+          x_tie += yt;
+        }
+      }
+      int p_sel = 0, p_tie = 0;
+      if (lane == 31) {
+        if (x_above) p_sel = atomicAdd(&s_sel_n, x_above);
+        if (x_tie) p_tie = atomicAdd(&s_tie_n, x_tie);
+      }
+      p_sel = __shfl_sync(kFull, p_sel, 31) + x_above - c_above;
+      p_tie = __shfl_sync(kFull, p_tie, 31) + x_tie - c_tie;
+#pragma unroll
+      for (int u = 0; u < kRegKeys; ++u) {
+        if ((m_above >> u) & 1u) {
+          if (p_sel < kMaxK) s_sel[p_sel] = key[u];
+          ++p_sel;
+        }
+        if ((m_tie >> u) & 1u) {
+          if (p_tie < kTieCap) s_tie[p_tie] = key[u];
+          ++p_tie;
+        }
+      }
+    } else {
+      for_each_segment_key(a, s_cnt, row, [&](bool active, uint64_t k) {
+        const int b = active ? bucket(k) : -1;
+        const unsigned ab = __ballot_sync(kFull, b > bstar), ti = __ballot_sync(kFull, b == bstar);
+        int p_sel = 0, p_tie = 0;
+        if (lane == 0) {
+          if (ab) p_sel = atomicAdd(&s_sel_n, __popc(ab));
+          if (ti) p_tie = atomicAdd(&s_tie_n, __popc(ti));
+        }
+        p_sel = __shfl_sync(kFull, p_sel, 0) + __popc(ab & below_me);
+        p_tie = __shfl_sync(kFull, p_tie, 0) + __popc(ti & below_me);
+        if (b > bstar && p_sel < kMaxK) s_sel[p_sel] = k;
+        if (b == bstar && p_tie < kTieCap) s_tie[p_tie] = k;
+      });
+    }
     __syncthreads();
     const int ties = s_tie_n, need = m - s_above;
     if (ties <= kTieCap) {
@@ -523,7 +647,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
       for (int shift = 56 - ((common / 8) * 8); shift >= 0 && need > 0; shift -= 8) {
         hist[tid] = 0;
         __syncthreads();
-        for_each_key(staged, n, s_keys, cnt, seg, tiles, [&](bool active, uint64_t k) {
+        visit([&](bool active, uint64_t k) {
           const int d = (active && (k & pmask) == prefix) ? (int)((k >> shift) & 255) : 256;
           const unsigned same = __match_any_sync(kFull, d);
           if (d < 256 && lane == __ffs(same) - 1) atomicAdd(&hist[d], __popc(same));
@@ -560,7 +684,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
       }
     }
     // the m largest keys are exactly those >= prefix
-    for_each_key(staged, n, s_keys, cnt, seg, tiles, [&](bool active, uint64_t k) {
+    visit([&](bool active, uint64_t k) {
       if (active && k >= prefix) {
         const int p = atomicAdd(&s_sel_n, 1);
         if (p < kMaxK) s_sel[p] = k;
@@ -570,26 +694,26 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const uint64_t
   }
   const int sel = m;
   // ---- sort the selected keys: warp-sorted lists of 32, then rank in the union
-  uint64_t key = tid < sel ? s_sel[tid] : 0ull;
-  key = warp_sort_desc(key, lane);
-  s_wl[warp][lane] = key;
+  uint64_t mine_key = tid < sel ? s_sel[tid] : 0ull;
+  mine_key = warp_sort_desc(mine_key, lane);
+  s_wl[warp][lane] = mine_key;
   __syncthreads();
-  int* io = idx_out + (long long)r * K;
-  float* to = top_out ? top_out + (long long)r * K : nullptr;
-  if (key != 0ull) {
+  int* io = a.idx + (long long)r * K;
+  float* to = a.top ? a.top + (long long)r * K : nullptr;
+  if (mine_key != 0ull) {
     int pos[kSelThreads / 32];
 #pragma unroll
     for (int w = 0; w < kSelThreads / 32; ++w) pos[w] = 0;
 #pragma unroll
     for (int step = 16; step > 0; step >>= 1)
 #pragma unroll
-      for (int w = 0; w < kSelThreads / 32; ++w) pos[w] += (s_wl[w][pos[w] + step] > key) ? step : 0;
+      for (int w = 0; w < kSelThreads / 32; ++w) pos[w] += (s_wl[w][pos[w] + step] > mine_key) ? step : 0;
     int rank = 0;
 #pragma unroll
-    for (int w = 0; w < kSelThreads / 32; ++w) rank += (s_wl[w][0] > key) ? pos[w] + 1 : 0;
+    for (int w = 0; w < kSelThreads / 32; ++w) rank += (s_wl[w][0] > mine_key) ? pos[w] + 1 : 0;
     if (rank < K) {
-      io[rank] = (int)key_index(key);
-      if (to) to[rank] = key_score(key);
+      io[rank] = (int)key_index(mine_key);
+      if (to) to[rank] = key_score(mine_key);
     }
   }
   for (int i = sel + tid; i < K; i += kSelThreads) {
@@ -631,36 +755,62 @@ cudaError_t setup_gemm() {
   return cudaSuccess;
 }
 
+// Work split of the shared-pool scorer: MT M-tiles of 128 anchors, P CTAs
+// per M-tile (one CTA per SM in all), CTA p of an M-tile taking tiles p,
+// p + P, ...; each (anchor, CTA) segment holds up to `cap` keys.
+struct PoolLayout {
+  int tiles, MT, P;
+  long long cap;
+  size_t counts_bytes, bytes;
+};
+
+PoolLayout pool_layout(int R, int N) {
+  PoolLayout L;
+  L.tiles = (N + kBN - 1) / kBN;
+  L.MT = (R + kBM - 1) / kBM;
+  L.P = L.tiles == 0 ? 0 : std::max(1, std::min(std::min(L.tiles, kMaxSegs), sm_count() / std::max(1, L.MT)));
+  L.cap = L.P == 0 ? 0 : (long long)((L.tiles + L.P - 1) / L.P) * kBN;
+  L.counts_bytes = (sizeof(int) * (size_t)R * (size_t)L.P + 255) & ~size_t(255);
+  L.bytes = L.counts_bytes + sizeof(uint64_t) * (size_t)R * (size_t)L.P * (size_t)L.cap;
+  return L;
+}
+
 }  // namespace
 
-size_t batched_workspace_bytes(int R, int N) {
-  const size_t tiles = ((size_t)N + kBN - 1) / kBN;
-  return ((sizeof(int) * (size_t)R * tiles + 255) & ~size_t(255)) + sizeof(uint64_t) * (size_t)R * tiles * kBN;
-}
+size_t batched_workspace_bytes(int R, int N) { return pool_layout(R, N).bytes; }
 
 cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask, int R,
                                       int N, int K, int* idx, float* top, void* ws, int* err,
                                       cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  const int tiles = (N + kBN - 1) / kBN;
+  const PoolLayout L = pool_layout(R, N);
   int* counts = static_cast<int*>(ws);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) +
-                                               ((sizeof(int) * (size_t)R * tiles + 255) & ~size_t(255)));
+  uint64_t* cand = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + L.counts_bytes);
   cudaError_t e = setup_gemm();
   if (e != cudaSuccess) return e;
-  if (N > 0) {
+  if (L.P > 0) {
     CUtensorMap ma, mv;
     if (!make_map(&ma, A, R) || !make_map(&mv, V, N)) return cudaErrorInvalidValue;
-    GemmArgs g{mask, R, N, (N + 31) / 32, tiles, counts, cand, err};
-    // one CTA per SM, split evenly across the M-tiles of the anchors
-    const int MT = (R + kBM - 1) / kBM;
-    const int P = std::max(1, std::min(tiles, sm_count() / MT));
-    score_pool_kernel<<<MT * P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
+    const int mask_words = (N + 31) / 32;
+    const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
+    GemmArgs g{mask, R, N, mask_words, L.tiles, counts, cand, L.cap, mask_vec, err};
+    score_pool_kernel<<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  select_rows_kernel<<<R, kSelThreads, sizeof(uint64_t) * kSelStage, s>>>(cand, counts, tiles, K, idx,
-                                                                          top, err);
-  return cudaGetLastError();
+  // programmatic dependent launch: the select grid is scheduled while the
+  // GEMM drains and waits (griddepcontrol.wait) for its results
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)R);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = sizeof(uint64_t) * kSelStage;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const SelArgs sa{cand, counts, L.P, L.cap, K, idx, top, err};
+  return cudaLaunchKernelEx(&cfg, select_rows_kernel, sa);
 }
 
 }  // namespace kk
