@@ -25,6 +25,14 @@ Cache 重要性评估" (cited below as [KK §n]):
   normalised so the weights sum to one.
 * [KK §5.1]: a coarse (Grid / Chunk) representation is the mean of its
   children's representations.
+* [KK §5.3]: the stability score of a block is the fraction of the last W
+  decode steps (W = 20 by default) in which its affinity exceeded the
+  threshold theta (0.5 by default); the page's example: one step at 0.9 and
+  nineteen at 0.2 give 1/20 = 0.05, twenty steps above 0.6 give 1.0. Reading
+  used here: "exceeded" is strict (a score equal to theta does not count),
+  the fraction is always over W (before W steps exist the missing steps count
+  as not high), and the loading decision ranks blocks by stability, then by
+  the current affinity, then by the lower index.
 
 Every function accumulates in float64. bf16 inputs are decoded exactly
 (bits << 16). Parity of the variance weighting and of the (1+cos)/2 formula
@@ -47,6 +55,8 @@ __all__ = [
     "score_topk",
     "score_pool_batched",
     "coarse_means",
+    "stability",
+    "stable_topk",
 ]
 
 
@@ -235,3 +245,32 @@ def coarse_means(vb_logical, group: int) -> np.ndarray:
     for g in range(ng):
         out[g] = vb_logical[g * group : min((g + 1) * group, nb)].mean(axis=0)
     return out
+
+
+def stability(score_history, W: int = 20, theta: float = 0.5) -> np.ndarray:
+    """Stability score of every block [KK §5.3]: over the last W decode steps
+    (``score_history`` oldest first, one score array per step), the number of
+    steps whose affinity was strictly above ``theta``, divided by W.
+    """
+    hist = np.asarray(score_history, dtype=np.float64)
+    if hist.ndim != 2:
+        raise ValueError("score_history must be [steps][blocks]")
+    recent = hist[max(0, hist.shape[0] - W):]
+    return (recent > theta).sum(axis=0) / float(W)
+
+
+def stable_topk(stab, scores, K: int):
+    """The K blocks to load under the stability filter [KK §5.3]: order by
+    stability descending, then by the current affinity descending, then by
+    the lower index. Slots beyond the candidates hold -1 / -inf.
+
+    Returns (idx int64 [K], current affinity float64 [K]).
+    """
+    stab = np.asarray(stab, dtype=np.float64)
+    s = np.asarray(scores, dtype=np.float64)
+    order = np.lexsort((np.arange(len(s)), -s, -stab))[:K]
+    idx = np.full(K, -1, dtype=np.int64)
+    val = np.full(K, -np.inf)
+    idx[: len(order)] = order
+    val[: len(order)] = s[order]
+    return idx, val

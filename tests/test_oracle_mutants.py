@@ -147,12 +147,39 @@ def m_batched_ignores_mask(o):
     o.score_pool_batched = score_pool_batched
 
 
+def m_stability_counts_equal_theta(o):
+    def stability(score_history, W=20, theta=0.5):
+        h = np.asarray(score_history, dtype=np.float64)
+        return (h[max(0, h.shape[0] - W):] >= theta).sum(axis=0) / float(W)
+    o.stability = stability
+
+
+def m_stability_divides_by_steps_seen(o):
+    def stability(score_history, W=20, theta=0.5):
+        h = np.asarray(score_history, dtype=np.float64)
+        recent = h[max(0, h.shape[0] - W):]
+        return (recent > theta).sum(axis=0) / float(recent.shape[0])
+    o.stability = stability
+
+
+def m_stability_window_one_too_long(o):
+    def stability(score_history, W=20, theta=0.5):
+        h = np.asarray(score_history, dtype=np.float64)
+        return (h[max(0, h.shape[0] - W - 1):] > theta).sum(axis=0) / float(W)
+    o.stability = stability
+
+
+def m_stable_topk_ignores_stability(o):
+    o.stable_topk = lambda stab, scores, K: ko.topk(scores, K)
+
+
 MUTANTS = [
     m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
     m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
     m_topk_ties_to_higher_index, m_topk_ascending, m_anchor_first_tokens,
     m_anchor_ignores_block_table, m_variance_one_mean_for_all_dims, m_variance_std_not_var,
-    m_coarse_last_group_divided_by_group, m_batched_ignores_mask,
+    m_coarse_last_group_divided_by_group, m_batched_ignores_mask, m_stability_counts_equal_theta,
+    m_stability_divides_by_steps_seen, m_stability_window_one_too_long, m_stable_topk_ignores_stability,
 ]
 
 

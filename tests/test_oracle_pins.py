@@ -260,11 +260,40 @@ def check_planted_topics(o):
                 assert s[same].min() > s[off].max()
 
 
+def check_stability_golden(o):
+    g = gold("stability.json")
+    for c in g["cases"]:
+        hist = np.array(c["history"], dtype=np.float64)[:, None]  # [steps][1 block]
+        got = o.stability(hist, g["W"], g["theta"])
+        assert abs(got[0] - c["stability"]) < 1e-15, c
+
+
+def check_stability_window(o):
+    # the threshold is strict, the fraction is over W, and the window slides
+    W, th = 4, 0.5
+    hist = np.array([[0.9, 0.5, 0.51, 0.0],
+                     [0.9, 0.5, 0.49, 0.0],
+                     [0.1, 0.5, 0.51, 0.0]])
+    np.testing.assert_array_equal(o.stability(hist, W, th), [2 / 4, 0.0, 2 / 4, 0.0])  # 3 steps, still over W
+    more = np.vstack([hist, [[0.1, 0.6, 0.1, 0.7]] * 2])  # 5 steps: the first drops out
+    np.testing.assert_array_equal(o.stability(more, W, th), [1 / 4, 2 / 4, 1 / 4, 2 / 4])
+    # W = 1: the indicator of the last step
+    np.testing.assert_array_equal(o.stability(more, 1, th), [0.0, 1.0, 0.0, 1.0])
+
+
+def check_stable_topk(o):
+    stab = [0.05, 1.0, 1.0, 0.5, 1.0]
+    scores = [0.9, 0.3, 0.7, 0.8, 0.7]
+    idx, val = o.stable_topk(stab, scores, 6)
+    assert list(idx) == [2, 4, 1, 3, 0, -1]  # stability, then affinity, then the lower index
+    assert [float(v) for v in val] == [0.7, 0.7, 0.3, 0.8, 0.9, float("-inf")]
+
+
 ALL_CHECKS = [
     check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
     check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
     check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,
-    check_planted_topics,
+    check_planted_topics, check_stability_golden, check_stability_window, check_stable_topk,
 ]
 
 
