@@ -199,6 +199,31 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
                          float* top_scores, float* scores, cudaStream_t stream);
 
 /*
+ * Stability filter [KK §5.3] fused into scoring: kk_score_topk and
+ * kk_select_step that also keep, per block, the last stab_window (1..32)
+ * steps' "score > theta" bits and rank the top K by their count (the
+ * block's stability is count / stab_window), then by the current score,
+ * then by the lower index.
+ * hist: device uint32 [offsets[R]], one word per logical block of the
+ *   table, caller-owned state that persists across steps: bit 0 is the
+ *   newest step. A block with no history starts at 0 (append a 0 word when
+ *   a request's table grows). Updated in place by every call.
+ * stab: nullable device float [offsets[R]]: count / stab_window after this
+ *   step's update.
+ * top_scores hold the current step's scores of the selected blocks.
+ * Requires max_blocks < 2^27 - 1 (KK_ERR_UNSUPPORTED otherwise); theta
+ * must be finite. Other arguments as in kk_score_topk / kk_select_step.
+ */
+kk_status kk_score_topk_stable(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                               const float* va, int32_t K, int32_t stab_window, float theta,
+                               uint32_t* hist, float* stab, int32_t* idx, float* top_scores, float* scores,
+                               cudaStream_t stream);
+kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                                const float* head_w, const float* vb, int32_t K, int32_t stab_window,
+                                float theta, uint32_t* hist, float* stab, float* va, int32_t* idx,
+                                float* top_scores, float* scores, cudaStream_t stream);
+
+/*
  * Shared-pool scoring [KK §5.1] (every representation against the anchors
  * in one matrix product, then a mask): R anchors A (device bf16 bits [R][D])
  * against N pooled block vectors V (device bf16 bits [N][D]); anchor r may

@@ -1,8 +1,10 @@
 // C ABI of the selector (include/kk.h): argument checks on the host, then
 // launches. Nothing here allocates device memory.
+#include <cmath>
 #include <mutex>
 
 #include "../../include/kk.h"
+
 #include "kk_internal.h"
 
 namespace {
@@ -257,6 +259,61 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
   if ((st = check_table(bt, true, &p.bt)) != KK_OK) return st;
   if (W < 1 || W > kk::kMaxW || K < 1 || K > kk::kMaxK || !vb || !idx) return KK_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
+  p.W = W;
+  p.head_w = head_w;
+  p.va_out = va;
+  p.vb = vb;
+  p.vb_rows = p.kc.num_pages;
+  p.D = p.kc.D;
+  p.K = K;
+  p.idx_out = idx;
+  p.top_out = top_scores;
+  p.scores_out = scores;
+  p.flags = kk::kStepAnchor | kk::kStepScore | kk::kStepTopK;
+  return step_common(p, stream);
+}
+
+// Stability-filter arguments shared by the two *_stable entry points.
+static kk_status stability_args(int32_t stab_window, float theta, uint32_t* hist, float* stab,
+                                kk::StepParams* p) {
+  if (stab_window < 1 || stab_window > 32 || !hist || !std::isfinite(theta)) return KK_ERR_INVALID;
+  if (p->bt.max_blocks > (int32_t)kk::kStabIdxMask - 1) return KK_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(hist) % 4 || reinterpret_cast<uintptr_t>(stab) % 4) return KK_ERR_INVALID;
+  p->hist = hist;
+  p->stab_out = stab;
+  p->stab_w = stab_window;
+  p->stab_theta = theta;
+  return KK_OK;
+}
+
+kk_status kk_score_topk_stable(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                               const float* va, int32_t K, int32_t stab_window, float theta,
+                               uint32_t* hist, float* stab, int32_t* idx, float* top_scores, float* scores,
+                               cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = score_args(vb, D, num_pages, bt, va, &p);
+  if (st != KK_OK) return st;
+  if (K < 1 || K > kk::kMaxK || !idx) return KK_ERR_INVALID;
+  if ((st = stability_args(stab_window, theta, hist, stab, &p)) != KK_OK) return st;
+  p.K = K;
+  p.idx_out = idx;
+  p.top_out = top_scores;
+  p.scores_out = scores;
+  p.flags = kk::kStepScore | kk::kStepTopK;
+  return step_common(p, stream);
+}
+
+kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
+                                const float* head_w, const float* vb, int32_t K, int32_t stab_window,
+                                float theta, uint32_t* hist, float* stab, float* va, int32_t* idx,
+                                float* top_scores, float* scores, cudaStream_t stream) {
+  kk::StepParams p = {};
+  kk_status st = check_kcache(kc, &p.kc);
+  if (st != KK_OK) return st;
+  if ((st = check_table(bt, true, &p.bt)) != KK_OK) return st;
+  if (W < 1 || W > kk::kMaxW || K < 1 || K > kk::kMaxK || !vb || !idx) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
+  if ((st = stability_args(stab_window, theta, hist, stab, &p)) != KK_OK) return st;
   p.W = W;
   p.head_w = head_w;
   p.va_out = va;

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kk_internal.h"
+
 namespace kk {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -82,6 +84,19 @@ __device__ __forceinline__ uint64_t make_key(float score, uint32_t idx) {
 }
 __device__ __forceinline__ uint32_t key_index(uint64_t k) { return ~(uint32_t)k; }
 __device__ __forceinline__ float key_score(uint64_t k) { return ordered_to_f32((uint32_t)(k >> 32)); }
+
+// Key of a candidate ranked by stability first: the count of high steps (6
+// bits), then the score (a non-negative float's 31 bits, which order like
+// the float), then the complement of the index in 27 bits. Indices stay
+// below 2^27 - 1, so a real key is never 0.
+__device__ __forceinline__ uint64_t make_stab_key(uint32_t high_steps, float score, uint32_t idx) {
+  const uint32_t sb = __float_as_uint(fmaxf(score, 0.f)) & 0x7FFFFFFFu;
+  return ((uint64_t)high_steps << 58) | ((uint64_t)sb << kStabIdxBits) | (uint64_t)(kStabIdxMask - idx);
+}
+__device__ __forceinline__ uint32_t stab_key_index(uint64_t k) { return kStabIdxMask - (uint32_t)(k & kStabIdxMask); }
+__device__ __forceinline__ float stab_key_score(uint64_t k) {
+  return __uint_as_float((uint32_t)(k >> kStabIdxBits) & 0x7FFFFFFFu);
+}
 
 // Bitonic sort of one key per lane across a warp, descending (lane 0 largest).
 __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {

@@ -13,6 +13,10 @@ constexpr int kMergeSlots = 2048;  // cluster size * K
 
 enum ErrorCode { kErrBadIndex = 4, kErrTimeout = 5 };
 
+// Stability-ranked keys keep a block index in 27 bits (see make_stab_key).
+constexpr int kStabIdxBits = 27;
+constexpr uint32_t kStabIdxMask = (1u << kStabIdxBits) - 1u;
+
 struct KCache {
   const void* base;
   int dtype;  // 0 f32, 1 bf16
@@ -64,6 +68,12 @@ struct StepParams {
   int* idx_out;      // [R][K]
   float* top_out;    // [R][K] or null
   int flags;
+  // stability filter (nullable): per logical block, the last stab_w steps'
+  // "score > stab_theta" bits (newest in bit 0); ranks by their count first
+  uint32_t* hist;
+  float* stab_out;
+  int stab_w;
+  float stab_theta;
   int* err;
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);

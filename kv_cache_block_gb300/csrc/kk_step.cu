@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   const bool do_score = p.flags & kStepScore;
   const bool do_topk = p.flags & kStepTopK;
   const bool from_scores = p.flags & kStepTopKFromScores;
+  const bool stab = p.hist != nullptr;  // keys ranked by stability (score mode only)
   const int K = p.K;
   const int Kp = K <= 1 ? 1 : 1 << (32 - __clz(K - 1));  // next power of two >= K
 
@@ -321,7 +322,20 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
               const float sc = fmaf(0.5f, cosv, 0.5f);
               const int j = tile0 + slot;
               if (p.scores_out) p.scores_out[off + j] = sc;
-              sm.keys[slot] = sm.pg[slot] >= 0 ? make_key(sc, (uint32_t)j) : 0ull;
+              uint64_t key = 0ull;
+              if (sm.pg[slot] >= 0) {
+                if (p.hist) {
+                  // stability filter: shift this step's bit into the block's window
+                  const uint32_t wmask = p.stab_w >= 32 ? 0xFFFFFFFFu : ((1u << p.stab_w) - 1u);
+                  const uint32_t h = ((p.hist[off + j] << 1) | (sc > p.stab_theta ? 1u : 0u)) & wmask;
+                  p.hist[off + j] = h;
+                  if (p.stab_out) p.stab_out[off + j] = (float)__popc(h) / (float)p.stab_w;
+                  key = make_stab_key((uint32_t)__popc(h), sc, (uint32_t)j);
+                } else {
+                  key = make_key(sc, (uint32_t)j);
+                }
+              }
+              sm.keys[slot] = key;
             }
           }
         }
@@ -388,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       for (int i = tid; i < K; i += kThreads) {
         const bool have = i < run_n;
         const uint64_t k = have ? sm.run[cur][i] : 0ull;
-        idx_out[i] = have ? (int)key_index(k) : -1;
-        if (top_out) top_out[i] = have ? key_score(k) : -__int_as_float(0x7f800000);
+        idx_out[i] = have ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
+        if (top_out) top_out[i] = have ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
       }
     } else {
       if (!start_waited) {
@@ -415,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         int cnt = count_greater_pow2(&sm.merge[list * Kp], Kp, k);
         for (int o = 1; o < CL; o <<= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
         if (have && list == 0 && cnt < K) {
-          idx_out[cnt] = (int)key_index(k);
-          if (top_out) top_out[cnt] = key_score(k);
+          idx_out[cnt] = (int)(stab ? stab_key_index(k) : key_index(k));
+          if (top_out) top_out[cnt] = stab ? stab_key_score(k) : key_score(k);
         }
       }
       if (crank == 0) {

@@ -73,6 +73,8 @@ def _load():
         "kk_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
         "kk_score_topk": (ctypes.c_int, [P, I32, I32, BT, P, I32, P, P, P, P]),
         "kk_select_step": (ctypes.c_int, [KC, BT, I32, P, P, I32, P, P, P, P, P]),
+        "kk_score_topk_stable": (ctypes.c_int, [P, I32, I32, BT, P, I32, I32, F, P, P, P, P, P, P]),
+        "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, P]),
         "kk_score_pool_batched_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
         "kk_coarse_means": (ctypes.c_int, [P, I32, I32, BT, I32, P, P]),
@@ -91,7 +93,8 @@ _lib = _load()
 EXPORTS = (
     "kk_status_str", "kk_device_error", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
     "kk_head_variance", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static", "kk_anchor", "kk_score", "kk_topk",
-    "kk_score_topk", "kk_select_step", "kk_score_pool_batched_workspace_bytes",
+    "kk_score_topk", "kk_select_step", "kk_score_topk_stable", "kk_select_step_stable",
+    "kk_score_pool_batched_workspace_bytes",
     "kk_score_pool_batched", "kk_coarse_means",
 )
 
@@ -227,6 +230,26 @@ def kk_select_step(kc, bt: BlockTable, W: int, vb, K: int, idx, top_scores=None,
     _check("kk_select_step", _lib.kk_select_step(
         ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
         _ptr(vb, torch.float32, "vb"), K, _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
+        _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _stream(stream)))
+
+
+def kk_score_topk_stable(vb, bt: BlockTable, va, K: int, stab_window: int, theta: float, hist, idx,
+                         stab=None, top_scores=None, scores=None, stream=None):
+    """``hist``: int32 tensor [offsets[R]] holding the uint32 history words (updated in place)."""
+    _check("kk_score_topk_stable", _lib.kk_score_topk_stable(
+        _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c), _ptr(va, torch.float32, "va"),
+        K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"), _ptr(stab, torch.float32, "stab"),
+        _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"),
+        _ptr(scores, torch.float32, "scores"), _stream(stream)))
+
+
+def kk_select_step_stable(kc, bt: BlockTable, W: int, vb, K: int, stab_window: int, theta: float, hist, idx,
+                          stab=None, top_scores=None, va=None, scores=None, head_w=None, stream=None):
+    """``hist``: int32 tensor [offsets[R]] holding the uint32 history words (updated in place)."""
+    _check("kk_select_step_stable", _lib.kk_select_step_stable(
+        ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
+        _ptr(vb, torch.float32, "vb"), K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"),
+        _ptr(stab, torch.float32, "stab"), _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
         _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _stream(stream)))
 
 

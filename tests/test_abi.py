@@ -100,6 +100,20 @@ def test_host_argument_errors(kk):
     # kk_select_step
     assert lib.kk_select_step(B(d), B(t), 8, None, None, 4, None, 16, None, None, None) == kk.KK_ERR_INVALID
     assert lib.kk_select_step(B(d), B(t), 8, None, 16, 0, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    # stability filter: window, history words, threshold, table size
+    f = float
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 0, f(0.5), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 33, f(0.5), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), None, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("nan"), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("inf"), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), 18, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(_table(kk, max_blocks=1 << 27)), 16, 4, 20, f(0.5), 16, None, 16,
+                                    None, None, None) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 0, f(0.5), 16, None, None, 16, None, None,
+                                     None) == kk.KK_ERR_INVALID
+    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 20, f(0.5), None, None, None, 16, None, None,
+                                     None) == kk.KK_ERR_INVALID
     # kk_head_variance: workspace too small / missing output
     assert lib.kk_head_variance(B(d), B(t), 4, 16, 256, 1, None) == kk.KK_ERR_INVALID
     assert lib.kk_head_variance(B(d), B(t), 4, None, 256, 1 << 30, None) == kk.KK_ERR_INVALID
