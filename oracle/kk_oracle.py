@@ -25,6 +25,12 @@ Cache 重要性评估" (cited below as [KK §n]):
   normalised so the weights sum to one.
 * [KK §5.1]: a coarse (Grid / Chunk) representation is the mean of its
   children's representations.
+* [KK §5.2 step 4]: only the selected blocks are loaded for attention. The
+  compact table lists the physical pages of the selected blocks in logical
+  order (the order a paged-attention kernel walks them), -1 padded.
+* [KK §5.2 step 2], [KK §2.2 step 1]: v_b is computed when the block is
+  written. Maintained incrementally, after each appended token the block's
+  v_b equals the pooled mean of the tokens it holds so far.
 * [KK §5.3]: the stability score of a block is the fraction of the last W
   decode steps (W = 20 by default) in which its affinity exceeded the
   threshold theta (0.5 by default); the page's example: one step at 0.9 and
@@ -57,6 +63,8 @@ __all__ = [
     "coarse_means",
     "stability",
     "stable_topk",
+    "compact_table",
+    "append_token",
 ]
 
 
@@ -274,3 +282,39 @@ def stable_topk(stab, scores, K: int):
     idx[: len(order)] = order
     val[: len(order)] = s[order]
     return idx, val
+
+
+def compact_table(pages_r, idx_r):
+    """The selected blocks of one request as a table for attention
+    [KK §5.2 step 4]: their logical indices in ascending order, the physical
+    pages in that order, and their number. Entries of ``idx_r`` that are -1
+    (empty top-K slots) are skipped; slots past the count hold -1.
+
+    Returns (pages int64 [len(idx_r)], logical int64 [len(idx_r)], count).
+    """
+    pages_r = np.asarray(pages_r, dtype=np.int64)
+    idx_r = np.asarray(idx_r, dtype=np.int64)
+    chosen = np.sort(idx_r[idx_r >= 0])
+    n = len(chosen)
+    logical = np.full(len(idx_r), -1, dtype=np.int64)
+    pages = np.full(len(idx_r), -1, dtype=np.int64)
+    logical[:n] = chosen
+    pages[:n] = pages_r[chosen]
+    return pages, logical, n
+
+
+def append_token(kc, pages_r, seq_len: int, bs: int, k_new, head_w=None):
+    """Write one decode token's Keys into the paged cache and return the new
+    v_b of the block that holds it [KK §5.2 step 2].
+
+    kc: the cache view [L][P][H][bs][D] (float32 or bf16 bits), modified in
+    place; seq_len: the request's length after the append (the token sits at
+    position seq_len - 1); k_new: [L][H][D] in the cache's storage type.
+    Returns (physical page, v_b float64 [D]): the pooled mean of the block's
+    tokens so far, i.e. pool_block over its first (seq_len - 1) % bs + 1 tokens.
+    """
+    t = seq_len - 1
+    page = int(np.asarray(pages_r)[t // bs])
+    slot = t % bs
+    kc[:, page, :, slot, :] = k_new
+    return page, pool_block(block_keys(kc, page, slot + 1), head_w)

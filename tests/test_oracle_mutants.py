@@ -173,6 +173,38 @@ def m_stable_topk_ignores_stability(o):
     o.stable_topk = lambda stab, scores, K: ko.topk(scores, K)
 
 
+def m_compact_table_keeps_topk_order(o):
+    def compact_table(pages_r, idx_r):
+        pages_r = np.asarray(pages_r, dtype=np.int64)
+        idx_r = np.asarray(idx_r, dtype=np.int64)
+        chosen = idx_r[idx_r >= 0]
+        logical = np.full(len(idx_r), -1, dtype=np.int64)
+        pages = np.full(len(idx_r), -1, dtype=np.int64)
+        logical[:len(chosen)] = chosen
+        pages[:len(chosen)] = pages_r[chosen]
+        return pages, logical, len(chosen)
+    o.compact_table = compact_table
+
+
+def m_append_token_divides_by_block_size(o):
+    def append_token(kc, pages_r, seq_len, bs, k_new, head_w=None):
+        t = seq_len - 1
+        page = int(np.asarray(pages_r)[t // bs])
+        kc[:, page, :, t % bs, :] = k_new
+        v = ko.pool_block(ko.block_keys(kc, page, t % bs + 1), head_w)
+        return page, v * (t % bs + 1) / bs
+    o.append_token = append_token
+
+
+def m_append_token_slot_off_by_one(o):
+    def append_token(kc, pages_r, seq_len, bs, k_new, head_w=None):
+        page = int(np.asarray(pages_r)[(seq_len - 1) // bs])
+        slot = seq_len % bs
+        kc[:, page, :, slot, :] = k_new
+        return page, ko.pool_block(ko.block_keys(kc, page, slot + 1), head_w)
+    o.append_token = append_token
+
+
 MUTANTS = [
     m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
     m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
@@ -180,6 +212,7 @@ MUTANTS = [
     m_anchor_ignores_block_table, m_variance_one_mean_for_all_dims, m_variance_std_not_var,
     m_coarse_last_group_divided_by_group, m_batched_ignores_mask, m_stability_counts_equal_theta,
     m_stability_divides_by_steps_seen, m_stability_window_one_too_long, m_stable_topk_ignores_stability,
+    m_compact_table_keeps_topk_order, m_append_token_divides_by_block_size, m_append_token_slot_off_by_one,
 ]
 
 

@@ -289,11 +289,43 @@ def check_stable_topk(o):
     assert [float(v) for v in val] == [0.7, 0.7, 0.3, 0.8, 0.9, float("-inf")]
 
 
+def check_compact_table_golden(o):
+    g = gold("compact_table.json")
+    for c in g["cases"]:
+        pages, logical, n = o.compact_table(g["pages"], c["idx"])
+        assert list(pages) == c["pages"] and list(logical) == c["logical"] and n == c["count"], c
+
+
+def check_append_token(o):
+    # one layer, one head, D = 2, block size 3: hand-computed running means
+    kc = np.full((1, 3, 1, 3, 2), np.nan)
+    pages_r = [2, 0]
+    toks = [[2.0, 4.0], [4.0, 0.0], [0.0, 8.0], [6.0, -2.0]]
+    want = [(2, [2.0, 4.0]), (2, [3.0, 2.0]), (2, [2.0, 4.0]), (0, [6.0, -2.0])]
+    for t, (k, (pg, vb)) in enumerate(zip(toks, want)):
+        page, got = o.append_token(kc, pages_r, t + 1, 3, np.array(k).reshape(1, 1, 2))
+        assert page == pg and np.array_equal(got, vb), (t, page, got)
+    assert np.array_equal(kc[0, 2, 0], [[2, 4], [4, 0], [0, 8]]) and np.array_equal(kc[0, 0, 0, 0], [6, -2])
+    assert np.isnan(kc[0, 0, 0, 1:]).all() and np.isnan(kc[0, 1]).all()  # nothing else written
+    # a block filled token by token equals the block pooled at once (weighted too)
+    spec = synth.tiny_05b(L=2, H=3, D=4, bs=5, seq_lens=[5 * 3], num_topics=2, W=2, K=2)
+    full = synth.view_paged(synth.gen_paged_numpy(spec), spec)
+    kc = np.full_like(full, np.nan)
+    w = np.arange(1.0, 7.0) / 21.0
+    pr = spec.pages_of(0)
+    for t in range(spec.seq_lens[0]):
+        j, slot = divmod(t, spec.bs)
+        page, got = o.append_token(kc, pr, t + 1, spec.bs, full[:, pr[j], :, slot, :], w)
+        want = o.pool_blocks(full, [pr[j]], [slot + 1], [w], [0])[0]
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
     check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
     check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,
     check_planted_topics, check_stability_golden, check_stability_window, check_stable_topk,
+    check_compact_table_golden, check_append_token,
 ]
 
 
