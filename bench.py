@@ -337,6 +337,23 @@ def run_gpu(args, spec, rank, world, local_rank):
     except Exception as exc:  # noqa: BLE001
         graph_us = None
         print(f"cuda graph capture failed: {exc}", file=sys.stderr)
+    # the same step with the stability filter (history words updated in place)
+    hist = torch.zeros(spec.total_blocks, dtype=torch.int32, device=dev)
+    stab = torch.zeros(spec.total_blocks, device=dev)
+
+    def select_stable():
+        kk.kk_select_step_stable(desc, bt, spec.W, vb, spec.K, 20, 0.5, hist, idx, stab=stab, top_scores=top,
+                                 head_w=head_w)
+
+    for _ in range(5):
+        select_stable()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n_sel):
+        select_stable()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sel_stable_us = e0.elapsed_time(e1) * 1e3 / n_sel
     if kk.kk_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -370,6 +387,7 @@ def run_gpu(args, spec, rank, world, local_rank):
     return {
         "pool_ms": statistics.mean(pool_ms), "select_ms": statistics.mean(sel_ms), "step_ms": statistics.mean(step_ms),
         "total_ms": total_ms, "wall_s": t_end - t_start, "sel_b2b_us": sel_back_to_back_us, "sel_graph_us": graph_us,
+        "sel_stable_us": sel_stable_us,
         "clocks": clocks.summary(), "e2e": e2e, "launches": launches_per_step * args.steps,
     }
 
@@ -506,6 +524,7 @@ def main():
         "blocks_scored_per_s": spec.total_blocks / (res["select_ms"] * 1e-3),
         "score_topk_us_per_step": res["select_ms"] * 1e3,
         "score_topk_us_back_to_back": res["sel_b2b_us"], "score_topk_us_cuda_graph": res["sel_graph_us"],
+        "score_topk_stable_us_back_to_back": res["sel_stable_us"],
         "pool_ms_per_step": res["pool_ms"], "clocks": res["clocks"], "gpu_launches": res["launches"],
         "e2e": res["e2e"],
     }

@@ -224,6 +224,40 @@ kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* 
                                 float* top_scores, float* scores, cudaStream_t stream);
 
 /*
+ * The selected blocks as a table for the attention kernel [KK §5.2 step 4]
+ * (only they are loaded): for request r, the valid entries of
+ * idx[r][0..K) (logical block indices as kk_topk writes them; -1 slots are
+ * skipped) sorted ascending, their physical pages
+ *   sel_pages[r][i] = pages[offsets[r] + logical_i]      (device int32 [R][K])
+ * and optionally the logical indices sel_logical[r][i] (device int32 [R][K])
+ * and their number sel_count[r] (device int32 [R]); slots past the count
+ * are -1. An index outside [-1, nb_r) is skipped and reported through the
+ * device error word. 1 <= K <= 256.
+ */
+kk_status kk_compact_table(const int32_t* idx, int32_t K, const kk_block_table* bt, int32_t* sel_pages,
+                           int32_t* sel_logical, int32_t* sel_count, cudaStream_t stream);
+
+/*
+ * Incremental write-path pooling [KK §5.2 step 2] (v_b computed as the
+ * block is written), fused with the write of the Keys: for every request r,
+ * the decode token at position seq_lens[r] - 1 (seq_lens counts it; the
+ * table already holds its block) has its Keys k_new[r] (device, the cache's
+ * element type, [R][L][H][D], 16-byte aligned) written into slot
+ * (seq_lens[r] - 1) % block_size of its page in the cache at kc->base
+ * (which this call writes), and
+ *   block_sum[p][d] = sum over the block's tokens so far and (l, h) of
+ *                     w_lh * K[l][p][h][t][d]   (restarted at slot 0)
+ *   vb[p][d]        = block_sum[p][d] / n_p      (/ (L*H) when head_w is NULL)
+ * with w = head_w[r] (device float [R][L*H]) or 1. block_sum: device float
+ * [num_pages][D], caller-owned state carried from token to token; vb: the
+ * v_b table of kk_pool_blocks. A request whose table disagrees with seq_lens
+ * or holds a bad page is skipped and reported through the device error word.
+ * Blocks must not be shared between the requests of one call.
+ */
+kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, const void* k_new,
+                           const float* head_w, float* block_sum, float* vb, cudaStream_t stream);
+
+/*
  * Shared-pool scoring [KK §5.1] (every representation against the anchors
  * in one matrix product, then a mask): R anchors A (device bf16 bits [R][D])
  * against N pooled block vectors V (device bf16 bits [N][D]); anchor r may

@@ -328,6 +328,31 @@ kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* 
   return step_common(p, stream);
 }
 
+kk_status kk_compact_table(const int32_t* idx, int32_t K, const kk_block_table* bt, int32_t* sel_pages,
+                           int32_t* sel_logical, int32_t* sel_count, cudaStream_t stream) {
+  kk::Table t;
+  kk_status st = check_table(bt, false, &t);
+  if (st != KK_OK) return st;
+  if (K < 1 || K > kk::kMaxK || (t.R > 0 && (!idx || !sel_pages))) return KK_ERR_INVALID;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_compact_table(idx, K, t, sel_pages, sel_logical, sel_count, err, stream));
+}
+
+kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, const void* k_new,
+                           const float* head_w, float* block_sum, float* vb, cudaStream_t stream) {
+  kk::KCache c;
+  kk_status st = check_kcache(kc, &c);
+  if (st != KK_OK) return st;
+  kk::Table t;
+  if ((st = check_table(bt, true, &t)) != KK_OK) return st;
+  if (t.R > 0 && (!k_new || !block_sum || !vb)) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(k_new) % 16) return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_append(c, t, k_new, head_w, block_sum, vb, err, stream));
+}
+
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {
   (void)K;
   if (R < 0 || N < 0) return 0;

@@ -84,6 +84,12 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
                                       int N, int K, int* idx, float* top, void* ws, int* err,
                                       cudaStream_t s);
 
+// kk_write.cu
+cudaError_t launch_compact_table(const int* idx, int K, const Table& bt, int* out_pages, int* out_logical,
+                                 int* out_count, int* err, cudaStream_t s);
+cudaError_t launch_append(const KCache& kc, const Table& bt, const void* k_new, const float* head_w,
+                          float* block_sum, float* vb, int* err, cudaStream_t s);
+
 // kk_host.cu
 void* tensor_map_encoder();  // cuTensorMapEncodeTiled (driver ABI 12.0), or null
 int sm_count();              // SMs of the current device

@@ -1,0 +1,161 @@
+// The write side around a decode step ("Key-Key Semantic Affinity" page):
+//  * compact_table_kernel: the selected blocks of each request as a table for
+//    the attention kernel, physical pages in logical order (§5.2 step 4: only
+//    the selected blocks are loaded);
+//  * append_kernel: one decode token per request written into its block of
+//    the paged cache and folded into that block's running sum, so v_b is the
+//    pooled mean of the block's tokens after every token (§5.2 step 2, v_b
+//    computed as the block is written; §2.2 step 1).
+#include "kk_device.cuh"
+#include "kk_internal.h"
+
+namespace kk {
+namespace {
+
+constexpr int kThreads = 256;
+
+// One CTA per request, one thread per top-K slot (K <= 256): a slot's place
+// in the table is the number of valid slots with a smaller logical index
+// (equal indices by slot order).
+__global__ void __launch_bounds__(kThreads) compact_table_kernel(const int* idx, int K, Table bt, int* out_pages,
+                                                                 int* out_logical, int* out_count, int* err) {
+  __shared__ int s_v[kMaxK];
+  __shared__ int s_n;
+  const int r = blockIdx.x, t = threadIdx.x;
+  const int off = bt.offsets[r];
+  int nb = bt.offsets[r + 1] - off;
+  if (nb < 0 || nb > bt.max_blocks) {
+    if (t == 0) flag_error(err, kErrBadIndex);
+    nb = 0;
+  }
+  if (t == 0) s_n = 0;
+  int v = -1;
+  if (t < K) {
+    v = idx[(long long)r * K + t];
+    if (v < -1 || v >= nb) {
+      flag_error(err, kErrBadIndex);
+      v = -1;
+    }
+    s_v[t] = v;
+  }
+  __syncthreads();
+  if (v >= 0) atomicAdd(&s_n, 1);
+  int rank = 0;
+  if (v >= 0)
+    for (int u = 0; u < K; ++u) {
+      const int w = s_v[u];
+      rank += (w >= 0 && (w < v || (w == v && u < t))) ? 1 : 0;
+    }
+  __syncthreads();
+  const int n = s_n;
+  int* op = out_pages + (long long)r * K;
+  int* ol = out_logical ? out_logical + (long long)r * K : nullptr;
+  if (v >= 0) {
+    op[rank] = bt.pages[off + v];
+    if (ol) ol[rank] = v;
+  }
+  for (int i = n + t; i < K; i += kThreads) {
+    op[i] = -1;
+    if (ol) ol[i] = -1;
+  }
+  if (t == 0 && out_count) out_count[r] = n;
+}
+
+// One CTA per request. The new token's Keys k_new[r] ([L][H][D], the cache's
+// element type) are copied 16 bytes at a time into slot (T-1) % bs of the
+// block holding position T-1, and summed over (layer, head) with the
+// request's weights (uniform when head_w is null); the block's running sum
+// restarts at its first token, and v_b = sum / n (/ (L*H) unweighted).
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) append_kernel(KCache kc, Table bt, const void* k_new, const float* head_w,
+                                                          float* block_sum, float* vb, int* err) {
+  constexpr int EPV = Vec16<T>::kElems;
+  constexpr int V16 = D / EPV;  // 16-byte vectors per row
+  constexpr int RSTEP = kThreads / V16;
+  constexpr int ES = elem_bytes<T>();
+  static_assert(V16 >= 1 && V16 <= 32 && (32 % V16) == 0, "row must be 16..512 bytes");
+  __shared__ float s_red[RSTEP][D];
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int off = bt.offsets[r];
+  const int nb = bt.offsets[r + 1] - off;
+  const int T_r = bt.seq_lens[r];
+  if (T_r < 1 || nb > bt.max_blocks || nb != (T_r + kc.bs - 1) / kc.bs) {
+    if (tid == 0) flag_error(err, kErrBadIndex);
+    return;
+  }
+  const int t = T_r - 1, slot = t % kc.bs;
+  const int page = bt.pages[off + t / kc.bs];
+  if (page < 0 || page >= kc.num_pages) {
+    if (tid == 0) flag_error(err, kErrBadIndex);
+    return;
+  }
+  const int LH = kc.L * kc.H;
+  const int vec = tid % V16, s0 = tid / V16;
+  const char* src = static_cast<const char*>(k_new) + (long long)r * LH * D * ES;  // byte offsets: T is a tag
+  char* base = reinterpret_cast<char*>(const_cast<void*>(kc.base));
+  float acc[EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+  for (int s = s0; s < LH; s += RSTEP) {
+    const int l = s / kc.H, h = s - l * kc.H;
+    const uint4 x = *reinterpret_cast<const uint4*>(src + ((long long)s * D + vec * EPV) * ES);
+    char* dst = base + ((long long)l * kc.sL + (long long)page * kc.sP + (long long)h * kc.sH +
+                        (long long)slot * kc.sT + vec * EPV) * ES;
+    *reinterpret_cast<uint4*>(dst) = x;
+    float f[EPV];
+    Vec16<T>::unpack(x, f);
+    const float w = head_w ? head_w[(long long)r * LH + s] : 1.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) s_red[s0][vec * EPV + e] = acc[e];
+  __syncthreads();
+  const float scale = head_w ? 1.f / (float)(slot + 1) : 1.f / ((float)(slot + 1) * (float)LH);
+  for (int d = tid; d < D; d += kThreads) {
+    float x = 0.f;
+    for (int q = 0; q < RSTEP; ++q) x += s_red[q][d];
+    float* sum = block_sum + (long long)page * D + d;
+    const float total = slot == 0 ? x : *sum + x;
+    *sum = total;
+    vb[(long long)page * D + d] = total * scale;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_append_t(const KCache& kc, const Table& bt, const void* k_new, const float* head_w,
+                            float* block_sum, float* vb, int* err, cudaStream_t s) {
+  append_kernel<T, D><<<bt.R, kThreads, 0, s>>>(kc, bt, k_new, head_w, block_sum, vb, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compact_table(const int* idx, int K, const Table& bt, int* out_pages, int* out_logical,
+                                 int* out_count, int* err, cudaStream_t s) {
+  if (bt.R == 0) return cudaSuccess;
+  compact_table_kernel<<<bt.R, kThreads, 0, s>>>(idx, K, bt, out_pages, out_logical, out_count, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const KCache& kc, const Table& bt, const void* k_new, const float* head_w,
+                          float* block_sum, float* vb, int* err, cudaStream_t s) {
+  if (bt.R == 0) return cudaSuccess;
+  if (kc.dtype == 1) {
+    switch (kc.D) {
+      case 32: return launch_append_t<bf16_t, 32>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+      case 64: return launch_append_t<bf16_t, 64>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+      case 128: return launch_append_t<bf16_t, 128>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+      case 256: return launch_append_t<bf16_t, 256>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+    }
+  } else {
+    switch (kc.D) {
+      case 32: return launch_append_t<float, 32>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+      case 64: return launch_append_t<float, 64>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+      case 128: return launch_append_t<float, 128>(kc, bt, k_new, head_w, block_sum, vb, err, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kk

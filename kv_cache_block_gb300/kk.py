@@ -75,6 +75,8 @@ def _load():
         "kk_select_step": (ctypes.c_int, [KC, BT, I32, P, P, I32, P, P, P, P, P]),
         "kk_score_topk_stable": (ctypes.c_int, [P, I32, I32, BT, P, I32, I32, F, P, P, P, P, P, P]),
         "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, P]),
+        "kk_compact_table": (ctypes.c_int, [P, I32, BT, P, P, P, P]),
+        "kk_append_tokens": (ctypes.c_int, [KC, BT, P, P, P, P, P]),
         "kk_score_pool_batched_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
         "kk_coarse_means": (ctypes.c_int, [P, I32, I32, BT, I32, P, P]),
@@ -94,7 +96,7 @@ EXPORTS = (
     "kk_status_str", "kk_device_error", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
     "kk_head_variance", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static", "kk_anchor", "kk_score", "kk_topk",
     "kk_score_topk", "kk_select_step", "kk_score_topk_stable", "kk_select_step_stable",
-    "kk_score_pool_batched_workspace_bytes",
+    "kk_compact_table", "kk_append_tokens", "kk_score_pool_batched_workspace_bytes",
     "kk_score_pool_batched", "kk_coarse_means",
 )
 
@@ -251,6 +253,21 @@ def kk_select_step_stable(kc, bt: BlockTable, W: int, vb, K: int, stab_window: i
         _ptr(vb, torch.float32, "vb"), K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"),
         _ptr(stab, torch.float32, "stab"), _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
         _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _stream(stream)))
+
+
+def kk_compact_table(idx, bt: BlockTable, sel_pages, sel_logical=None, sel_count=None, stream=None):
+    _check("kk_compact_table", _lib.kk_compact_table(
+        _ptr(idx, torch.int32, "idx"), idx.shape[1], ctypes.byref(bt.c), _ptr(sel_pages, torch.int32, "sel_pages"),
+        _ptr(sel_logical, torch.int32, "sel_logical"), _ptr(sel_count, torch.int32, "sel_count"), _stream(stream)))
+
+
+def kk_append_tokens(kc, bt: BlockTable, k_new, block_sum, vb, head_w=None, stream=None):
+    """``k_new``: [R][L][H][D] tensor of the cache's element type (int16 bf16 bits or float32)."""
+    if not k_new.is_cuda or not k_new.is_contiguous():
+        raise ValueError("k_new must be a contiguous CUDA tensor")
+    _check("kk_append_tokens", _lib.kk_append_tokens(
+        ctypes.byref(kc), ctypes.byref(bt.c), ctypes.c_void_p(k_new.data_ptr()), _ptr(head_w, torch.float32, "head_w"),
+        _ptr(block_sum, torch.float32, "block_sum"), _ptr(vb, torch.float32, "vb"), _stream(stream)))
 
 
 def kk_score_pool_batched_workspace_bytes(R: int, N: int, K: int) -> int:
