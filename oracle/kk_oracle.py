@@ -31,6 +31,15 @@ Cache 重要性评估" (cited below as [KK §n]):
 * [KK §5.2 step 2], [KK §2.2 step 1]: v_b is computed when the block is
   written. Maintained incrementally, after each appended token the block's
   v_b equals the pooled mean of the tokens it holds so far.
+* [KK §5.1]: hierarchical selection Grid -> Chunk -> Page. Readings used
+  here: a Chunk is 64 consecutive pages and a Grid 8 consecutive Chunks of a
+  request (the page fixes neither); a Chunk's representation is the mean of
+  its pages' v_b and a Grid's the mean of its Chunks' representations; every
+  level is scored with the same affinity; a level keeps ceil(rate * n) of
+  its n active members (rates 50 %, 20 %, 10 %: of the active children, which
+  gives the page's 1 % of the cache), the children of unselected parents are
+  excluded (their scores "set to zero" on the page, read as masked out), and
+  ties go to the lower index.
 * [KK §5.3]: the stability score of a block is the fraction of the last W
   decode steps (W = 20 by default) in which its affinity exceeded the
   threshold theta (0.5 by default); the page's example: one step at 0.9 and
@@ -65,6 +74,8 @@ __all__ = [
     "stable_topk",
     "compact_table",
     "append_token",
+    "hier_reps",
+    "hier_select",
 ]
 
 
@@ -318,3 +329,54 @@ def append_token(kc, pages_r, seq_len: int, bs: int, k_new, head_w=None):
     slot = t % bs
     kc[:, page, :, slot, :] = k_new
     return page, pool_block(block_keys(kc, page, slot + 1), head_w)
+
+
+def hier_reps(vb_logical, chunk_pages: int = 64, grid_chunks: int = 8):
+    """Chunk and Grid representations of one request [KK §5.1]: a Chunk is
+    the mean of its pages' v_b, a Grid the mean of its Chunks'
+    representations (the last of each may be partial).
+
+    vb_logical: [nb][D] in logical order. Returns (chunks [C][D], grids [G][D]).
+    """
+    chunks = coarse_means(vb_logical, chunk_pages)
+    grids = coarse_means(chunks, grid_chunks) if len(chunks) else np.zeros((0, chunks.shape[1]))
+    return chunks, grids
+
+
+def _keep(scores, members, permille: int):
+    """The ceil(n * permille / 1000) members with the highest scores (ties:
+    lower index); integer arithmetic, so the count is exact."""
+    members = np.asarray(members, dtype=np.int64)
+    n = len(members)
+    k = -(-n * int(permille) // 1000)
+    order = np.lexsort((members, -np.asarray(scores, dtype=np.float64)[members]))
+    return members[order[:k]]
+
+
+def hier_select(vb_logical, va, K: int, chunk_pages: int = 64, grid_chunks: int = 8,
+                permille=(500, 200, 100)):
+    """Hierarchical selection of one request's pages [KK §5.1]: score the
+    Grids and keep the best share of them, then score only the Chunks of the
+    kept Grids and keep the best share of those, then the pages of the kept
+    Chunks likewise. The kept pages are returned in the order of kk_topk
+    (score descending, ties to the lower index), the first K of them.
+
+    Returns (idx int64 [K] logical pages, score float64 [K], number of pages
+    the last level keeps, kept grids, kept chunks).
+    """
+    vb_logical = decode(vb_logical)
+    nb = vb_logical.shape[0]
+    chunks, grids = hier_reps(vb_logical, chunk_pages, grid_chunks)
+    g_keep = _keep(affinity(grids, va) if len(grids) else [], np.arange(len(grids)), permille[0])
+    c_active = np.array([c for c in range(len(chunks)) if c // grid_chunks in set(g_keep.tolist())],
+                        dtype=np.int64)
+    c_keep = _keep(affinity(chunks, va) if len(chunks) else [], c_active, permille[1])
+    p_active = np.array([j for j in range(nb) if j // chunk_pages in set(c_keep.tolist())], dtype=np.int64)
+    p_keep = _keep(affinity(vb_logical, va) if nb else [], p_active, permille[2])
+    s = affinity(vb_logical, va) if nb else np.zeros(0)
+    idx = np.full(K, -1, dtype=np.int64)
+    val = np.full(K, -np.inf)
+    m = min(K, len(p_keep))
+    idx[:m] = p_keep[:m]
+    val[:m] = s[p_keep[:m]]
+    return idx, val, len(p_keep), np.sort(g_keep), np.sort(c_keep)

@@ -205,6 +205,54 @@ def m_append_token_slot_off_by_one(o):
     o.append_token = append_token
 
 
+def m_hier_grid_is_mean_of_pages(o):
+    def hier_reps(vb_logical, chunk_pages=64, grid_chunks=8):
+        chunks = ko.coarse_means(vb_logical, chunk_pages)
+        return chunks, ko.coarse_means(vb_logical, chunk_pages * grid_chunks)
+    o.hier_reps = hier_reps
+
+
+def m_hier_no_mask(o):
+    def hier_select(vb_logical, va, K, chunk_pages=64, grid_chunks=8, permille=(500, 200, 100)):
+        vb_logical = ko.decode(vb_logical)
+        nb = vb_logical.shape[0]
+        chunks, grids = o.hier_reps(vb_logical, chunk_pages, grid_chunks)
+        gk = ko._keep(ko.affinity(grids, va), np.arange(len(grids)), permille[0])
+        n_active_c = sum(1 for c in range(len(chunks)) if c // grid_chunks in set(gk.tolist()))
+        ck = ko._keep(ko.affinity(chunks, va), np.arange(len(chunks)), permille[1] * n_active_c / max(1, len(chunks)))
+        pk = ko._keep(ko.affinity(vb_logical, va), np.arange(nb), permille[2])
+        s = ko.affinity(vb_logical, va)
+        idx = np.full(K, -1, dtype=np.int64)
+        val = np.full(K, -np.inf)
+        m = min(K, len(pk))
+        idx[:m], val[:m] = pk[:m], s[pk[:m]]
+        return idx, val, len(pk), np.sort(gk), np.sort(ck)
+    o.hier_select = hier_select
+
+
+def m_hier_rates_of_all_members(o):
+    def hier_select(vb_logical, va, K, chunk_pages=64, grid_chunks=8, permille=(500, 200, 100)):
+        vb_logical = ko.decode(vb_logical)
+        nb = vb_logical.shape[0]
+        chunks, grids = o.hier_reps(vb_logical, chunk_pages, grid_chunks)
+        gk = ko._keep(ko.affinity(grids, va), np.arange(len(grids)), permille[0])
+        ca = np.array([c for c in range(len(chunks)) if c // grid_chunks in set(gk.tolist())], dtype=np.int64)
+        k = -(-len(chunks) * permille[1] // 1000)
+        order = np.lexsort((ca, -ko.affinity(chunks, va)[ca]))
+        ck = ca[order[:k]]
+        pa = np.array([j for j in range(nb) if j // chunk_pages in set(ck.tolist())], dtype=np.int64)
+        k = -(-nb * permille[2] // 1000)
+        s = ko.affinity(vb_logical, va)
+        order = np.lexsort((pa, -s[pa]))
+        pk = pa[order[:k]]
+        idx = np.full(K, -1, dtype=np.int64)
+        val = np.full(K, -np.inf)
+        m = min(K, len(pk))
+        idx[:m], val[:m] = pk[:m], s[pk[:m]]
+        return idx, val, len(pk), np.sort(gk), np.sort(ck)
+    o.hier_select = hier_select
+
+
 MUTANTS = [
     m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
     m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
@@ -213,6 +261,7 @@ MUTANTS = [
     m_coarse_last_group_divided_by_group, m_batched_ignores_mask, m_stability_counts_equal_theta,
     m_stability_divides_by_steps_seen, m_stability_window_one_too_long, m_stable_topk_ignores_stability,
     m_compact_table_keeps_topk_order, m_append_token_divides_by_block_size, m_append_token_slot_off_by_one,
+    m_hier_grid_is_mean_of_pages, m_hier_no_mask, m_hier_rates_of_all_members,
 ]
 
 

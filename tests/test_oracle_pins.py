@@ -320,12 +320,53 @@ def check_append_token(o):
         np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
 
 
+def check_hier_golden(o):
+    g = gold("hier.json")
+    vb = np.array(g["vb"], dtype=np.float64)
+    chunks, grids = o.hier_reps(vb, g["chunk_pages"], g["grid_chunks"])
+    np.testing.assert_array_equal(chunks, g["chunks"])
+    np.testing.assert_array_equal(grids, g["grids"])
+    for c in g["cases"]:
+        idx, val, kept, gk, ck = o.hier_select(vb, np.array(g["va"]), c["K"], g["chunk_pages"], g["grid_chunks"],
+                                               c["permille"])
+        assert list(idx) == c["idx"] and kept == c["kept"], c
+        assert list(gk) == c["grids_kept"] and list(ck) == c["chunks_kept"], c
+
+
+def check_hier_invariants(o):
+    rng = np.random.default_rng(21)
+    for nb, cp, gc in ((1000, 64, 8), (77, 4, 3), (5, 64, 8), (130, 8, 2)):
+        vb = rng.standard_normal((nb, 6))
+        va = rng.standard_normal(6)
+        s = o.affinity(vb, va)
+        # keeping every grid and chunk reduces to the plain top-k of all pages
+        for q in (100, 333, 1000):
+            k = -(-nb * q // 1000)
+            idx, val, kept, _, _ = o.hier_select(vb, va, nb, cp, gc, (1000, 1000, q))
+            want, _ = o.topk(s, k)
+            assert kept == k and list(idx[:k]) == list(want)
+        # the kept sets nest, and each level keeps its share of the active members
+        idx, val, kept, gk, ck = o.hier_select(vb, va, nb, cp, gc)
+        C = -(-nb // cp)
+        G = -(-C // gc)
+        assert len(gk) == -(-G * 500 // 1000)
+        active_c = [c for c in range(C) if c // gc in set(gk.tolist())]
+        assert set(ck.tolist()) <= set(active_c) and len(ck) == -(-len(active_c) * 200 // 1000)
+        active_p = [j for j in range(nb) if j // cp in set(ck.tolist())]
+        assert set(idx[:kept].tolist()) <= set(active_p) and kept == -(-len(active_p) * 100 // 1000)
+        np.testing.assert_array_equal(val[:kept], s[idx[:kept]])
+    # a Grid is the mean of its Chunks, not of its pages (partial last chunk)
+    vb = np.array([[1.0, 0.0]] * 4 + [[0.0, 1.0]])
+    chunks, grids = o.hier_reps(vb, 2, 4)
+    np.testing.assert_allclose(grids[0], [2.0 / 3.0, 1.0 / 3.0], rtol=0, atol=1e-15)
+
+
 ALL_CHECKS = [
     check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
     check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
     check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,
     check_planted_topics, check_stability_golden, check_stability_window, check_stable_topk,
-    check_compact_table_golden, check_append_token,
+    check_compact_table_golden, check_append_token, check_hier_golden, check_hier_invariants,
 ]
 
 
