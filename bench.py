@@ -354,6 +354,70 @@ def run_gpu(args, spec, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     sel_stable_us = e0.elapsed_time(e1) * 1e3 / n_sel
+    # hierarchical Grid -> Chunk -> Page selection (64 blocks a Chunk, 8
+    # Chunks a Grid, 50 / 20 / 10 %) against the same anchors, its coarse
+    # levels built once (write time)
+    va_h = torch.zeros((spec.R, spec.D), device=dev)
+    kk.kk_anchor(desc, bt, spec.W, va_h, head_w=head_w)
+    c_max = -(-max(spec.nb) // 64)
+    g_max = -(-c_max // 8)
+    chunk_reps = torch.zeros((spec.R, c_max, spec.D), device=dev)
+    grid_reps = torch.zeros((spec.R, g_max, spec.D), device=dev)
+    kk.kk_hier_reps(vb, bt, 64, 8, chunk_reps, grid_reps)
+    h_idx = torch.zeros((spec.R, spec.K), dtype=torch.int32, device=dev)
+    h_kept = torch.zeros(spec.R, dtype=torch.int32, device=dev)
+
+    def hier_select():
+        kk.kk_hier_select(vb, bt, chunk_reps, grid_reps, va_h, 64, 8, (500, 200, 100), h_idx, kept=h_kept)
+
+    for _ in range(5):
+        hier_select()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n_sel):
+        hier_select()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    hier_us = e0.elapsed_time(e1) * 1e3 / n_sel
+    hier_kept = int(h_kept.sum().item())
+
+    # one whole decode step of the method as a CUDA graph: every request's new
+    # token written into its block with v_b kept current (kk_append_tokens),
+    # the stability-filtered selection (kk_select_step_stable) and the table
+    # of selected pages for attention (kk_compact_table). The token is written
+    # at position seq_len - 1 (its block exists in this fixed-size cache).
+    k_new = torch.randn((spec.R, spec.L, spec.H, spec.D), device=dev)
+    k_new = k_new.to(torch.bfloat16).view(torch.int16) if spec.dtype == "bf16" else k_new
+    block_sum = torch.zeros((spec.num_pages, spec.D), device=dev)
+    sel_pages = torch.zeros((spec.R, spec.K), dtype=torch.int32, device=dev)
+    sel_count = torch.zeros(spec.R, dtype=torch.int32, device=dev)
+
+    def decode_step():
+        kk.kk_append_tokens(desc, bt, k_new, block_sum, vb, head_w=head_w)
+        select_stable()
+        kk.kk_compact_table(idx, bt, sel_pages, sel_count=sel_count)
+
+    decode_us = None
+    try:
+        g2 = torch.cuda.CUDAGraph()
+        s3 = torch.cuda.Stream(dev)
+        s3.wait_stream(stream)
+        with torch.cuda.stream(s3):
+            decode_step()
+            with torch.cuda.graph(g2, stream=s3):
+                for _ in range(20):
+                    decode_step()
+        torch.cuda.synchronize(dev)
+        g2.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(10):
+            g2.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        decode_us = e0.elapsed_time(e1) * 1e3 / 200
+    except Exception as exc:  # noqa: BLE001
+        print(f"cuda graph capture failed: {exc}", file=sys.stderr)
     if kk.kk_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -387,7 +451,7 @@ def run_gpu(args, spec, rank, world, local_rank):
     return {
         "pool_ms": statistics.mean(pool_ms), "select_ms": statistics.mean(sel_ms), "step_ms": statistics.mean(step_ms),
         "total_ms": total_ms, "wall_s": t_end - t_start, "sel_b2b_us": sel_back_to_back_us, "sel_graph_us": graph_us,
-        "sel_stable_us": sel_stable_us,
+        "sel_stable_us": sel_stable_us, "decode_step_us": decode_us, "hier_us": hier_us, "hier_kept": hier_kept,
         "clocks": clocks.summary(), "e2e": e2e, "launches": launches_per_step * args.steps,
     }
 
@@ -525,6 +589,8 @@ def main():
         "score_topk_us_per_step": res["select_ms"] * 1e3,
         "score_topk_us_back_to_back": res["sel_b2b_us"], "score_topk_us_cuda_graph": res["sel_graph_us"],
         "score_topk_stable_us_back_to_back": res["sel_stable_us"],
+        "decode_step_us_cuda_graph": res["decode_step_us"],
+        "hier_select_us_back_to_back": res["hier_us"], "hier_blocks_kept": res["hier_kept"],
         "pool_ms_per_step": res["pool_ms"], "clocks": res["clocks"], "gpu_launches": res["launches"],
         "e2e": res["e2e"],
     }

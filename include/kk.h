@@ -258,6 +258,39 @@ kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, c
                            const float* head_w, float* block_sum, float* vb, cudaStream_t stream);
 
 /*
+ * Hierarchical selection Grid -> Chunk -> Page [KK §5.1]. A Chunk is
+ * chunk_pages consecutive blocks of a request's table and a Grid grid_chunks
+ * consecutive Chunks (the page names the levels but not their sizes; 64 and
+ * 8 are the usual choice).
+ *
+ * kk_hier_reps builds the two coarse levels from the v_b table (device float
+ * [num_pages][D], as kk_pool_blocks writes it):
+ *   chunk_reps[r][c] = mean of vb[pages[offsets[r] + j]], j in Chunk c
+ *                      (device float [R][C_max][D], C_max = ceil(max_blocks / chunk_pages))
+ *   grid_reps[r][g]  = mean of chunk_reps[r][c], c in Grid g
+ *                      (device float [R][G_max][D], G_max = ceil(C_max / grid_chunks))
+ * Levels past a request's end are zero. Call it when blocks change (write time).
+ *
+ * kk_hier_select scores the levels against the anchor va (device float
+ * [R][D]) with the affinity of kk_score and keeps, level by level,
+ * ceil(n * permille / 1000) of its n active members (permille in 1..1000;
+ * 500 / 200 / 100 keep 1 % of the blocks), where only the Chunks of kept
+ * Grids and the blocks of kept Chunks are active (ties to the lower index).
+ * The kept blocks of request r are written to idx[r][0..K) in kk_topk order
+ * (logical indices, -1 / -inf padding; at most K of them) and their number
+ * to kept[r] (nullable, device int32 [R]; may exceed K). 1 <= K <= 16384.
+ * Returns KK_ERR_UNSUPPORTED when a level of the table's longest request
+ * could hold more than 16384 members. D in {32, 64, 128, 256}.
+ */
+kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                       int32_t chunk_pages, int32_t grid_chunks, float* chunk_reps, float* grid_reps,
+                       cudaStream_t stream);
+kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                         const float* chunk_reps, const float* grid_reps, const float* va, int32_t chunk_pages,
+                         int32_t grid_chunks, int32_t permille_grid, int32_t permille_chunk, int32_t permille_page,
+                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, cudaStream_t stream);
+
+/*
  * Shared-pool scoring [KK §5.1] (every representation against the anchors
  * in one matrix product, then a mask): R anchors A (device bf16 bits [R][D])
  * against N pooled block vectors V (device bf16 bits [N][D]); anchor r may

@@ -1,5 +1,6 @@
 // C ABI of the selector (include/kk.h): argument checks on the host, then
 // launches. Nothing here allocates device memory.
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -351,6 +352,62 @@ kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, c
   int* err = error_word();
   if (!err) return KK_ERR_CUDA;
   return from_cuda(kk::launch_append(c, t, k_new, head_w, block_sum, vb, err, stream));
+}
+
+// Sizes of the hierarchical levels for a table whose longest request has
+// max_blocks blocks, and whether the worst case fits the kernel.
+static bool hier_dims(int32_t max_blocks, int32_t chunk_pages, int32_t grid_chunks, const int32_t* permille,
+                      int* c_max, int* g_max) {
+  const long long C = ((long long)max_blocks + chunk_pages - 1) / chunk_pages;
+  const long long G = (C + grid_chunks - 1) / grid_chunks;
+  *c_max = (int)C;
+  *g_max = (int)G;
+  const long long kg = (G * permille[0] + 999) / 1000;
+  const long long ac = std::min(C, kg * grid_chunks);
+  const long long kc = (ac * permille[1] + 999) / 1000;
+  const long long ap = std::min((long long)max_blocks, kc * chunk_pages);
+  return C <= kk::kHierMax && G <= kk::kHierMax && ac <= kk::kHierMax && ap <= kk::kHierMax;
+}
+
+kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                       int32_t chunk_pages, int32_t grid_chunks, float* chunk_reps, float* grid_reps,
+                       cudaStream_t stream) {
+  kk::Table t;
+  kk_status st = check_table(bt, false, &t);
+  if (st != KK_OK) return st;
+  if (!vb || !chunk_reps || !grid_reps || chunk_pages < 1 || grid_chunks < 1 || num_pages <= 0)
+    return KK_ERR_INVALID;
+  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  const long long C = ((long long)t.max_blocks + chunk_pages - 1) / chunk_pages;
+  const long long G = (C + grid_chunks - 1) / grid_chunks;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  cudaError_t e = kk::launch_coarse(vb, D, num_pages, t, chunk_pages, chunk_reps, err, stream);
+  if (e == cudaSuccess)
+    e = kk::launch_grid_reps(chunk_reps, D, (int)C, (int)G, t, chunk_pages, grid_chunks, grid_reps, stream);
+  return from_cuda(e);
+}
+
+kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
+                         const float* chunk_reps, const float* grid_reps, const float* va, int32_t chunk_pages,
+                         int32_t grid_chunks, int32_t permille_grid, int32_t permille_chunk, int32_t permille_page,
+                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, cudaStream_t stream) {
+  kk::Table t;
+  kk_status st = check_table(bt, false, &t);
+  if (st != KK_OK) return st;
+  const int32_t pm[3] = {permille_grid, permille_chunk, permille_page};
+  if (!vb || !chunk_reps || !grid_reps || !va || !idx || chunk_pages < 1 || grid_chunks < 1 || num_pages <= 0 ||
+      K < 1 || K > kk::kHierMax)
+    return KK_ERR_INVALID;
+  for (int32_t q : pm)
+    if (q < 1 || q > 1000) return KK_ERR_INVALID;
+  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  int c_max = 0, g_max = 0;
+  if (!hier_dims(t.max_blocks, chunk_pages, grid_chunks, pm, &c_max, &g_max)) return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_hier_select(vb, D, num_pages, t, chunk_reps, grid_reps, c_max, g_max, va,
+                                          chunk_pages, grid_chunks, pm, K, idx, top_scores, kept, err, stream));
 }
 
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {

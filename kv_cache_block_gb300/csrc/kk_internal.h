@@ -90,6 +90,16 @@ cudaError_t launch_compact_table(const int* idx, int K, const Table& bt, int* ou
 cudaError_t launch_append(const KCache& kc, const Table& bt, const void* k_new, const float* head_w,
                           float* block_sum, float* vb, int* err, cudaStream_t s);
 
+// kk_hier.cu: members of one level of the hierarchical selection held in
+// shared memory at once (Grids, active Chunks, active blocks of a request)
+constexpr int kHierMax = 16384;
+cudaError_t launch_grid_reps(const float* chunk, int D, int c_max, int g_max, const Table& bt, int chunk_pages,
+                             int grid_chunks, float* grid, cudaStream_t s);
+cudaError_t launch_hier_select(const float* vb, int D, int vb_rows, const Table& bt, const float* chunk,
+                               const float* grid, int c_max, int g_max, const float* va, int chunk_pages,
+                               int grid_chunks, const int* permille, int K, int* idx, float* top, int* kept,
+                               int* err, cudaStream_t s);
+
 // kk_host.cu
 void* tensor_map_encoder();  // cuTensorMapEncodeTiled (driver ABI 12.0), or null
 int sm_count();              // SMs of the current device

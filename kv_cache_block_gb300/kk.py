@@ -76,6 +76,8 @@ def _load():
         "kk_score_topk_stable": (ctypes.c_int, [P, I32, I32, BT, P, I32, I32, F, P, P, P, P, P, P]),
         "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, P]),
         "kk_compact_table": (ctypes.c_int, [P, I32, BT, P, P, P, P]),
+        "kk_hier_reps": (ctypes.c_int, [P, I32, I32, BT, I32, I32, P, P, P]),
+        "kk_hier_select": (ctypes.c_int, [P, I32, I32, BT, P, P, P, I32, I32, I32, I32, I32, I32, P, P, P, P]),
         "kk_append_tokens": (ctypes.c_int, [KC, BT, P, P, P, P, P]),
         "kk_score_pool_batched_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
@@ -96,7 +98,8 @@ EXPORTS = (
     "kk_status_str", "kk_device_error", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
     "kk_head_variance", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static", "kk_anchor", "kk_score", "kk_topk",
     "kk_score_topk", "kk_select_step", "kk_score_topk_stable", "kk_select_step_stable",
-    "kk_compact_table", "kk_append_tokens", "kk_score_pool_batched_workspace_bytes",
+    "kk_compact_table", "kk_append_tokens", "kk_hier_reps", "kk_hier_select",
+    "kk_score_pool_batched_workspace_bytes",
     "kk_score_pool_batched", "kk_coarse_means",
 )
 
@@ -268,6 +271,23 @@ def kk_append_tokens(kc, bt: BlockTable, k_new, block_sum, vb, head_w=None, stre
     _check("kk_append_tokens", _lib.kk_append_tokens(
         ctypes.byref(kc), ctypes.byref(bt.c), ctypes.c_void_p(k_new.data_ptr()), _ptr(head_w, torch.float32, "head_w"),
         _ptr(block_sum, torch.float32, "block_sum"), _ptr(vb, torch.float32, "vb"), _stream(stream)))
+
+
+def kk_hier_reps(vb, bt: BlockTable, chunk_pages: int, grid_chunks: int, chunk_reps, grid_reps, stream=None):
+    _check("kk_hier_reps", _lib.kk_hier_reps(
+        _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c), chunk_pages, grid_chunks,
+        _ptr(chunk_reps, torch.float32, "chunk_reps"), _ptr(grid_reps, torch.float32, "grid_reps"), _stream(stream)))
+
+
+def kk_hier_select(vb, bt: BlockTable, chunk_reps, grid_reps, va, chunk_pages: int, grid_chunks: int, permille,
+                   idx, top_scores=None, kept=None, stream=None):
+    pg, pc, pp = (int(x) for x in permille)
+    _check("kk_hier_select", _lib.kk_hier_select(
+        _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c),
+        _ptr(chunk_reps, torch.float32, "chunk_reps"), _ptr(grid_reps, torch.float32, "grid_reps"),
+        _ptr(va, torch.float32, "va"), chunk_pages, grid_chunks, pg, pc, pp, idx.shape[1],
+        _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"), _ptr(kept, torch.int32, "kept"),
+        _stream(stream)))
 
 
 def kk_score_pool_batched_workspace_bytes(R: int, N: int, K: int) -> int:
