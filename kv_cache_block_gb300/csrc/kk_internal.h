@@ -35,8 +35,8 @@ struct Table {
 cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_valid, int n,
                                const float* head_w, int n_sets, const int* w_set, float* vb,
                                int* err, cudaStream_t s);
-cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, float* S, float* Q, int* err,
-                               cudaStream_t s);
+cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, long long total_blocks, float* S, float* Q,
+                               int* err, cudaStream_t s);
 cudaError_t launch_head_var(const KCache& kc, const Table& bt, const float* S, const float* Q,
                             double* var, int* err, cudaStream_t s);
 cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, const double* var,
@@ -110,6 +110,10 @@ int sm_count();              // SMs of the current device
 cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_valid, int n,
                             const float* head_w, int n_sets, const int* w_set, float* vb, int* err,
                             cudaStream_t s);
+// the per-(layer, head) token sums and squares of every block of a table
+// (inputs of the head-variance weights) on the same TMA ring
+cudaError_t launch_pool_tma_slices(const KCache& kc, const Table& bt, long long total_blocks, float* S, float* Q,
+                                   int* err, cudaStream_t s);
 
 // kk_api.cu (used by kk_static.cu)
 int* device_error_word();

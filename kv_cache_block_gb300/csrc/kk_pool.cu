@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
 }
 
 // Per (request, layer-head): Var = E_t[sum_d K^2]/D - sum_d (E_t K_d)^2 / D,
-// from the per-block sums, accumulated in float64 in a fixed order.
+// from the per-block sums, accumulated in float64 in a fixed order. A thread
+// owns four dims (16-byte loads) of every kThreads/(D/4)-th block.
 __global__ void __launch_bounds__(kThreads) head_var_kernel(const float* S, const float* Q,
                                                             const int* offsets, const int* seq_lens,
                                                             int bs, int LH, int D, int max_blocks,
                                                             double* var, int* err) {
-  __shared__ double s_sum[kThreads];
+  __shared__ double s_sum[kThreads * 4];  // [row group][D]: kThreads / (D/4) groups of D
   __shared__ double s_q[kThreads];
   const int s = blockIdx.x, r = blockIdx.y;
   const int off = offsets[r];
@@ -225,21 +226,50 @@ __global__ void __launch_bounds__(kThreads) head_var_kernel(const float* S, cons
     if (threadIdx.x == 0 && s == 0) flag_error(err, kErrBadIndex);
     return;
   }
-  const int KS = kThreads / D;  // row lanes per dim
-  const int d = threadIdx.x % D, k = threadIdx.x / D;
-  double acc = 0.0;
-  if (k < KS)
-    for (int j = k; j < nb; j += KS) acc += (double)S[((long long)(off + j) * LH + s) * D + d];
+  const int C4 = D / 4;            // float4 columns of a row
+  const int KS = kThreads / C4;    // row groups
+  const int c4 = threadIdx.x % C4, kr = threadIdx.x / C4;
+  const float4* S4 = reinterpret_cast<const float4*>(S);
+  // compensated (Kahan) float32 sums: float64 arithmetic is scarce on this
+  // GPU, and the compensation keeps the error independent of the block count
+  float a[4] = {0.f, 0.f, 0.f, 0.f}, cmp[4] = {0.f, 0.f, 0.f, 0.f};
+  auto add4 = [&](const float4& v) {
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float y = x[e] - cmp[e];
+      const float t = a[e] + y;
+      cmp[e] = (t - a[e]) - y;
+      a[e] = t;
+    }
+  };
+  int j = kr;
+  for (; j + 3 * KS < nb; j += 4 * KS) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = S4[((long long)(off + j + u * KS) * LH + s) * C4 + c4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) add4(v[u]);
+  }
+  for (; j < nb; j += KS) add4(S4[((long long)(off + j) * LH + s) * C4 + c4]);
+  const double a0 = (double)a[0] - (double)cmp[0], a1 = (double)a[1] - (double)cmp[1];
+  const double a2 = (double)a[2] - (double)cmp[2], a3 = (double)a[3] - (double)cmp[3];
   double q = 0.0;
-  for (int j = threadIdx.x; j < nb; j += kThreads) q += (double)Q[(long long)(off + j) * LH + s];
-  s_sum[threadIdx.x] = acc;
+  for (int jj = threadIdx.x; jj < nb; jj += kThreads) q += (double)Q[(long long)(off + jj) * LH + s];
+  double* row = s_sum + kr * D + c4 * 4;
+  row[0] = a0;
+  row[1] = a1;
+  row[2] = a2;
+  row[3] = a3;
   s_q[threadIdx.x] = q;
   __syncthreads();
-  if (threadIdx.x < D) {
+  // per dim: the mean over the request's tokens, squared (row group 0 is
+  // overwritten only after every group's value for that dim has been read)
+  for (int d = threadIdx.x; d < D; d += kThreads) {
     double m = 0.0;
-    for (int kk2 = 0; kk2 < KS; ++kk2) m += s_sum[kk2 * D + threadIdx.x];
+    for (int g = 0; g < KS; ++g) m += s_sum[g * D + d];
     const double mu = T_r > 0 ? m / (double)T_r : 0.0;
-    s_sum[threadIdx.x] = mu * mu;  // row 0 is no longer read by other threads after this point
+    s_sum[d] = mu * mu;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -276,12 +306,14 @@ __global__ void __launch_bounds__(kThreads) finalize_weights_kernel(const double
 }
 
 // vb[page] = (1/n) * sum_s w[r][s] * S[block][s] (weights fixed per request).
+// A thread owns four dims (16-byte loads) of every kThreads/(D/4)-th slice.
 __global__ void __launch_bounds__(kThreads) combine_kernel(const float* S, const float* head_w,
                                                            const int* pages, const int* offsets,
                                                            const int* seq_lens, int bs, int LH,
                                                            int D, int max_blocks, int num_pages,
                                                            float* vb) {
   __shared__ float s_w[kMaxLH];
+  __shared__ float4 s_part[kThreads];
   const int j = blockIdx.x, r = blockIdx.y;
   const int off = offsets[r];
   const int nb = offsets[r + 1] - off;
@@ -289,15 +321,43 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* S, const
   if (j >= nb || nb > max_blocks || T_r < 0 || nb != (T_r + bs - 1) / bs) return;  // flagged upstream
   const int page = pages[off + j];
   if (page < 0 || page >= num_pages) return;  // flagged by the slice kernel
-  for (int s = threadIdx.x; s < LH; s += blockDim.x) s_w[s] = head_w[(long long)r * LH + s];
+  for (int s = threadIdx.x; s < LH; s += kThreads) s_w[s] = head_w[(long long)r * LH + s];
+  __syncthreads();
+  const int C4 = D / 4, KS = kThreads / C4;
+  const int c4 = threadIdx.x % C4, kr = threadIdx.x / C4;
+  const float4* src = reinterpret_cast<const float4*>(S + (long long)(off + j) * LH * D);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = kr; s < LH; s += KS) {
+    const float4 v = src[(long long)s * C4 + c4];
+    const float w = s_w[s];
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  s_part[threadIdx.x] = acc;
   __syncthreads();
   const int n = min(bs, T_r - j * bs);
   const float inv_n = n > 0 ? 1.f / (float)n : 0.f;
-  const float* src = S + (long long)(off + j) * LH * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < LH; ++s) v = fmaf(s_w[s], src[(long long)s * D + d], v);
-    vb[(long long)page * D + d] = v * inv_n;
+  if (threadIdx.x < C4) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < KS; ++g) {
+      const float4 v = s_part[g * C4 + threadIdx.x];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    float* out = vb + (long long)page * D + threadIdx.x * 4;
+    if ((reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+      *reinterpret_cast<float4*>(out) = make_float4(t.x * inv_n, t.y * inv_n, t.z * inv_n, t.w * inv_n);
+    } else {  // a v_b table not 16-byte aligned
+      out[0] = t.x * inv_n;
+      out[1] = t.y * inv_n;
+      out[2] = t.z * inv_n;
+      out[3] = t.w * inv_n;
+    }
   }
 }
 
@@ -373,9 +433,12 @@ cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_
   return dispatch_pool<false>(kc, a, dim3((unsigned)n * split), split, s);
 }
 
-cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, float* S, float* Q, int* err,
-                               cudaStream_t s) {
+cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, long long total_blocks, float* S, float* Q,
+                               int* err, cudaStream_t s) {
   if (bt.R == 0 || bt.max_blocks == 0) return cudaSuccess;
+  // at least one block per SM: the persistent TMA ring (kk_pool_tma.cu)
+  const cudaError_t e = launch_pool_tma_slices(kc, bt, total_blocks, S, Q, err, s);
+  if (e != cudaErrorNotSupported) return e;
   PoolArgs a = base_args(kc, err);
   a.bt_pages = bt.pages;
   a.offsets = bt.offsets;
@@ -406,7 +469,7 @@ cudaError_t launch_combine(const KCache& kc, const Table& bt, const float* S, co
                            float* vb, int* err, cudaStream_t s) {
   (void)err;
   if (bt.R == 0 || bt.max_blocks == 0) return cudaSuccess;
-  combine_kernel<<<dim3(bt.max_blocks, bt.R), kc.D, 0, s>>>(S, head_w, bt.pages, bt.offsets,
+  combine_kernel<<<dim3(bt.max_blocks, bt.R), kThreads, 0, s>>>(S, head_w, bt.pages, bt.offsets,
                                                             bt.seq_lens, kc.bs, kc.L * kc.H, kc.D,
                                                             bt.max_blocks, kc.num_pages, vb);
   return cudaGetLastError();

@@ -263,6 +263,198 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
+// ---- per-(layer, head) sums for the head-variance weights -----------------
+// The same ring over the blocks of a block table, writing for every block g
+// and (layer, head) slice s the token sum S[g][s][:] and the sum of squares
+// Q[g][s] (the inputs of the variance weights). A box holds at most eight
+// slices, tokens innermost; each slice of a box is summed by one consumer
+// warp (rotated from box to box), which keeps its sums in registers across
+// the slice's token boxes and writes them once.
+struct SliceTmaArgs {
+  Table bt;
+  long long total;  // blocks in S / Q (offsets[R])
+  int L, H, bs, num_pages;
+  int tb, hb, lb, nhb, nlb;
+  int pos[4];
+  float* S;
+  float* Q;
+  int* err;
+};
+
+struct SliceBlock {
+  int page, n;
+  bool ok, bad;
+};
+
+// Block g of the table; r is the request holding it, advanced monotonically.
+__device__ __forceinline__ SliceBlock slice_block(const SliceTmaArgs& a, long long g, int& r) {
+  while (r < a.bt.R && a.bt.offsets[r + 1] <= g) ++r;
+  SliceBlock m{0, 0, false, false};
+  if (r >= a.bt.R) return m;
+  const int off = a.bt.offsets[r], nb = a.bt.offsets[r + 1] - off, T = a.bt.seq_lens[r];
+  if (nb < 0 || nb > a.bt.max_blocks || T < 0 || nb != (T + a.bs - 1) / a.bs || g < off) {
+    m.bad = true;
+    return m;
+  }
+  m.page = a.bt.pages[g];
+  m.n = min(a.bs, T - (int)(g - off) * a.bs);
+  m.bad = m.page < 0 || m.page >= a.num_pages;
+  m.ok = !m.bad && m.n > 0;
+  return m;
+}
+
+// first request holding block g (offsets non-decreasing)
+__device__ __forceinline__ int request_of(const Table& bt, long long g) {
+  int lo = 0, hi = bt.R;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (bt.offsets[mid + 1] <= g) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    pool_tma_slices_kernel(const __grid_constant__ CUtensorMap tm, const SliceTmaArgs a) {
+  constexpr int ES = elem_bytes<T>();
+  constexpr int EPV = Vec16<T>::kElems;
+  constexpr int V16 = D / EPV;
+  constexpr int RPW = 32 / V16;  // rows one warp covers per pass
+  static_assert(V16 >= 1 && V16 <= 32 && (32 % V16) == 0, "row must be 16..512 bytes");
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = base;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  int* s_abort = reinterpret_cast<int*>(empty + kStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long b0 = a.total * blockIdx.x / gridDim.x;
+  const long long b1 = a.total * (blockIdx.x + 1) / gridDim.x;
+  const int LH = a.L * a.H;
+  const int nsub = a.hb * a.lb;
+  const uint32_t box_bytes = (uint32_t)(a.tb * nsub * D * ES);
+
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumerWarps);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = s_abort;
+  int r = b0 < b1 ? request_of(a.bt, b0) : a.bt.R;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t k = 0;
+      bool alive = true;
+      for (long long g = b0; g < b1 && alive; ++g) {
+        const SliceBlock m = slice_block(a, g, r);
+        if (!m.ok) continue;
+        const int nt = (m.n + a.tb - 1) / a.tb;
+        for (int lbi = 0; lbi < a.nlb && alive; ++lbi)
+          for (int hbi = 0; hbi < a.nhb && alive; ++hbi)
+            for (int tbi = 0; tbi < nt; ++tbi) {
+              const int st = (int)(k % kStages);
+              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, kWaitLimitNs)) ||
+                  *abort_flag) {
+                if (!*abort_flag) flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+                alive = false;
+                break;
+              }
+              const int ct = tbi * a.tb, ch = hbi * a.hb, cl = lbi * a.lb;
+              mbar_arrive_expect_tx(&full[st], box_bytes);
+              tma_load_5d(stages + st * kStageBytes, &tm, 0, ct, ch, a.pos[kPage] == 3 ? m.page : cl,
+                          a.pos[kPage] == 3 ? cl : m.page, &full[st]);
+              ++k;
+            }
+      }
+      for (uint32_t j = k > (uint32_t)kStages ? k - kStages : 0; j < k; ++j)
+        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, kWaitLimitNs)) {
+          flag_error(a.err, kErrTimeout);
+          break;
+        }
+    }
+    return;
+  }
+
+  // ---- consumers: warp cw sums the slice `sub` of a box with
+  // (sub + unit) % 8 == cw, unit counting the (layer, head) box groups
+  const int cw = warp - 1;
+  const int col = lane % V16, rg = lane / V16;
+  uint32_t k = 0, unit = 0;
+  bool alive = true;
+  for (long long g = b0; g < b1; ++g) {
+    const SliceBlock m = slice_block(a, g, r);
+    if (!m.ok) {
+      if (m.bad && cw == 0 && lane == 0) flag_error(a.err, kErrBadIndex);
+      continue;
+    }
+    const int nt = (m.n + a.tb - 1) / a.tb;
+    for (int lbi = 0; lbi < a.nlb; ++lbi)
+      for (int hbi = 0; hbi < a.nhb; ++hbi, ++unit) {
+        const int sub = (int)((cw + kConsumerWarps - (int)(unit % kConsumerWarps)) % kConsumerWarps);
+        const bool mine = sub < nsub;
+        float acc[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+        float q = 0.f;
+        for (int tbi = 0; tbi < nt; ++tbi, ++k) {
+          if (!alive) continue;
+          const int st = (int)(k % kStages);
+          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, kWaitLimitNs);
+          ok = __all_sync(kFull, ok);
+          if (!ok) {
+            if (lane == 0 && !*abort_flag) flag_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+            alive = false;
+            continue;
+          }
+          if (mine) {
+            const int tvalid = min(a.tb, m.n - tbi * a.tb);
+            const uint32_t rows = smem_u32(stages + st * kStageBytes) + (uint32_t)((sub * a.tb) * D * ES + col * 16);
+#pragma unroll 4
+            for (int t = rg; t < tvalid; t += RPW) {
+              const uint4 v = lds16(rows + (uint32_t)(t * D * ES));
+              float f[EPV];
+              Vec16<T>::unpack(v, f);
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) {
+                acc[e] += f[e];
+                q = fmaf(f[e], f[e], q);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        if (mine && alive) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+#pragma unroll
+            for (int o = V16; o < 32; o <<= 1) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(kFull, q, o);
+          const int ll = sub / a.hb, hh = sub - ll * a.hb;
+          const int sl = (lbi * a.lb + ll) * a.H + hbi * a.hb + hh;
+          float* dst = a.S + ((long long)g * LH + sl) * D + col * EPV;
+          if (rg == 0) {
+#pragma unroll
+            for (int e = 0; e < EPV; e += 4)
+              *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+          }
+          if (lane == 0) a.Q[(long long)g * LH + sl] = q;
+        }
+      }
+  }
+}
+
 template <typename T, int D, bool kWeighted>
 cudaError_t launch_t(const CUtensorMap& tm, const PoolTmaArgs& a, int grid, cudaStream_t s) {
   static std::mutex mu;
@@ -303,31 +495,95 @@ int largest_divisor_at_most(int x, int cap) {
 
 }  // namespace
 
+namespace {
+
+// Box and tensor map of a paged cache for the TMA pools: box = tokens first,
+// then whole heads, then whole layers, up to one stage and max_sub (layer,
+// head) slices; the four strided axes sorted by stride.
+struct TmaPlan {
+  int tb, hb, lb;
+  int pos[4];
+  int ext[5];
+  CUtensorMap tm;
+};
+
+bool plan_tma(const KCache& kc, int max_sub, TmaPlan* pl) {
+  const int ES = kc.dtype == 1 ? 2 : 4;
+  const long long row_bytes = (long long)kc.D * ES;
+  if (kc.D > kMaxD || row_bytes % 16 != 0 || row_bytes > 512 || (reinterpret_cast<uintptr_t>(kc.base) & 15))
+    return false;
+  const long long stride[4] = {kc.sT * ES, kc.sH * ES, kc.sP * ES, kc.sL * ES};
+  for (long long b : stride)
+    if (b <= 0 || b % 16 != 0 || b >= (1ll << 40)) return false;
+  const int rows_cap = (int)std::min<long long>(kStageBytes / row_bytes, 1 << 30);
+  int tb = kc.bs;
+  if (tb > rows_cap) {
+    if ((kc.bs & (kc.bs - 1)) != 0) return false;
+    tb = rows_cap;  // a power of two dividing bs
+  }
+  if (tb > 256) tb = 256;
+  if (kc.bs % tb != 0) return false;
+  const int hb = tb == kc.bs ? largest_divisor_at_most(kc.H, std::min({256, rows_cap / tb, max_sub})) : 1;
+  const int lb = (tb == kc.bs && hb == kc.H)
+                     ? largest_divisor_at_most(kc.L, std::min({256, rows_cap / (tb * hb), max_sub / hb}))
+                     : 1;
+  pl->tb = tb;
+  pl->hb = hb;
+  pl->lb = lb;
+  const long long extent[4] = {kc.bs, kc.H, kc.num_pages, kc.L};
+  const int box[4] = {tb, hb, 1, lb};
+  int order[4] = {kTok, kHead, kPage, kLayer};
+  std::stable_sort(order, order + 4, [&](int x, int y) { return stride[x] < stride[y]; });
+  cuuint64_t dims[5] = {(cuuint64_t)kc.D, 0, 0, 0, 0};
+  cuuint64_t strides[4] = {};
+  cuuint32_t bdim[5] = {(cuuint32_t)kc.D, 0, 0, 0, 0};
+  pl->ext[0] = kc.D;
+  for (int p = 1; p <= 4; ++p) {
+    const int d = order[p - 1];
+    pl->pos[d] = p;
+    dims[p] = (cuuint64_t)extent[d];
+    strides[p - 1] = (cuuint64_t)stride[d];
+    bdim[p] = (cuuint32_t)box[d];
+    pl->ext[p] = box[d];
+  }
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  return encode &&
+         encode(&pl->tm, kc.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
+                const_cast<void*>(kc.base), dims, strides, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D>
+cudaError_t launch_slices_t(const CUtensorMap& tm, const SliceTmaArgs& a, int grid, cudaStream_t s) {
+  static std::mutex mu;
+  static bool ready[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      e = cudaFuncSetAttribute(pool_tma_slices_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem);
+      if (e != cudaSuccess) return e;
+      ready[dev] = true;
+    }
+  }
+  pool_tma_slices_kernel<T, D><<<grid, kTmaThreads, kTmaSmem, s>>>(tm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_valid, int n,
                             const float* head_w, int n_sets, const int* w_set, float* vb, int* err,
                             cudaStream_t s) {
   const int sms = sm_count();
   if (n < sms) return cudaErrorNotSupported;  // too few blocks for one per SM: the cluster path splits them
-  const int ES = kc.dtype == 1 ? 2 : 4;
-  const long long row_bytes = (long long)kc.D * ES;
-  if (kc.D > kMaxD || row_bytes % 16 != 0 || row_bytes > 512 || (reinterpret_cast<uintptr_t>(kc.base) & 15))
-    return cudaErrorNotSupported;
-  // the four non-contiguous dims, sorted by stride (token, head, page, layer order on ties)
-  const long long stride[4] = {kc.sT * ES, kc.sH * ES, kc.sP * ES, kc.sL * ES};
-  for (long long b : stride)
-    if (b <= 0 || b % 16 != 0 || b >= (1ll << 40)) return cudaErrorNotSupported;
-  // box: tokens first, then whole heads, then whole layers, up to one stage
-  const int rows_cap = std::min<long long>(kStageBytes / row_bytes, 1 << 30);
-  int tb = kc.bs;
-  if (tb > rows_cap) {
-    if ((kc.bs & (kc.bs - 1)) != 0) return cudaErrorNotSupported;
-    tb = rows_cap;  // a power of two dividing bs
-  }
-  if (tb > 256) tb = 256;
-  if (kc.bs % tb != 0) return cudaErrorNotSupported;
-  const int hb = tb == kc.bs ? largest_divisor_at_most(kc.H, std::min(256, rows_cap / tb)) : 1;
-  const int lb = (tb == kc.bs && hb == kc.H) ? largest_divisor_at_most(kc.L, std::min(256, rows_cap / (tb * hb))) : 1;
-
+  TmaPlan pl;
+  if (!plan_tma(kc, 256, &pl)) return cudaErrorNotSupported;
   PoolTmaArgs a = {};
   a.pages = pages;
   a.n_valid = n_valid;
@@ -340,41 +596,59 @@ cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_val
   a.H = kc.H;
   a.bs = kc.bs;
   a.num_pages = kc.num_pages;
-  a.tb = tb;
-  a.hb = hb;
-  a.lb = lb;
-  a.nhb = kc.H / hb;
-  a.nlb = kc.L / lb;
+  a.tb = pl.tb;
+  a.hb = pl.hb;
+  a.lb = pl.lb;
+  a.nhb = kc.H / pl.hb;
+  a.nlb = kc.L / pl.lb;
   a.err = err;
-  const long long extent[4] = {kc.bs, kc.H, kc.num_pages, kc.L};
-  const int box[4] = {tb, hb, 1, lb};
-  int order[4] = {kTok, kHead, kPage, kLayer};
-  std::stable_sort(order, order + 4, [&](int x, int y) { return stride[x] < stride[y]; });
-  cuuint64_t dims[5] = {(cuuint64_t)kc.D, 0, 0, 0, 0};
-  cuuint64_t strides[4] = {};
-  cuuint32_t bdim[5] = {(cuuint32_t)kc.D, 0, 0, 0, 0};
-  a.ext[0] = kc.D;
-  for (int p = 1; p <= 4; ++p) {
-    const int d = order[p - 1];
-    a.pos[d] = p;
-    dims[p] = (cuuint64_t)extent[d];
-    strides[p - 1] = (cuuint64_t)stride[d];
-    bdim[p] = (cuuint32_t)box[d];
-    a.ext[p] = box[d];
-  }
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
-  if (!encode) return cudaErrorNotSupported;
-  CUtensorMap tm;
-  if (encode(&tm, kc.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
-             const_cast<void*>(kc.base), dims, strides, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorNotSupported;
+  for (int i = 0; i < 4; ++i) a.pos[i] = pl.pos[i];
+  for (int i = 0; i < 5; ++i) a.ext[i] = pl.ext[i];
   const int grid = std::min(n, sms);
   if (kc.dtype == 1)
-    return head_w ? dispatch_d<bf16_t, true>(kc.D, tm, a, grid, s) : dispatch_d<bf16_t, false>(kc.D, tm, a, grid, s);
-  return head_w ? dispatch_d<float, true>(kc.D, tm, a, grid, s) : dispatch_d<float, false>(kc.D, tm, a, grid, s);
+    return head_w ? dispatch_d<bf16_t, true>(kc.D, pl.tm, a, grid, s) : dispatch_d<bf16_t, false>(kc.D, pl.tm, a, grid, s);
+  return head_w ? dispatch_d<float, true>(kc.D, pl.tm, a, grid, s) : dispatch_d<float, false>(kc.D, pl.tm, a, grid, s);
+}
+
+cudaError_t launch_pool_tma_slices(const KCache& kc, const Table& bt, long long total_blocks, float* S, float* Q,
+                                   int* err, cudaStream_t s) {
+  const int sms = sm_count();
+  if (total_blocks < sms) return cudaErrorNotSupported;
+  TmaPlan pl;
+  if (!plan_tma(kc, kConsumerWarps, &pl)) return cudaErrorNotSupported;
+  if (pl.pos[kTok] != 1 || pl.pos[kHead] != 2) return cudaErrorNotSupported;  // slices must be contiguous rows
+  SliceTmaArgs a = {};
+  a.bt = bt;
+  a.total = total_blocks;
+  a.L = kc.L;
+  a.H = kc.H;
+  a.bs = kc.bs;
+  a.num_pages = kc.num_pages;
+  a.tb = pl.tb;
+  a.hb = pl.hb;
+  a.lb = pl.lb;
+  a.nhb = kc.H / pl.hb;
+  a.nlb = kc.L / pl.lb;
+  for (int i = 0; i < 4; ++i) a.pos[i] = pl.pos[i];
+  a.S = S;
+  a.Q = Q;
+  a.err = err;
+  const int grid = (int)std::min<long long>(total_blocks, sms);
+  if (kc.dtype == 1) {
+    switch (kc.D) {
+      case 32: return launch_slices_t<bf16_t, 32>(pl.tm, a, grid, s);
+      case 64: return launch_slices_t<bf16_t, 64>(pl.tm, a, grid, s);
+      case 128: return launch_slices_t<bf16_t, 128>(pl.tm, a, grid, s);
+      case 256: return launch_slices_t<bf16_t, 256>(pl.tm, a, grid, s);
+    }
+  } else {
+    switch (kc.D) {
+      case 32: return launch_slices_t<float, 32>(pl.tm, a, grid, s);
+      case 64: return launch_slices_t<float, 64>(pl.tm, a, grid, s);
+      case 128: return launch_slices_t<float, 128>(pl.tm, a, grid, s);
+    }
+  }
+  return cudaErrorNotSupported;
 }
 
 }  // namespace kk

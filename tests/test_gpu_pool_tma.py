@@ -154,3 +154,25 @@ def test_both_regimes_agree(kk):
     assert kk.kk_device_error() == 0
     a, b = vb_long.cpu().numpy(), vb_short.cpu().numpy()
     assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
+
+
+def test_weighted_pool_many_blocks(kk, dev):
+    """kk_pool_blocks_weighted on more blocks than SMs: the per-(layer, head)
+    token sums and squares come from the TMA ring (token-innermost layouts),
+    then the head-variance weights and the weighted v_b."""
+    sp = dev.spec
+    kc = dev.host_view()
+    LH = sp.L * sp.H
+    ws = torch.empty(kk.kk_head_variance_workspace_bytes(dev.desc, sp.total_blocks, sp.R), dtype=torch.uint8,
+                     device="cuda")
+    w_out = torch.zeros((sp.R, LH), device="cuda")
+    vb = torch.zeros((sp.num_pages, sp.D), device="cuda")
+    kk.kk_pool_blocks_weighted(dev.desc, dev.bt, sp.total_blocks, w_out, vb, ws)
+    assert kk.kk_device_error() == 0
+    want_w = np.stack([ko.head_variance_weights(kc, sp.pages_of(r), sp.seq_lens[r], sp.bs) for r in range(sp.R)])
+    assert_vec_close(w_out.cpu().numpy(), want_w, "head weights")
+    got = vb.cpu().numpy()
+    for r in range(sp.R):
+        blk = slice(sp.offsets[r], sp.offsets[r + 1])
+        want = ko.pool_blocks(kc, sp.pages[blk], sp.n_valid[blk], [want_w[r]], [0] * (blk.stop - blk.start))
+        assert_vec_close(got[sp.pages[blk]], want, f"weighted vb r={r}")
