@@ -66,11 +66,52 @@ struct RowSlice {
       v[0] = q[0];
     }
   }
+  // the same from global memory through the read-only path
+  __device__ __forceinline__ void load_global(const float* row, int lane) {
+    const float* q = row + lane * kPer;
+    if (kPer == 8) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(q));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(q) + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else if (kPer == 4) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(q));
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else if (kPer == 2) {
+      const float2 a = __ldg(reinterpret_cast<const float2*>(q));
+      v[0] = a.x; v[1] = a.y;
+    } else {
+      v[0] = __ldg(q);
+    }
+  }
   __device__ __forceinline__ void zero() {
 #pragma unroll
     for (int e = 0; e < kPer; ++e) v[e] = 0.f;
   }
 };
+
+// Sums NV values (a power of two, <= 32) across the warp at once: afterwards
+// lane L holds in v[0] the warp total of value L % NV. A butterfly that keeps
+// half of the values at every step: 31 shuffles for 32 values instead of
+// 5 per value.
+template <int NV>
+__device__ __forceinline__ void warp_sum_transpose(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int o = 16; o >= NV; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(kFull, v[i], o);
+#pragma unroll
+  for (int n = NV; n > 1; n >>= 1) {
+    const int o = n >> 1;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -290,53 +331,65 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
           sm.pg[tid] = pg;
           __syncthreads();
         }
-        // warp w scores tile slots w, w + 8, w + 16, ...; kUnroll rows in flight
-        for (int base = warp; base < tcount; base += kWarps * kUnroll) {
-          RowSlice<D> b[kUnroll];
+        // warp w scores tile slots w, w + 8, w + 16, ...; kRows rows in flight
+        constexpr int kRows = D <= 128 ? 16 : 8;
+        for (int base = warp; base < tcount; base += kWarps * kRows) {
+          RowSlice<D> b[kRows];
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
+          for (int u = 0; u < kRows; ++u) {
             // always load (row 0 for empty slots, masked below): no branch, so
-            // all kUnroll rows are in flight together
+            // all kRows rows are in flight together
             const int slot = base + u * kWarps;
             const int pg = slot < tcount ? sm.pg[slot] : -1;
             const bool staged = first && slot < nstage;
-            const float* row = (staged || pg < 0) ? &sm.stage[staged ? slot : 0][0] : p.vb + (long long)pg * D;
-            b[u].load(row, lane);
+            if (staged) {
+              b[u].load(&sm.stage[slot][0], lane);  // bulk-copied into shared memory
+            } else {
+              b[u].load_global(p.vb + (long long)(pg < 0 ? 0 : pg) * D, lane);
+            }
             if (pg < 0 || (staged && !staged_ok)) b[u].zero();
           }
+          // per-lane partial dots and squared norms of the kRows rows, then
+          // one transposed reduction: lane u ends with row u's dot, lane
+          // kRows + u with its squared norm
+          float part[2 * kRows];
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
-            const int slot = base + u * kWarps;
+          for (int u = 0; u < kRows; ++u) {
             float dot = 0.f, n2 = 0.f;
 #pragma unroll
             for (int e = 0; e < RowSlice<D>::kPer; ++e) {
               dot = fmaf(a.v[e], b[u].v[e], dot);
               n2 = fmaf(b[u].v[e], b[u].v[e], n2);
             }
-            dot = warp_sum(dot);
-            n2 = warp_sum(n2);
-            if (lane == 0 && slot < tcount) {
-              float cosv = 0.f;
-              if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
-              cosv = fminf(1.f, fmaxf(-1.f, cosv));
-              const float sc = fmaf(0.5f, cosv, 0.5f);
-              const int j = tile0 + slot;
-              if (p.scores_out) p.scores_out[off + j] = sc;
-              uint64_t key = 0ull;
-              if (sm.pg[slot] >= 0) {
-                if (p.hist) {
-                  // stability filter: shift this step's bit into the block's window
-                  const uint32_t wmask = p.stab_w >= 32 ? 0xFFFFFFFFu : ((1u << p.stab_w) - 1u);
-                  const uint32_t h = ((p.hist[off + j] << 1) | (sc > p.stab_theta ? 1u : 0u)) & wmask;
-                  p.hist[off + j] = h;
-                  if (p.stab_out) p.stab_out[off + j] = (float)__popc(h) / (float)p.stab_w;
-                  key = make_stab_key((uint32_t)__popc(h), sc, (uint32_t)j);
-                } else {
-                  key = make_key(sc, (uint32_t)j);
-                }
+            part[u] = dot;
+            part[kRows + u] = n2;
+          }
+          warp_sum_transpose<2 * kRows>(part, lane);
+          const float n2 = __shfl_down_sync(kFull, part[0], kRows);
+          const int u = lane;
+          const int slot = base + u * kWarps;
+          if (u < kRows && slot < tcount) {
+            const float dot = part[0];
+            float cosv = 0.f;
+            if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
+            cosv = fminf(1.f, fmaxf(-1.f, cosv));
+            const float sc = fmaf(0.5f, cosv, 0.5f);
+            const int j = tile0 + slot;
+            if (p.scores_out) p.scores_out[off + j] = sc;
+            uint64_t key = 0ull;
+            if (sm.pg[slot] >= 0) {
+              if (p.hist) {
+                // stability filter: shift this step's bit into the block's window
+                const uint32_t wmask = p.stab_w >= 32 ? 0xFFFFFFFFu : ((1u << p.stab_w) - 1u);
+                const uint32_t h = ((p.hist[off + j] << 1) | (sc > p.stab_theta ? 1u : 0u)) & wmask;
+                p.hist[off + j] = h;
+                if (p.stab_out) p.stab_out[off + j] = (float)__popc(h) / (float)p.stab_w;
+                key = make_stab_key((uint32_t)__popc(h), sc, (uint32_t)j);
+              } else {
+                key = make_key(sc, (uint32_t)j);
               }
-              sm.keys[slot] = key;
             }
+            sm.keys[slot] = key;
           }
         }
       } else {
