@@ -55,6 +55,23 @@ struct HierArgs {
   int* err;
 };
 
+// kPer consecutive floats of a global row through the read-only path.
+template <int kPer>
+__device__ __forceinline__ void load_row_slice(const float* q, float (&x)[kPer]) {
+  if constexpr (kPer == 8) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(q)), b = __ldg(reinterpret_cast<const float4*>(q) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else if constexpr (kPer == 4) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(q));
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  } else if constexpr (kPer == 2) {
+    const float2 a = __ldg(reinterpret_cast<const float2*>(q));
+    x[0] = a.x; x[1] = a.y;
+  } else {
+    x[0] = __ldg(q);
+  }
+}
+
 // Descending bitonic sort of n keys (padded with 0 to a power of two).
 __device__ void sort_desc(uint64_t* keys, int n) {
   int p2 = 1;
@@ -86,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
   __shared__ float s_va[D];
   __shared__ uint32_t s_gbits[kHierMax / 32];  // kept Grids
   __shared__ uint32_t s_cbits[kHierMax / 32];  // kept Chunks
-  __shared__ int s_n, s_wsum[kWarps];
+  __shared__ int s_wsum[kWarps];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int off = a.bt.offsets[r];
   int nb = a.bt.offsets[r + 1] - off;
@@ -113,43 +130,69 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
   for (int o = 16; o > 0; o >>= 1) na2 += __shfl_xor_sync(kFull, na2, o);
   const float na = sqrtf(na2);
 
-  // key of member `id` whose representation is the row at `row` (null: empty)
-  auto score_key = [&](const float* row, uint32_t id) -> uint64_t {
-    float dot = 0.f, n2 = 0.f;
-    if (row) {
-      const float* q = row + lane * kPer;
+  // keys of up to 16 members whose representations are rows[0..16) (null:
+  // empty) in one pass: per-lane partial dots and squared norms, one
+  // transposed warp reduction, lane u < 16 forms member u's key
+  auto score_keys16 = [&](const float* const (&rows)[16], const uint32_t (&ids)[16]) -> uint64_t {
+    float part[32];
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        const float x = q[e];
-        dot = fmaf(va_l[e], x, dot);
-        n2 = fmaf(x, x, n2);
+    for (int u = 0; u < 16; ++u) {
+      float dot = 0.f, n2 = 0.f;
+      if (rows[u]) {
+        float x[kPer];
+        load_row_slice<kPer>(rows[u] + lane * kPer, x);
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          dot = fmaf(va_l[e], x[e], dot);
+          n2 = fmaf(x[e], x[e], n2);
+        }
+      }
+      part[u] = dot;
+      part[16 + u] = n2;
+    }
+#pragma unroll
+    for (int n = 32; n > 1; n >>= 1) {
+      const int o = n >> 1;
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = upper ? part[i] : part[i + n / 2];
+        const float keep = upper ? part[i + n / 2] : part[i];
+        part[i] = keep + __shfl_xor_sync(kFull, send, o);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      dot += __shfl_xor_sync(kFull, dot, o);
-      n2 += __shfl_xor_sync(kFull, n2, o);
-    }
+    const float n2 = __shfl_down_sync(kFull, part[0], 16);
     float cosv = 0.f;
-    if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
+    if (na2 > 0.f && n2 > 0.f) cosv = part[0] / (na * sqrtf(n2));
     cosv = fminf(1.f, fmaxf(-1.f, cosv));
+    uint32_t id = 0;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) id = lane == u ? ids[u] : id;
     return make_key(fmaf(0.5f, cosv, 0.5f), id);
   };
 
-  // One level: members m in [0, n_all) that pass `active(m)` are scored
-  // (representation row(m)), sorted, and the best ceil(n * permille / 1000)
-  // are marked in `bits` (when given); returns the number kept.
-  auto level = [&](int n_all, auto&& active, auto&& row_of, uint32_t* bits, int permille) -> int {
-    if (tid == 0) s_n = 0;
-    __syncthreads();
-    // compact the active members' indices into s_keys (each slot becomes
-    // the member's key below)
+  // One level: the active members are the children of the kept parents
+  // (parent p holds members [p * fan, min((p + 1) * fan, n_members)); every
+  // parent is kept when `pbits` is null). They are scored (representation
+  // row_of(m)) and sorted, and the best ceil(n * permille / 1000) are marked
+  // in `bits` (when given); returns the number kept.
+  auto level = [&](int n_parents, int fan, int n_members, const uint32_t* pbits, auto&& row_of, uint32_t* bits,
+                   int permille) -> int {
+    // list the active members' indices in s_keys (each slot becomes the
+    // member's key below): one thread per parent, a block scan of the counts
     int n = 0;
-    for (int base = 0; base < n_all; base += kThreads) {
-      const int m = base + tid;
-      const bool act = m < n_all && active(m);
-      const unsigned bal = __ballot_sync(kFull, act);
-      if (lane == 0) s_wsum[warp] = __popc(bal);
+    for (int base = 0; base < n_parents; base += kThreads) {
+      const int p = base + tid;
+      int cnt = 0;
+      if (p < n_parents && (!pbits || ((pbits[p >> 5] >> (p & 31)) & 1u)))
+        cnt = max(0, min(fan, n_members - p * fan));
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) s_wsum[warp] = incl;
       __syncthreads();
       int before = 0, total = 0;
 #pragma unroll
@@ -157,17 +200,25 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
         before += w < warp ? s_wsum[w] : 0;
         total += s_wsum[w];
       }
-      const int slot = n + before + __popc(bal & ((1u << lane) - 1u));
-      if (act) s_keys[slot] = (uint64_t)(uint32_t)m;  // index for now
+      const int slot = n + before + incl - cnt;
+      for (int c = 0; c < cnt; ++c) s_keys[slot + c] = (uint64_t)(uint32_t)(p * fan + c);  // index for now
       n += total;
       __syncthreads();
     }
-    // score every active member (one warp each), replacing its slot by the key
-    for (int i = warp; i < n; i += kWarps) {
-      const uint32_t m = (uint32_t)s_keys[i];
+    // score the active members, sixteen per warp at a time, replacing each
+    // slot by the member's key
+    for (int i0 = warp * 16; i0 < n; i0 += kWarps * 16) {
+      const float* rows[16];
+      uint32_t ids[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const bool have = i0 + u < n;
+        ids[u] = have ? (uint32_t)s_keys[i0 + u] : 0u;
+        rows[u] = have ? row_of((int)ids[u]) : nullptr;
+      }
       __syncwarp();
-      const uint64_t key = score_key(row_of((int)m), m);
-      if (lane == 0) s_keys[i] = key;
+      const uint64_t key = score_keys16(rows, ids);
+      if (lane < 16 && i0 + lane < n) s_keys[i0 + lane] = key;
     }
     __syncthreads();
     sort_desc(s_keys, n);
@@ -182,12 +233,11 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
   };
 
   const long long rrow = (long long)r;
-  level(G, [&](int) { return true; },
-        [&](int g) { return a.grid + (rrow * a.g_max + g) * D; }, s_gbits, a.permille[0]);
-  level(C, [&](int c) { return (s_gbits[(c / a.grid_chunks) >> 5] >> ((c / a.grid_chunks) & 31)) & 1u; },
-        [&](int c) { return a.chunk + (rrow * a.c_max + c) * D; }, s_cbits, a.permille[1]);
+  level(G, 1, G, nullptr, [&](int g) { return a.grid + (rrow * a.g_max + g) * D; }, s_gbits, a.permille[0]);
+  level(G, a.grid_chunks, C, s_gbits, [&](int c) { return a.chunk + (rrow * a.c_max + c) * D; }, s_cbits,
+        a.permille[1]);
   const int kp = level(
-      nb, [&](int j) { return (s_cbits[(j / a.chunk_pages) >> 5] >> ((j / a.chunk_pages) & 31)) & 1u; },
+      C, a.chunk_pages, nb, s_cbits,
       [&](int j) -> const float* {
         const int pg = a.bt.pages[off + j];
         if (pg < 0 || pg >= a.vb_rows) {
