@@ -8,10 +8,14 @@
 //
 // grid_reps_kernel builds the Grid level from the Chunk level (the Chunk
 // level is kk_coarse_means over the blocks). hier_select_kernel runs the
-// three levels for one request per CTA: score the level's active members
-// (one warp per member, 16-byte loads), sort their 64-bit keys (score, index)
-// in shared memory, keep the best share and mark it; the last level's kept
-// blocks are written in kk_topk order.
+// three levels for one request per thread-block cluster (one CTA unless a
+// few long requests leave SMs idle): every CTA lists the level's active
+// members, scores its share (sixteen per warp, one transposed reduction) and
+// stores the 64-bit keys (score, index) into the leader's shared memory; the
+// leader sorts them, keeps the best share and sends the kept bitmap to every
+// CTA; the last level's kept blocks are written in kk_topk order.
+#include <mutex>
+
 #include "kk_device.cuh"
 #include "kk_internal.h"
 
@@ -20,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kHierOut = 2048;  // output blocks ordered by rank counting (more: a full sort)
 
 // grid[r][g][d] = mean over chunks c in [g*gc, min((g+1)*gc, C_r)) of
 // chunk[r][c][d] (float64 sum), zero past the request's last Grid.
@@ -72,22 +77,46 @@ __device__ __forceinline__ void load_row_slice(const float* q, float (&x)[kPer])
   }
 }
 
-// Descending bitonic sort of n keys (padded with 0 to a power of two).
-__device__ void sort_desc(uint64_t* keys, int n) {
+__device__ __forceinline__ uint64_t lds_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// Descending bitonic sort of n keys in shared memory (padded with 0 to a
+// power of two). Each stage walks the p2/2 compare-exchange pairs, eight per
+// thread at a time: all eight pairs are loaded before any is stored, so the
+// loads overlap.
+__device__ __forceinline__ void sort_desc(uint64_t* keys_ptr, int n) {
+  constexpr int kBatch = 8;
+  const uint32_t keys = smem_u32(keys_ptr);
   int p2 = 1;
   while (p2 < n) p2 <<= 1;
-  for (int i = n + threadIdx.x; i < p2; i += kThreads) keys[i] = 0ull;
+  for (int i = n + threadIdx.x; i < p2; i += kThreads) sts_u64(keys + i * 8, 0ull);
   __syncthreads();
+  const int pairs = p2 >> 1;
   for (int k = 2; k <= p2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < p2; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = keys[i], b = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            keys[i] = b;
-            keys[ixj] = a;
+      for (int q0 = threadIdx.x; q0 < pairs; q0 += kThreads * kBatch) {
+        int lo[kBatch];
+        uint64_t a[kBatch], b[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int q = q0 + u * kThreads;
+          lo[u] = q < pairs ? (((q & ~(j - 1)) << 1) | (q & (j - 1))) : -1;  // j is a power of two
+          a[u] = lo[u] >= 0 ? lds_u64(keys + lo[u] * 8) : 0ull;
+          b[u] = lo[u] >= 0 ? lds_u64(keys + (lo[u] + j) * 8) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (lo[u] < 0) continue;
+          const bool desc = (lo[u] & k) == 0;
+          if (desc ? (a[u] < b[u]) : (a[u] > b[u])) {
+            sts_u64(keys + lo[u] * 8, b[u]);
+            sts_u64(keys + (lo[u] + j) * 8, a[u]);
           }
         }
       }
@@ -96,15 +125,67 @@ __device__ void sort_desc(uint64_t* keys, int n) {
   }
 }
 
+// The smallest key T such that exactly k of keys[0..n) (distinct, in shared
+// memory) are >= T: a radix select on 8-bit digits, most significant first,
+// stopping as soon as a digit's bucket holds exactly the keys still needed.
+// `hist` is 256 ints of shared memory, `s_sel` two ints; k in [1, n].
+__device__ __forceinline__ uint64_t kth_largest(const uint64_t* keys_ptr, int n, int k, int* hist, int* s_sel) {
+  const uint32_t keys = smem_u32(keys_ptr);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t prefix = 0ull, pmask = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint64_t key = lds_u64(keys + i * 8);
+      if ((key & pmask) == prefix) atomicAdd(&hist[(int)((key >> shift) & 255)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // counts above each lane's 8 buckets (255 .. 0 from the top)
+      int local = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) local += hist[lane * 8 + b];
+      int sfx = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, sfx, o);
+        if (lane + o < 32) sfx += y;
+      }
+      int above = sfx - local;
+      for (int b = 7; b >= 0; --b) {
+        const int hb = hist[lane * 8 + b];
+        if (above < need && above + hb >= need) {
+          s_sel[0] = lane * 8 + b;
+          s_sel[1] = above;
+        }
+        above += hb;
+      }
+    }
+    __syncthreads();
+    const int b = s_sel[0];
+    need -= s_sel[1];
+    prefix |= (uint64_t)b << shift;
+    pmask |= (uint64_t)0xFF << shift;
+    const bool exact = hist[b] == need;  // every key of this bucket is needed
+    __syncthreads();
+    if (exact) break;
+  }
+  return prefix;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs a) {
   constexpr int kPer = D / 32;
-  extern __shared__ __align__(16) uint64_t s_keys[];  // [kHierMax]
+  extern __shared__ __align__(16) uint64_t s_keys[];  // [kHierMax] level list, then [kHierOut] output stage
   __shared__ float s_va[D];
   __shared__ uint32_t s_gbits[kHierMax / 32];  // kept Grids
   __shared__ uint32_t s_cbits[kHierMax / 32];  // kept Chunks
   __shared__ int s_wsum[kWarps];
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int s_hist[256], s_sel[2], s_cnt;
+  const int r = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int CL = (int)cluster_size(), crank = (int)cluster_rank();
   const int off = a.bt.offsets[r];
   int nb = a.bt.offsets[r + 1] - off;
   if (nb < 0 || nb > a.bt.max_blocks) {
@@ -173,11 +254,14 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
 
   // One level: the active members are the children of the kept parents
   // (parent p holds members [p * fan, min((p + 1) * fan, n_members)); every
-  // parent is kept when `pbits` is null). They are scored (representation
-  // row_of(m)) and sorted, and the best ceil(n * permille / 1000) are marked
-  // in `bits` (when given); returns the number kept.
+  // parent is kept when `pbits` is null). Every CTA of the cluster lists
+  // them; CTA c scores its share and stores the keys into the leader's
+  // list; the leader sorts, keeps the best ceil(n * permille / 1000), marks
+  // them in `bits` (when given) and copies those words to every CTA. Returns
+  // the number kept.
+  int n_last = 0;  // members of the most recent level
   auto level = [&](int n_parents, int fan, int n_members, const uint32_t* pbits, auto&& row_of, uint32_t* bits,
-                   int permille) -> int {
+                   int n_bits, int permille) -> int {
     // list the active members' indices in s_keys (each slot becomes the
     // member's key below): one thread per parent, a block scan of the counts
     int n = 0;
@@ -205,36 +289,58 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
       n += total;
       __syncthreads();
     }
-    // score the active members, sixteen per warp at a time, replacing each
-    // slot by the member's key
-    for (int i0 = warp * 16; i0 < n; i0 += kWarps * 16) {
+    // every CTA has its list before any key lands in the leader's
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    // score this CTA's share, sixteen members per warp at a time
+    const int i_lo = (int)((long long)n * crank / CL), i_hi = (int)((long long)n * (crank + 1) / CL);
+    const uint32_t keys0 = map_to_rank(smem_u32(s_keys), 0);
+    for (int i0 = i_lo + warp * 16; i0 < i_hi; i0 += kWarps * 16) {
       const float* rows[16];
       uint32_t ids[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        const bool have = i0 + u < n;
+        const bool have = i0 + u < i_hi;
         ids[u] = have ? (uint32_t)s_keys[i0 + u] : 0u;
         rows[u] = have ? row_of((int)ids[u]) : nullptr;
       }
       __syncwarp();
       const uint64_t key = score_keys16(rows, ids);
-      if (lane < 16 && i0 + lane < n) s_keys[i0 + lane] = key;
+      if (lane < 16 && i0 + lane < i_hi) st_cluster_u64(keys0 + (uint32_t)((i0 + lane) * 8), key);
     }
-    __syncthreads();
-    sort_desc(s_keys, n);
-    const int k = (int)(((long long)n * permille + 999) / 1000);
-    if (bits)
-      for (int i = tid; i < k; i += kThreads) {
-        const uint32_t m = key_index(s_keys[i]);
-        atomicOr(&bits[m >> 5], 1u << (m & 31));
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    int k = (int)(((long long)n * permille + 999) / 1000);
+    n_last = n;
+    if (crank == 0 && bits && k > 0) {
+      // the kept members: the k largest keys
+      const uint64_t thr = kth_largest(s_keys, n, k, s_hist, s_sel);
+      for (int i = tid; i < n; i += kThreads) {
+        const uint64_t key = s_keys[i];
+        if (key >= thr) {
+          const uint32_t m = key_index(key);
+          atomicOr(&bits[m >> 5], 1u << (m & 31));
+        }
       }
-    __syncthreads();
+      __syncthreads();
+    }
+    if (crank == 0) {
+      if (bits) {
+        for (int q = 1; q < CL; ++q)
+          for (int i = tid; i < (n_bits + 31) / 32; i += kThreads)
+            st_cluster_s32(map_to_rank(smem_u32(&bits[i]), q), (int)bits[i]);
+      }
+    }
+    if (bits) {  // the kept bits reach every CTA before the next level
+      cluster_arrive_release();
+      cluster_wait_acquire();
+    }
     return k;
   };
 
   const long long rrow = (long long)r;
-  level(G, 1, G, nullptr, [&](int g) { return a.grid + (rrow * a.g_max + g) * D; }, s_gbits, a.permille[0]);
-  level(G, a.grid_chunks, C, s_gbits, [&](int c) { return a.chunk + (rrow * a.c_max + c) * D; }, s_cbits,
+  level(G, 1, G, nullptr, [&](int g) { return a.grid + (rrow * a.g_max + g) * D; }, s_gbits, G, a.permille[0]);
+  level(G, a.grid_chunks, C, s_gbits, [&](int c) { return a.chunk + (rrow * a.c_max + c) * D; }, s_cbits, C,
         a.permille[1]);
   const int kp = level(
       C, a.chunk_pages, nb, s_cbits,
@@ -246,24 +352,104 @@ __global__ void __launch_bounds__(kThreads) hier_select_kernel(const HierArgs a)
         }
         return a.vb + (long long)pg * D;
       },
-      nullptr, a.permille[2]);
+      nullptr, 0, a.permille[2]);
+  if (crank != 0) return;
+  // the first m = min(K, kp) blocks of the last level in kk_topk order: the
+  // m largest keys, each written at its rank among them
   int* io = a.idx + (long long)r * a.K;
   float* to = a.top ? a.top + (long long)r * a.K : nullptr;
-  for (int i = tid; i < a.K; i += kThreads) {
-    const bool have = i < kp;
-    io[i] = have ? (int)key_index(s_keys[i]) : -1;
-    if (to) to[i] = have ? key_score(s_keys[i]) : -__int_as_float(0x7f800000);
+  const int m = min(a.K, kp);
+  const int n3 = n_last;
+  if (m > 0 && m <= kHierOut) {
+    // the m largest keys, staged past the level's list, each written at its
+    // rank among them
+    const uint64_t thr = kth_largest(s_keys, n3, m, s_hist, s_sel);
+    uint64_t* stage = s_keys + kHierMax;
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (int i = tid; i < n3; i += kThreads) {
+      const uint64_t key = s_keys[i];
+      if (key >= thr) stage[atomicAdd(&s_cnt, 1)] = key;
+    }
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      const uint64_t key = stage[i];
+      int rank = 0;
+      for (int q = 0; q < m; ++q) rank += stage[q] > key;
+      io[rank] = (int)key_index(key);
+      if (to) to[rank] = key_score(key);
+    }
+  } else if (m > 0) {  // a very long output: sort the whole level
+    sort_desc(s_keys, n3);
+    for (int i = tid; i < m; i += kThreads) {
+      io[i] = (int)key_index(s_keys[i]);
+      if (to) to[i] = key_score(s_keys[i]);
+    }
+  }
+  for (int i = m + tid; i < a.K; i += kThreads) {
+    io[i] = -1;
+    if (to) to[i] = -__int_as_float(0x7f800000);
   }
   if (tid == 0 && a.kept) a.kept[r] = kp;
 }
 
 template <int D>
 cudaError_t launch_select_t(const HierArgs& a, cudaStream_t s) {
-  constexpr int smem = kHierMax * (int)sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(hier_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = (kHierMax + kHierOut) * (int)sizeof(uint64_t);
+  static std::mutex mu;
+  static int caps[64][kMaxCluster + 1];  // co-resident clusters of each size, per device (-1: not yet asked)
+  static bool ready[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  hier_select_kernel<D><<<a.bt.R, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      e = cudaFuncSetAttribute(hier_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(hier_select_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      for (int cl = 1; cl <= kMaxCluster; cl <<= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cl, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, hier_select_kernel<D>, &cfg) != cudaSuccess) n = 0;
+        (void)cudaGetLastError();  // an unsupported size is not an error here
+        caps[dev][cl] = n;
+      }
+      ready[dev] = true;
+    }
+  }
+  // A cluster per request splits each level's scoring over CL SMs: worth it
+  // only for a few long requests (otherwise one CTA per request already
+  // fills the GPU).
+  int cl = 1;
+  const int sms = sm_count();
+  for (int c = 2; c <= kMaxCluster; c <<= 1)
+    if ((long long)a.bt.R * c <= sms && a.bt.max_blocks >= 256 * c && caps[dev][c] >= a.bt.R) cl = c;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl, a.bt.R);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, hier_select_kernel<D>, a);
 }
 
 }  // namespace
