@@ -48,6 +48,17 @@ Cache 重要性评估" (cited below as [KK §n]):
   the fraction is always over W (before W steps exist the missing steps count
   as not high), and the loading decision ranks blocks by stability, then by
   the current affinity, then by the lower index.
+* [KK §5.1], the three levels in one product: the representations of all
+  levels are rows of one matrix scored against the anchors at once, and
+  boolean parent -> child masks do the filtering. Reading used here for a
+  pool shared by many anchors (the batched scorer's pool): Chunks are
+  consecutive pool ids and Grids consecutive Chunks, with the pool's own
+  coarse representations (the same for every anchor); for one anchor a
+  coarse member is active only if it covers at least one block the anchor's
+  mask allows (below the Grid level also only if its parent was kept), and a
+  block is active if the mask allows it and its Chunk was kept. With a mask
+  that allows exactly one request's blocks, in order and starting on a Grid
+  boundary, this is the per-request hierarchy above.
 
 Every function accumulates in float64. bf16 inputs are decoded exactly
 (bits << 16). Parity of the variance weighting and of the (1+cos)/2 formula
@@ -76,6 +87,7 @@ __all__ = [
     "append_token",
     "hier_reps",
     "hier_select",
+    "hier_select_pool",
 ]
 
 
@@ -380,3 +392,54 @@ def hier_select(vb_logical, va, K: int, chunk_pages: int = 64, grid_chunks: int 
     idx[:m] = p_keep[:m]
     val[:m] = s[p_keep[:m]]
     return idx, val, len(p_keep), np.sort(g_keep), np.sort(c_keep)
+
+
+def hier_select_pool(A, grids, chunks, V, mask_words, K: int, chunk_pages: int = 64, grid_chunks: int = 8,
+                     permille=(500, 200, 100)):
+    """Hierarchical selection over a shared pool for R anchors [KK §5.1]:
+    every Grid, Chunk and block representation is scored against every anchor
+    (one product), then per anchor the levels are filtered top down. A level
+    keeps ceil(n * permille / 1000) of its n active members (ties to the
+    lower index). Active Grids: those covering an allowed block. Active
+    Chunks: those of kept Grids covering an allowed block. Active blocks:
+    allowed blocks of kept Chunks.
+
+    A: [R][D] anchors; grids [G][D], chunks [C][D], V [N][D] (bf16 bits or
+    floats), Chunk c = blocks [c*chunk_pages, (c+1)*chunk_pages) of the pool,
+    Grid g = Chunks [g*grid_chunks, (g+1)*grid_chunks); mask_words uint32
+    [R][ceil(N/32)], bit (j % 32) of word j // 32 allows block j.
+    Returns (idx int64 [R][K] pool ids in kk_topk order, score float64
+    [R][K], kept int64 [R] blocks the last level keeps).
+    """
+    A = decode(A)
+    grids = np.atleast_2d(decode(grids))
+    chunks = np.atleast_2d(decode(chunks))
+    V = decode(V)
+    R, N = A.shape[0], V.shape[0]
+    C = -(-N // chunk_pages) if N else 0
+    G = -(-C // grid_chunks) if C else 0
+    assert chunks.shape[0] == C and grids.shape[0] == G
+    mw = np.asarray(mask_words, dtype=np.uint32)
+    idx = np.full((R, K), -1, dtype=np.int64)
+    val = np.full((R, K), -np.inf)
+    kept = np.zeros(R, dtype=np.int64)
+    for r in range(R):
+        j = np.arange(N)
+        allowed = ((mw[r, j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool) if N else np.zeros(0, bool)
+        chunk_allowed = np.zeros(C, dtype=bool)
+        chunk_allowed[j[allowed] // chunk_pages] = True
+        grid_allowed = np.zeros(G, dtype=bool)
+        grid_allowed[np.arange(C)[chunk_allowed] // grid_chunks] = True
+        s_g = affinity(grids, A[r]) if G else np.zeros(0)
+        s_c = affinity(chunks, A[r]) if C else np.zeros(0)
+        s_p = affinity(V, A[r]) if N else np.zeros(0)
+        g_keep = set(_keep(s_g, np.arange(G)[grid_allowed], permille[0]).tolist())
+        c_active = [c for c in range(C) if chunk_allowed[c] and c // grid_chunks in g_keep]
+        c_keep = set(_keep(s_c, c_active, permille[1]).tolist())
+        p_active = [b for b in range(N) if allowed[b] and b // chunk_pages in c_keep]
+        p_keep = _keep(s_p, p_active, permille[2])
+        m = min(K, len(p_keep))
+        idx[r, :m] = p_keep[:m]
+        val[r, :m] = s_p[p_keep[:m]]
+        kept[r] = len(p_keep)
+    return idx, val, kept

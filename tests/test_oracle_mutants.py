@@ -253,6 +253,59 @@ def m_hier_rates_of_all_members(o):
     o.hier_select = hier_select
 
 
+def _hier_pool_variant(o, coarse_mask=True, page_mask=True, share_of_active=True):
+    """The shared-pool hierarchy with one of its rules changed."""
+    def hier_select_pool(A, grids, chunks, V, mask_words, K, chunk_pages=64, grid_chunks=8,
+                         permille=(500, 200, 100)):
+        A, grids, chunks, V = (np.atleast_2d(ko.decode(x)) for x in (A, grids, chunks, V))
+        R, N, C, G = A.shape[0], V.shape[0], chunks.shape[0], grids.shape[0]
+        mw = np.asarray(mask_words, dtype=np.uint32)
+        idx = np.full((R, K), -1, dtype=np.int64)
+        val = np.full((R, K), -np.inf)
+        kept = np.zeros(R, dtype=np.int64)
+
+        def keep(scores, members, pool, q):
+            members = np.asarray(members, dtype=np.int64)
+            k = -(-(len(members) if share_of_active else pool) * int(q) // 1000)
+            order = np.lexsort((members, -np.asarray(scores)[members]))
+            return members[order[:k]]
+
+        for r in range(R):
+            j = np.arange(N)
+            allowed = ((mw[r, j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool)
+            c_ok = np.zeros(C, bool)
+            c_ok[j[allowed] // chunk_pages] = True
+            g_ok = np.zeros(G, bool)
+            g_ok[np.arange(C)[c_ok] // grid_chunks] = True
+            if not coarse_mask:
+                c_ok[:] = True
+                g_ok[:] = True
+            s_g, s_c, s_p = ko.affinity(grids, A[r]), ko.affinity(chunks, A[r]), ko.affinity(V, A[r])
+            gk = set(keep(s_g, np.nonzero(g_ok)[0], G, permille[0]).tolist())
+            ca = [c for c in range(C) if c_ok[c] and c // grid_chunks in gk]
+            ck = set(keep(s_c, ca, int(c_ok.sum()), permille[1]).tolist())
+            pa = [b for b in range(N) if (allowed[b] or not page_mask) and b // chunk_pages in ck]
+            pk = keep(s_p, pa, int(allowed.sum()), permille[2])
+            m = min(K, len(pk))
+            idx[r, :m] = pk[:m]
+            val[r, :m] = s_p[pk[:m]]
+            kept[r] = len(pk)
+        return idx, val, kept
+    o.hier_select_pool = hier_select_pool
+
+
+def m_hier_pool_coarse_ignores_mask(o):
+    _hier_pool_variant(o, coarse_mask=False)
+
+
+def m_hier_pool_blocks_ignore_mask(o):
+    _hier_pool_variant(o, page_mask=False)
+
+
+def m_hier_pool_share_of_allowed(o):
+    _hier_pool_variant(o, share_of_active=False)
+
+
 MUTANTS = [
     m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
     m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
@@ -262,6 +315,7 @@ MUTANTS = [
     m_stability_divides_by_steps_seen, m_stability_window_one_too_long, m_stable_topk_ignores_stability,
     m_compact_table_keeps_topk_order, m_append_token_divides_by_block_size, m_append_token_slot_off_by_one,
     m_hier_grid_is_mean_of_pages, m_hier_no_mask, m_hier_rates_of_all_members,
+    m_hier_pool_coarse_ignores_mask, m_hier_pool_blocks_ignore_mask, m_hier_pool_share_of_allowed,
 ]
 
 

@@ -361,12 +361,83 @@ def check_hier_invariants(o):
     np.testing.assert_allclose(grids[0], [2.0 / 3.0, 1.0 / 3.0], rtol=0, atol=1e-15)
 
 
+def check_hier_pool_golden(o):
+    g = gold("hier_pool.json")
+    vb = np.array(g["vb"], dtype=np.float64)
+    for c in g["cases"]:
+        idx, val, kept = o.hier_select_pool(np.array([c["va"]]), np.array(g["grids"]), np.array(g["chunks"]), vb,
+                                            np.array([[c["mask"]]], dtype=np.uint32), c["K"], g["chunk_pages"],
+                                            g["grid_chunks"], c["permille"])
+        assert list(idx[0]) == c["idx"] and kept[0] == c["kept"], c
+
+
+def _zeroed_levels(sg, sc, sp, allowed, cp, gc, pm):
+    """The page's formulation, as plain loops: scores of members whose parent
+    was not kept (or that cover no allowed block) are set to zero, and each
+    level takes its share of the active count from the whole zeroed level."""
+    N, C, G = len(sp), len(sc), len(sg)
+    c_ok = [any(allowed[b] for b in range(c * cp, min(N, (c + 1) * cp))) for c in range(C)]
+    g_ok = [any(c_ok[c] for c in range(g * gc, min(C, (g + 1) * gc))) for g in range(G)]
+
+    def take(scores, active, q):
+        n = sum(active)
+        m = (n * q + 999) // 1000
+        z = [scores[i] if active[i] else 0.0 for i in range(len(scores))]
+        return sorted(range(len(z)), key=lambda i: (-z[i], i))[:m]
+
+    gk = set(take(sg, g_ok, pm[0]))
+    ck = set(take(sc, [c_ok[c] and c // gc in gk for c in range(C)], pm[1]))
+    return take(sp, [bool(allowed[b]) and b // cp in ck for b in range(N)], pm[2])
+
+
+def check_hier_pool_bruteforce(o):
+    rng = np.random.default_rng(33)
+    for N, cp, gc, pm, density in ((300, 8, 3, (500, 200, 100), 0.3), (64, 4, 2, (700, 500, 400), 0.05),
+                                   (257, 16, 4, (300, 1000, 250), 0.9), (40, 64, 8, (500, 500, 500), 0.5)):
+        D, R = 5, 6
+        V = rng.standard_normal((N, D))
+        A = rng.standard_normal((R, D))
+        chunks, grids = o.hier_reps(V, cp, gc)
+        bits = rng.random((R, N)) < density
+        bits[0, :] = False
+        mw = np.zeros((R, (N + 31) // 32), dtype=np.uint32)
+        for r in range(R):
+            for j in np.nonzero(bits[r])[0]:
+                mw[r, j // 32] |= np.uint32(1 << (j % 32))
+        idx, val, kept = o.hier_select_pool(A, grids, chunks, V, mw, N, cp, gc, pm)
+        for r in range(R):
+            want = _zeroed_levels(o.affinity(grids, A[r]), o.affinity(chunks, A[r]), o.affinity(V, A[r]),
+                                  bits[r], cp, gc, pm)
+            assert kept[r] == len(want) and list(idx[r, :kept[r]]) == want, (N, r)
+            assert np.all(idx[r, kept[r]:] == -1)
+    # one request's blocks at the start of the pool, on a Grid boundary: the per-request hierarchy
+    V = rng.standard_normal((700, 4))
+    A = rng.standard_normal((1, 4))
+    chunks, grids = o.hier_reps(V, 8, 4)
+    nb = 8 * 4 * 15
+    mw = np.zeros((1, (700 + 31) // 32), dtype=np.uint32)
+    mw[0, :nb // 32] = 0xFFFFFFFF
+    idx, val, kept = o.hier_select_pool(A, grids, chunks, V, mw, 50, 8, 4, (400, 300, 200))
+    w_idx, w_val, w_kept, _, _ = o.hier_select(V[:nb], A[0], 50, 8, 4, (400, 300, 200))
+    assert kept[0] == w_kept and list(idx[0]) == list(w_idx)
+    # every level kept whole: the batched scorer's top-K of the allowed blocks
+    mw = rng.integers(0, 2**32, size=(3, (700 + 31) // 32), dtype=np.uint64).astype(np.uint32)
+    A = rng.standard_normal((3, 4))
+    idx, val, kept = o.hier_select_pool(A, grids, chunks, V, mw, 90, 8, 4, (1000, 1000, 1000))
+    w_idx, w_val = o.score_pool_batched(A, V, mw, 90)
+    assert np.array_equal(idx, w_idx) and np.array_equal(val, w_val)
+    allowed = [sum(bin(int(w)).count("1") for w in mw[r, :700 // 32]) +
+               bin(int(mw[r, 700 // 32]) & ((1 << (700 % 32)) - 1)).count("1") for r in range(3)]
+    assert list(kept) == allowed
+
+
 ALL_CHECKS = [
     check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
     check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
     check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,
     check_planted_topics, check_stability_golden, check_stability_window, check_stable_topk,
     check_compact_table_golden, check_append_token, check_hier_golden, check_hier_invariants,
+    check_hier_pool_golden, check_hier_pool_bruteforce,
 ]
 
 
