@@ -501,9 +501,52 @@ def run_pool_gpu(args, local_rank):
     warm_ms = e0.elapsed_time(e1) / 50
     owned = int(np.unpackbits(mask.view(np.uint8)).sum())
     in_bytes = A.numel() * 2 + V.numel() * 2 + mask.nbytes
+    hier = run_pool_hier(kk, dev, flush, max(args.warmup, 3), min(args.steps, 100))
     return {"ms": statistics.median(ms), "warm_ms": warm_ms, "R": R, "N": N, "K": K, "owned": owned,
             "flops": 2.0 * R * N * 128, "bytes": in_bytes + idx.numel() * 8, "clocks": clocks.summary(),
-            "launches": 2 * args.steps}
+            "launches": 2 * args.steps, "hier": hier}
+
+
+def run_pool_hier(kk, dev, flush, warmup: int, steps: int):
+    """The shared pool as documents, Grid -> Chunk -> block in one product
+    (kk_hier_select_pool: the tcgen05 GEMM over the coarse rows and the
+    blocks, then the per-anchor level selection), L2 flushed before every
+    timed call; kk_hier_pool_reps (write time) timed the same way."""
+    import torch
+
+    v_spec, a_spec, mask, K = synth.shared_pool_hier()
+    R, N, cp, gc, pm = a_spec.N, v_spec.N, 64, 8, (500, 200, 100)
+    H = kk.kk_hier_pool_coarse_rows(N, cp, gc)
+    M = torch.zeros((H + N, 128), dtype=torch.int16, device=dev)
+    M[H:] = synth.gen_rows_cuda(v_spec, device=dev)
+    A = synth.gen_rows_cuda(a_spec, device=dev)
+    mt = torch.from_numpy(mask.view(np.int32)).to(dev)
+    ws = torch.empty(kk.kk_hier_select_pool_workspace_bytes(R, N, cp, gc), dtype=torch.uint8, device=dev)
+    idx = torch.zeros((R, K), dtype=torch.int32, device=dev)
+    top = torch.zeros((R, K), device=dev)
+    kept = torch.zeros(R, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = lambda: kk.kk_hier_pool_reps(M, N, cp, gc)
+    select = lambda: kk.kk_hier_select_pool(A, M, mt, N, cp, gc, pm, idx, top, kept, ws)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 255)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    reps_us = timed(reps)
+    sel_us = timed(select)
+    if kk.kk_device_error() != 0:
+        raise RuntimeError("device error in the hierarchical shared-pool leg")
+    return {"select_us": sel_us, "reps_us": reps_us, "rows": H + N, "kept_mean": float(kept.float().mean()),
+            "flops": 2.0 * R * (H + N) * 128, "launches": 2 * steps}
 
 
 def main():
@@ -539,6 +582,9 @@ def main():
             "hbm": {"bytes": res["bytes"], "achieved_gbs": res["bytes"] / (res["ms"] * 1e-3) / 1e9,
                     "peak_gbs": float(peaks["hbm_gbs"])},
             "us_per_step": res["ms"] * 1e3, "us_per_step_warm_l2": res["warm_ms"] * 1e3,
+            "hier_select_pool_us": res["hier"]["select_us"], "hier_pool_reps_us": res["hier"]["reps_us"],
+            "hier_pool_rows": res["hier"]["rows"], "hier_pool_blocks_kept_mean": res["hier"]["kept_mean"],
+            "hier_pool_tflops": res["hier"]["flops"] / (res["hier"]["select_us"] * 1e-6) / 1e12,
             "clocks": res["clocks"], "gpu_launches": res["launches"], "e2e": None,
         }
         print(json.dumps(line))

@@ -311,6 +311,48 @@ kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint
                                 cudaStream_t stream);
 
 /*
+ * Hierarchical selection over the shared pool [KK §5.1]: the representations
+ * of all three levels are rows of one matrix, scored against every anchor in
+ * one product, and parent -> child masks filter the levels. A Chunk is
+ * chunk_pages consecutive pool blocks (C = ceil(N / chunk_pages)), a Grid
+ * grid_chunks consecutive Chunks (G = ceil(C / grid_chunks)).
+ *
+ * M: device bf16 bits [H + N][128], H = kk_hier_pool_coarse_rows(N,
+ * chunk_pages, grid_chunks) (G + C rounded up to a multiple of 128): rows
+ * [0, G) the Grids, [G, G + C) the Chunks, [G + C, H) zero, [H, H + N) the
+ * pool's blocks (the V of kk_score_pool_batched, which the caller writes).
+ *
+ * kk_hier_pool_reps writes rows [0, H) of M from its block rows: a Chunk's
+ * row is the mean of its blocks' rows, a Grid's the mean of its Chunks' (the
+ * last of each may be partial), summed in float32 and rounded once to bf16.
+ * Call it whenever the pool's blocks change.
+ *
+ * kk_hier_select_pool scores A (device bf16 bits [R][128]) against all H + N
+ * rows in one tcgen05 pass (float32 dot products of the bf16 values, (1 +
+ * cos)/2), then for each anchor keeps, level by level, ceil(n * permille /
+ * 1000) of the level's n active members (ties to the lower index), where a
+ * Grid is active if it covers a block the anchor's mask allows (mask as in
+ * kk_score_pool_batched), a Chunk if it covers an allowed block and its Grid
+ * was kept, and a block if it is allowed and its Chunk was kept. The kept
+ * blocks go to idx [R][K] (pool ids, kk_topk order, -1 / -inf padding, at
+ * most K) and top_scores (nullable); their number to kept [R] (nullable; may
+ * exceed K). 1 <= K <= 256, permille in 1..1000, D = 128, G + C <= 4096.
+ * workspace: device memory, 256-byte aligned, of at least
+ * kk_hier_select_pool_workspace_bytes(R, N, chunk_pages, grid_chunks) bytes
+ * (depends on the SM count of the current device); concurrent calls need
+ * separate workspaces. Returns KK_ERR_UNSUPPORTED beyond the limits above.
+ */
+int32_t kk_hier_pool_coarse_rows(int32_t N, int32_t chunk_pages, int32_t grid_chunks);
+kk_status kk_hier_pool_reps(uint16_t* M, int32_t N, int32_t D, int32_t chunk_pages, int32_t grid_chunks,
+                            cudaStream_t stream);
+size_t kk_hier_select_pool_workspace_bytes(int32_t R, int32_t N, int32_t chunk_pages, int32_t grid_chunks);
+kk_status kk_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32_t* mask, int32_t R, int32_t N,
+                              int32_t D, int32_t chunk_pages, int32_t grid_chunks, int32_t permille_grid,
+                              int32_t permille_chunk, int32_t permille_page, int32_t K, int32_t* idx,
+                              float* top_scores, int32_t* kept, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/*
  * Coarse representations [KK §5.1] (a coarser level's representation is the
  * mean of its children's): for request r and group g,
  *   out[r][g][d] = mean over j in [g*group, min((g+1)*group, nb_r)) of vb[pages[offsets[r]+j]][d]

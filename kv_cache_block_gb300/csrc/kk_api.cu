@@ -434,6 +434,55 @@ kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint
                                                  err, stream));
 }
 
+static bool hier_pool_dims(int32_t N, int32_t chunk_pages, int32_t grid_chunks) {
+  if (N < 0 || chunk_pages < 1 || grid_chunks < 1) return false;
+  const long long C = N > 0 ? ((long long)N + chunk_pages - 1) / chunk_pages : 0;
+  const long long G = C > 0 ? (C + grid_chunks - 1) / grid_chunks : 0;
+  return G + C <= kk::kHierPoolCoarseMax;
+}
+
+int32_t kk_hier_pool_coarse_rows(int32_t N, int32_t chunk_pages, int32_t grid_chunks) {
+  if (!hier_pool_dims(N, chunk_pages, grid_chunks)) return -1;
+  return kk::hier_pool_coarse_rows(N, chunk_pages, grid_chunks);
+}
+
+kk_status kk_hier_pool_reps(uint16_t* M, int32_t N, int32_t D, int32_t chunk_pages, int32_t grid_chunks,
+                            cudaStream_t stream) {
+  if (N < 0 || chunk_pages < 1 || grid_chunks < 1) return KK_ERR_INVALID;
+  if (D != 128 || !hier_pool_dims(N, chunk_pages, grid_chunks)) return KK_ERR_UNSUPPORTED;
+  if (N == 0) return KK_OK;
+  if (!M) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(M) % 16) return KK_ERR_UNSUPPORTED;
+  return from_cuda(kk::launch_hier_pool_reps(M, N, chunk_pages, grid_chunks, stream));
+}
+
+size_t kk_hier_select_pool_workspace_bytes(int32_t R, int32_t N, int32_t chunk_pages, int32_t grid_chunks) {
+  if (R < 0 || !hier_pool_dims(N, chunk_pages, grid_chunks)) return 0;
+  return kk::batched_workspace_bytes(R, kk::hier_pool_coarse_rows(N, chunk_pages, grid_chunks) + N);
+}
+
+kk_status kk_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32_t* mask, int32_t R, int32_t N,
+                              int32_t D, int32_t chunk_pages, int32_t grid_chunks, int32_t permille_grid,
+                              int32_t permille_chunk, int32_t permille_page, int32_t K, int32_t* idx,
+                              float* top_scores, int32_t* kept, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  const int32_t permille[3] = {permille_grid, permille_chunk, permille_page};
+  if (R < 0 || N < 0 || K < 1 || K > kk::kMaxK || chunk_pages < 1 || grid_chunks < 1) return KK_ERR_INVALID;
+  for (int32_t q : permille)
+    if (q < 1 || q > 1000) return KK_ERR_INVALID;
+  if (R == 0) return KK_OK;
+  if (D != 128 || !hier_pool_dims(N, chunk_pages, grid_chunks)) return KK_ERR_UNSUPPORTED;
+  if (!idx || !workspace || (N > 0 && (!A || !M || !mask))) return KK_ERR_INVALID;
+  if (workspace_bytes < kk_hier_select_pool_workspace_bytes(R, N, chunk_pages, grid_chunks)) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(M) % 16 ||
+      reinterpret_cast<uintptr_t>(workspace) % 256)
+    return KK_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_hier_select_pool(A, M, mask, R, N, chunk_pages, grid_chunks, permille, K, idx,
+                                               top_scores, kept, workspace, err, stream));
+}
+
 kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                           int32_t group, float* out, cudaStream_t stream) {
   kk::Table t;

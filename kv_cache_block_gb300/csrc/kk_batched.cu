@@ -45,6 +45,8 @@ constexpr int kGemmSmem =
 struct GemmArgs {
   const uint32_t* mask;
   int R, N, mask_words, tiles;
+  int coarse_rows;  // rows before the pool's blocks that every anchor scores (0: none)
+  int coarse_tiles; // tiles holding them (their rows come first, 128 per tile)
   int* counts;      // [R][P] owned candidates of each anchor in each CTA's tiles
   uint64_t* cand;   // [R][P][cap] candidate keys, one segment per (anchor, CTA)
   long long cap;    // 128 x the most tiles a CTA takes
@@ -222,10 +224,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lo = range_lo(grp), len = range_len(grp);
     auto inv_norm = [](float sq) { return sq > 0.f ? 1.f / sqrtf(sq) : 0.f; };
     // ownership bits of this anchor's 128 columns of the CTA's local tile jj
-    // (limited to columns < N): one 16-byte load when the rows allow it
+    // (limited to columns < N): one 16-byte load when the rows allow it. The
+    // tiles of coarse rows come first and take every row below coarse_rows.
     const uint32_t* mrow = g.mask + (long long)(r < g.R ? r : 0) * g.mask_words;
     auto mask_words = [&](int jj, uint32_t (&w)[4]) {
-      const int wi0 = (p + jj * P) * (kBN / 32);
+      const int tile = p + jj * P;
+      if (tile < g.coarse_tiles) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int lim = g.coarse_rows - (tile * (kBN / 32) + c) * 32;
+          w[c] = (jj >= ntiles || r >= g.R || lim <= 0) ? 0u : (lim >= 32 ? kFull : (1u << lim) - 1u);
+        }
+        return;
+      }
+      const int wi0 = (tile - g.coarse_tiles) * (kBN / 32);
       if (g.mask_vec && jj < ntiles && r < g.R) {
         const uint4 x = *reinterpret_cast<const uint4*>(mrow + wi0);
         w[0] = x.x;
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 constexpr int kSelThreads = 256;
 constexpr int kSelStage = 6144;                    // keys of a row held in shared memory (48 KB)
 constexpr int kRegKeys = kSelStage / kSelThreads;  // and then in registers, 24 per thread
-constexpr int kMaxSegs = 1024;                     // segments (GEMM CTAs per M-tile) of a row
+constexpr int kMaxSegs = kPoolMaxSegs;             // segments (GEMM CTAs per M-tile) of a row
 constexpr int kBuckets = 2048;                     // linear buckets over a row's score range
 constexpr int kTieCap = 512;                       // boundary-bucket keys ranked exactly
 
@@ -779,24 +791,34 @@ PoolLayout pool_layout(int R, int N) {
 
 size_t batched_workspace_bytes(int R, int N) { return pool_layout(R, N).bytes; }
 
-cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask, int R,
-                                      int N, int K, int* idx, float* top, void* ws, int* err,
-                                      cudaStream_t s) {
-  if (R == 0) return cudaSuccess;
-  const PoolLayout L = pool_layout(R, N);
+cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, const uint32_t* mask, int R, int N,
+                             int coarse_rows, void* ws, int* err, cudaStream_t s, PoolSegments* out) {
+  const PoolLayout L = pool_layout(R, rows);
   int* counts = static_cast<int*>(ws);
   uint64_t* cand = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + L.counts_bytes);
+  *out = PoolSegments{cand, counts, L.P, L.cap};
+  if (R == 0) return cudaSuccess;
   cudaError_t e = setup_gemm();
   if (e != cudaSuccess) return e;
   if (L.P > 0) {
     CUtensorMap ma, mv;
-    if (!make_map(&ma, A, R) || !make_map(&mv, V, N)) return cudaErrorInvalidValue;
+    if (!make_map(&ma, A, R) || !make_map(&mv, V, rows)) return cudaErrorInvalidValue;
     const int mask_words = (N + 31) / 32;
     const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
-    GemmArgs g{mask, R, N, mask_words, L.tiles, counts, cand, L.cap, mask_vec, err};
+    GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, counts, cand, L.cap, mask_vec, err};
     score_pool_kernel<<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask, int R,
+                                      int N, int K, int* idx, float* top, void* ws, int* err,
+                                      cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  PoolSegments seg;
+  cudaError_t e = launch_pool_gemm(A, V, N, mask, R, N, 0, ws, err, s, &seg);
+  if (e != cudaSuccess) return e;
   // programmatic dependent launch: the select grid is scheduled while the
   // GEMM drains and waits (griddepcontrol.wait) for its results
   cudaLaunchConfig_t cfg = {};
@@ -809,7 +831,7 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const SelArgs sa{cand, counts, L.P, L.cap, K, idx, top, err};
+  const SelArgs sa{seg.cand, seg.counts, seg.segs, seg.cap, K, idx, top, err};
   return cudaLaunchKernelEx(&cfg, select_rows_kernel, sa);
 }
 

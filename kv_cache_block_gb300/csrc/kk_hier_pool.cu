@@ -1,0 +1,401 @@
+// Hierarchical selection Grid -> Chunk -> Page over a pool shared by many
+// anchors ("Key-Key Semantic Affinity" page, §5.1): the representations of
+// all three levels are rows of one matrix M, scored against every anchor in
+// one tensor-core product, and boolean parent -> child masks filter them.
+//
+// M (bf16, 128 columns) holds the Grid rows [0, G), the Chunk rows [G, G+C),
+// zero rows up to H = the next multiple of 128, then the pool's N blocks.
+// A Chunk is chunk_pages consecutive pool blocks, a Grid grid_chunks
+// consecutive Chunks; a Chunk's row is the mean of its blocks' rows and a
+// Grid's the mean of its Chunks' (pool_reps_kernel, float32 sums rounded
+// once to bf16).
+//
+// The product is the shared-pool GEMM of kk_batched.cu with the coarse rows
+// in front: every anchor gets a key (score, row) for every coarse row and for
+// each block its mask allows. hier_pool_select_kernel then takes one anchor
+// per CTA: the coarse keys sit at known places of the anchor's segments; a
+// coarse member is active when it covers an allowed block (and, for a Chunk,
+// its Grid was kept); each level keeps ceil(n * permille / 1000) of its n
+// active members by a radix select on the 64-bit keys; the allowed blocks of
+// kept Chunks are listed in shared memory and the best of them written out.
+#include <mutex>
+
+#include "kk_device.cuh"
+#include "kk_internal.h"
+
+namespace kk {
+namespace {
+
+constexpr int kCols = 128;        // head_dim of the shared pool
+constexpr int kRepThreads = 256;  // 16 column octets x 16 row slots
+constexpr int kRepSlots = kRepThreads / (kCols / 8);
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPageStage = 8192;  // active blocks of an anchor listed in shared memory
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+// Sum of rows [j0, j1) of the pool, columns 8*oct .. 8*oct+7, over the rows
+// of this thread's slot (four rows in flight per thread).
+__device__ __forceinline__ void sum_rows(const uint16_t* V, int j0, int j1, int slot, int oct, float (&acc)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int j = j0 + slot; j < j1; j += 4 * kRepSlots) {
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int jj = j + u * kRepSlots;
+      x[u] = jj < j1 ? __ldg(reinterpret_cast<const uint4*>(V + (long long)jj * kCols + oct * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += bf16_lo(w[q]);
+        acc[2 * q + 1] += bf16_hi(w[q]);
+      }
+    }
+  }
+}
+
+// CTA b < G: Grid b, the mean over its Chunks of each Chunk's mean block;
+// G <= b < G + C: Chunk b - G; the last CTA zeroes rows [G + C, H).
+__global__ void __launch_bounds__(kRepThreads) pool_reps_kernel(uint16_t* M, int N, int cp, int gc, int G, int C,
+                                                               int H) {
+  __shared__ float s_red[kRepSlots][kCols];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  if (b == G + C) {
+    for (long long i = tid; i < (long long)(H - G - C) * kCols; i += kRepThreads)
+      M[(long long)(G + C) * kCols + i] = 0;
+    return;
+  }
+  const uint16_t* V = M + (long long)H * kCols;
+  const int oct = tid % (kCols / 8), slot = tid / (kCols / 8);
+  float out[8];
+  const int c0 = b < G ? b * gc : b - G;
+  const int c1 = b < G ? min(C, c0 + gc) : c0 + 1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) out[e] = 0.f;
+  for (int c = c0; c < c1; ++c) {
+    const int j0 = c * cp, j1 = min(N, j0 + cp);
+    float part[8];
+    sum_rows(V, j0, j1, slot, oct, part);
+    const float inv = 1.f / (float)(j1 - j0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[e] = fmaf(part[e], inv, out[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s_red[slot][oct * 8 + e] = out[e];
+  __syncthreads();
+  if (tid < kCols) {
+    float x = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRepSlots; ++q) x += s_red[q][tid];
+    M[(long long)b * kCols + tid] = f32_to_bf16_rn(x / (float)(c1 - c0));
+  }
+}
+
+struct HierPoolArgs {
+  PoolSegments seg;
+  const uint32_t* mask;  // [R][ceil(N/32)]
+  int N, G, C, H, cp, gc;
+  int permille[3];
+  int K;
+  int* idx;   // [R][K] pool ids
+  float* top; // [R][K] or null
+  int* kept;  // [R] or null
+  int* err;
+};
+
+// Whether any bit in [lo, hi) of a mask row is set (lo < hi).
+__device__ __forceinline__ bool range_any(const uint32_t* row, int lo, int hi) {
+  const int w0 = lo >> 5, w1 = (hi - 1) >> 5;
+  for (int w = w0; w <= w1; ++w) {
+    uint32_t x = __ldg(row + w);
+    if (w == w0) x &= kFull << (lo & 31);
+    if (w == w1 && (hi & 31)) x &= (1u << (hi & 31)) - 1u;
+    if (x) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool bit(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
+
+// The smallest key T such that exactly k of the keys `visit` offers as
+// active are >= T (keys distinct, 1 <= k <= active count): a radix select on
+// 8-bit digits, most significant first, stopping as soon as a digit's bucket
+// holds exactly the keys still needed. visit(fn) calls fn(active, key) for
+// every candidate this thread owns.
+template <typename Visit>
+__device__ uint64_t radix_kth(Visit&& visit, int k, int* hist, int* s_pick) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t prefix = 0ull, pmask = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    visit([&](bool active, uint64_t key) {
+      if (active && (key & pmask) == prefix) atomicAdd(&hist[(int)((key >> shift) & 255)], 1);
+    });
+    __syncthreads();
+    if (warp == 0) {
+      int local = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) local += hist[lane * 8 + b];
+      int sfx = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, sfx, o);
+        if (lane + o < 32) sfx += y;
+      }
+      int above = sfx - local;
+      for (int b = 7; b >= 0; --b) {
+        const int hb = hist[lane * 8 + b];
+        if (above < need && above + hb >= need) {
+          s_pick[0] = lane * 8 + b;
+          s_pick[1] = above;
+        }
+        above += hb;
+      }
+    }
+    __syncthreads();
+    const int b = s_pick[0];
+    need -= s_pick[1];
+    prefix |= (uint64_t)b << shift;
+    pmask |= (uint64_t)0xFF << shift;
+    const bool exact = hist[b] == need;
+    __syncthreads();
+    if (exact) break;
+  }
+  return prefix;
+}
+
+__global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPoolArgs a) {
+  extern __shared__ __align__(16) uint64_t s_dyn[];
+  uint64_t* s_ck = s_dyn;                    // [kHierPoolCoarseMax] coarse keys by row
+  uint64_t* s_pk = s_dyn + kHierPoolCoarseMax;  // [kPageStage] active block keys
+  __shared__ uint32_t s_call[kHierPoolCoarseMax / 32];  // Chunks covering an allowed block
+  __shared__ uint32_t s_gall[kHierPoolCoarseMax / 32];  // Grids covering an allowed block
+  __shared__ uint32_t s_ckept[kHierPoolCoarseMax / 32];
+  __shared__ uint32_t s_gkept[kHierPoolCoarseMax / 32];
+  __shared__ int s_cnt[kPoolMaxSegs];
+  __shared__ int hist[256], s_pick[2], s_tmp[kWarps], s_np, s_nout;
+  __shared__ uint64_t s_out[kMaxK];
+  __shared__ uint64_t s_wl[kWarps][32];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G, C = a.C, N = a.N, segs = a.seg.segs;
+  const long long cap = a.seg.cap;
+  const int nco = G + C;
+  const int cwords = (C + 31) / 32, gwords = (G + 31) / 32;
+  for (int w = tid; w < cwords; w += kThreads) {
+    s_call[w] = 0u;
+    s_ckept[w] = 0u;
+  }
+  for (int w = tid; w < gwords; w += kThreads) {
+    s_gall[w] = 0u;
+    s_gkept[w] = 0u;
+  }
+  if (tid == 0) {
+    s_np = 0;
+    s_nout = 0;
+  }
+  // Chunks (then Grids) that cover an allowed block; the mask is an input,
+  // not a result of the GEMM, so this overlaps the GEMM's tail
+  const uint32_t* mrow = a.mask + (long long)r * ((N + 31) / 32);
+  __syncthreads();
+  for (int c = tid; c < C; c += kThreads)
+    if (range_any(mrow, c * a.cp, min(N, (c + 1) * a.cp))) atomicOr(&s_call[c >> 5], 1u << (c & 31));
+  __syncthreads();
+  for (int g = tid; g < G; g += kThreads) {
+    bool any = false;
+    for (int c = g * a.gc; c < min(C, (g + 1) * a.gc) && !any; ++c) any = bit(s_call, c);
+    if (any) atomicOr(&s_gall[g >> 5], 1u << (g & 31));
+  }
+
+  // the keys come from the GEMM grid launched just before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t* row = a.seg.cand + (long long)r * segs * cap;
+  for (int p = tid; p < segs; p += kThreads) {
+    int c = a.seg.counts[(long long)r * segs + p];
+    if (c < 0 || c > cap) {
+      flag_error(a.err, kErrBadIndex);
+      c = c < 0 ? 0 : (int)cap;
+    }
+    s_cnt[p] = c;
+  }
+  __syncthreads();
+  // Coarse row x lies in tile x / 128, which is GEMM CTA (tile % segs)'s
+  // local tile tile / segs; a CTA's coarse tiles are its first ones and all
+  // but the last coarse tile are full, so the key sits at a fixed place.
+  for (int x = tid; x < nco; x += kThreads) {
+    const int t = x / 128, p = t % segs;
+    const long long pos = (long long)(t / segs) * 128 + (x & 127);
+    uint64_t k = pos < s_cnt[p] ? row[p * cap + pos] : 0ull;
+    if (key_index(k) != (uint32_t)x) {
+      flag_error(a.err, kErrBadIndex);
+      k = 0ull;
+    }
+    s_ck[x] = k;
+  }
+  __syncthreads();
+
+  // ---- Grids, then Chunks: keep ceil(n * permille / 1000) of the n active
+  auto level = [&](int base, int n, auto&& active, uint32_t* kept_bits, int q) {
+    int na = 0;
+    for (int i = tid; i < n; i += kThreads) na += active(i) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) na += __shfl_xor_sync(kFull, na, o);
+    if (lane == 0) s_tmp[warp] = na;
+    __syncthreads();
+    na = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) na += s_tmp[w];
+    __syncthreads();
+    const int m = (int)(((long long)na * q + 999) / 1000);
+    if (m == 0) return;
+    const uint64_t T = radix_kth(
+        [&](auto&& fn) {
+          for (int i = tid; i < n; i += kThreads) fn(active(i), s_ck[base + i]);
+        },
+        m, hist, s_pick);
+    for (int i = tid; i < n; i += kThreads)
+      if (active(i) && s_ck[base + i] >= T) atomicOr(&kept_bits[i >> 5], 1u << (i & 31));
+    __syncthreads();
+  };
+  level(0, G, [&](int g) { return bit(s_gall, g); }, s_gkept, a.permille[0]);
+  level(G, C, [&](int c) { return bit(s_call, c) && bit(s_gkept, c / a.gc); }, s_ckept, a.permille[1]);
+
+  // ---- blocks: the allowed blocks of kept Chunks (their keys follow the
+  // coarse keys in each segment), listed in shared memory while they fit
+  auto coarse_in = [&](int p) {  // coarse keys at the head of segment p
+    int n = 0;
+    for (int t = p; t * 128 < nco; t += segs) n += min(128, nco - t * 128);
+    return n;
+  };
+  auto page_active = [&](uint64_t k) {
+    const long long i = (long long)key_index(k) - a.H;
+    return i >= 0 && i < N && bit(s_ckept, (int)(i / a.cp));
+  };
+  for (int p = warp; p < segs; p += kWarps) {
+    const int c = s_cnt[p];
+    for (int j0 = coarse_in(p); j0 < c; j0 += 32) {
+      const int j = j0 + lane;
+      const uint64_t k = j < c ? row[p * cap + j] : 0ull;
+      const bool act = j < c && page_active(k);
+      const unsigned bal = __ballot_sync(kFull, act);
+      int base = 0;
+      if (lane == 0 && bal) base = atomicAdd(&s_np, __popc(bal));
+      base = __shfl_sync(kFull, base, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (act && base < kPageStage) s_pk[base] = k;
+    }
+  }
+  __syncthreads();
+  const int np = s_np;
+  const bool staged = np <= kPageStage;
+  const int m_keep = (int)(((long long)np * a.permille[2] + 999) / 1000);
+  const int m = min(a.K, m_keep);
+  auto visit_pages = [&](auto&& fn) {
+    if (staged) {
+      for (int i = tid; i < np; i += kThreads) fn(true, s_pk[i]);
+    } else {
+      for (int p = warp; p < segs; p += kWarps) {
+        const int c = s_cnt[p];
+        for (int j = coarse_in(p) + lane; j < c; j += 32) {
+          const uint64_t k = row[p * cap + j];
+          fn(page_active(k), k);
+        }
+      }
+    }
+  };
+  if (m > 0) {
+    const uint64_t T = radix_kth(visit_pages, m, hist, s_pick);
+    visit_pages([&](bool act, uint64_t k) {
+      if (act && k >= T) {
+        const int q = atomicAdd(&s_nout, 1);
+        if (q < kMaxK) s_out[q] = k;
+      }
+    });
+    __syncthreads();
+  }
+  // ---- the m winners in order: warp-sorted lists of 32, then merge ranks
+  const int got = min(s_nout, kMaxK);
+  if (tid == 0 && got != m) flag_error(a.err, kErrBadIndex);  // the select lost or gained a key
+  uint64_t mine = tid < min(m, got) ? s_out[tid] : 0ull;
+  mine = warp_sort_desc(mine, lane);
+  s_wl[warp][lane] = mine;
+  __syncthreads();
+  int* io = a.idx + (long long)r * a.K;
+  float* to = a.top ? a.top + (long long)r * a.K : nullptr;
+  int rank = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) rank += count_greater_pow2(s_wl[w], 32, mine);
+  if (mine != 0ull && rank < a.K) {
+    io[rank] = (int)(key_index(mine) - (uint32_t)a.H);
+    if (to) to[rank] = key_score(mine);
+  }
+  for (int i = m + tid; i < a.K; i += kThreads) {
+    io[i] = -1;
+    if (to) to[i] = -__int_as_float(0x7f800000);
+  }
+  if (tid == 0 && a.kept) a.kept[r] = m_keep;
+}
+
+}  // namespace
+
+int hier_pool_coarse_rows(int N, int cp, int gc) {
+  if (N <= 0) return 0;
+  const int C = (N + cp - 1) / cp, G = (C + gc - 1) / gc;
+  return (G + C + 127) / 128 * 128;
+}
+
+cudaError_t launch_hier_pool_reps(uint16_t* M, int N, int cp, int gc, cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  const int C = (N + cp - 1) / cp, G = (C + gc - 1) / gc;
+  const int H = hier_pool_coarse_rows(N, cp, gc);
+  pool_reps_kernel<<<G + C + 1, kRepThreads, 0, s>>>(M, N, cp, gc, G, C, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32_t* mask, int R, int N,
+                                    int cp, int gc, const int* permille, int K, int* idx, float* top, int* kept,
+                                    void* ws, int* err, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const int C = N > 0 ? (N + cp - 1) / cp : 0, G = C > 0 ? (C + gc - 1) / gc : 0;
+  const int H = hier_pool_coarse_rows(N, cp, gc);
+  PoolSegments seg;
+  cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, ws, err, s, &seg);
+  if (e != cudaSuccess) return e;
+  constexpr int kDyn = (int)sizeof(uint64_t) * (kHierPoolCoarseMax + kPageStage);
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(hier_pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  HierPoolArgs ha{seg, mask, N, G, C, H, cp, gc, {permille[0], permille[1], permille[2]}, K, idx, top, kept, err};
+  // programmatic dependent launch: scheduled while the GEMM drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)R);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDyn;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, hier_pool_select_kernel, ha);
+}
+
+}  // namespace kk

@@ -82,6 +82,11 @@ def _load():
         "kk_score_pool_batched_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
         "kk_coarse_means": (ctypes.c_int, [P, I32, I32, BT, I32, P, P]),
+        "kk_hier_pool_coarse_rows": (I32, [I32, I32, I32]),
+        "kk_hier_pool_reps": (ctypes.c_int, [P, I32, I32, I32, I32, P]),
+        "kk_hier_select_pool_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+        "kk_hier_select_pool": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, P, P, P, P,
+                                               SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -100,7 +105,8 @@ EXPORTS = (
     "kk_score_topk", "kk_select_step", "kk_score_topk_stable", "kk_select_step_stable",
     "kk_compact_table", "kk_append_tokens", "kk_hier_reps", "kk_hier_select",
     "kk_score_pool_batched_workspace_bytes",
-    "kk_score_pool_batched", "kk_coarse_means",
+    "kk_score_pool_batched", "kk_coarse_means", "kk_hier_pool_coarse_rows", "kk_hier_pool_reps",
+    "kk_hier_select_pool_workspace_bytes", "kk_hier_select_pool",
 )
 
 
@@ -301,6 +307,37 @@ def kk_score_pool_batched(A, V, mask, K: int, idx, top_scores=None, workspace=No
         _ptr(mask, torch.int32, "mask"), A.shape[0], V.shape[0], A.shape[1], K, _ptr(idx, torch.int32, "idx"),
         _ptr(top_scores, torch.float32, "top_scores"), _ptr(workspace, name="workspace"), ws_bytes,
         _stream(stream)))
+
+
+def kk_hier_pool_coarse_rows(N: int, chunk_pages: int, grid_chunks: int) -> int:
+    return _lib.kk_hier_pool_coarse_rows(N, chunk_pages, grid_chunks)
+
+
+def _pool_matrix(M, N: int, chunk_pages: int, grid_chunks: int):
+    H = kk_hier_pool_coarse_rows(N, chunk_pages, grid_chunks)
+    if M is not None and H >= 0 and M.shape[0] != H + N:
+        raise ValueError(f"M has {M.shape[0]} rows, expected {H} coarse rows + {N} blocks")
+    return _ptr(M, (torch.int16, torch.bfloat16), "M")
+
+
+def kk_hier_pool_reps(M, N: int, chunk_pages: int, grid_chunks: int, stream=None):
+    _check("kk_hier_pool_reps", _lib.kk_hier_pool_reps(
+        _pool_matrix(M, N, chunk_pages, grid_chunks), N, M.shape[1], chunk_pages, grid_chunks, _stream(stream)))
+
+
+def kk_hier_select_pool_workspace_bytes(R: int, N: int, chunk_pages: int, grid_chunks: int) -> int:
+    return _lib.kk_hier_select_pool_workspace_bytes(R, N, chunk_pages, grid_chunks)
+
+
+def kk_hier_select_pool(A, M, mask, N: int, chunk_pages: int, grid_chunks: int, permille, idx, top_scores=None,
+                        kept=None, workspace=None, stream=None):
+    pg, pc, pp = (int(x) for x in permille)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kk_hier_select_pool", _lib.kk_hier_select_pool(
+        _ptr(A, (torch.int16, torch.bfloat16), "A"), _pool_matrix(M, N, chunk_pages, grid_chunks),
+        _ptr(mask, torch.int32, "mask"), A.shape[0], N, A.shape[1], chunk_pages, grid_chunks, pg, pc, pp,
+        idx.shape[1], _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"),
+        _ptr(kept, torch.int32, "kept"), _ptr(workspace, name="workspace"), ws_bytes, _stream(stream)))
 
 
 def kk_coarse_means(vb, bt: BlockTable, group: int, out, stream=None):

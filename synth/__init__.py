@@ -336,6 +336,41 @@ def shared_pool(N=POOL_N, R=POOL_R, D=POOL_D, owned=POOL_OWNED, K=POOL_K, seed=4
     return v, a, mask, K
 
 
+def owned_runs_mask(R: int, N: int, run: int, runs: int, seed: int) -> np.ndarray:
+    """uint32 [R][ceil(N/32)]: each row owns ``runs`` whole runs of ``run``
+    consecutive blocks (documents of a shared pool), drawn without replacement."""
+    rng = np.random.default_rng(seed)
+    n_runs = -(-N // run)
+    words = np.zeros((R, (N + 31) // 32), dtype=np.uint32)
+    for r in range(R):
+        for d in rng.choice(n_runs, size=min(runs, n_runs), replace=False):
+            j = np.arange(d * run, min(N, (d + 1) * run))
+            np.bitwise_or.at(words[r], j // 32, (np.uint32(1) << (j % 32).astype(np.uint32)))
+    return words
+
+
+def topic_runs(N: int, num_topics: int, run: int, seed: int) -> np.ndarray:
+    """int32 [N]: one random topic per run of ``run`` consecutive blocks."""
+    rng = np.random.default_rng(seed)
+    return np.repeat(rng.integers(0, num_topics, size=-(-N // run)), run)[:N].astype(np.int32)
+
+
+HIER_POOL_DOC = 512  # blocks per document: one Grid of 8 Chunks of 64 blocks
+
+
+def shared_pool_hier(N=POOL_N, R=POOL_R, D=POOL_D, docs=POOL_OWNED // HIER_POOL_DOC, K=POOL_K, seed=6):
+    """Shared pool for the three-level selection: the sizes and noise of
+    shared_pool, but the pool is a run of documents of HIER_POOL_DOC blocks
+    whose topics change every 32 blocks, and each anchor owns ``docs`` whole
+    documents (4096 blocks by default). Returns (V_spec, A_spec, mask_words, K)."""
+    v = RowsSpec(N=N, D=D, num_topics=32, scale=1.5, sigma=float(np.float32(1.0 / np.sqrt(128 * 28 * 4))),
+                 seed=seed, stream=2, dtype="bf16", topics=topic_runs(N, 32, 32, seed * 13 + 1))
+    a = RowsSpec(N=R, D=D, num_topics=32, scale=1.5, sigma=float(np.float32(1.0 / np.sqrt(16 * 28 * 4))),
+                 seed=seed, stream=3, dtype="bf16", centroid_seed=seed)
+    mask = owned_runs_mask(R, N, HIER_POOL_DOC, docs, seed * 31 + 7)
+    return v, a, mask, K
+
+
 # --------------------------------------------------------------------------
 # CUDA generator (large caches): synth/libkksynth.so
 # --------------------------------------------------------------------------

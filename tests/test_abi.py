@@ -151,3 +151,27 @@ def test_hier_host_errors(kk):
     big = kk.kk_block_table(4096, 4096, None, 1, 1 << 22)
     assert lib.kk_hier_select(16, 128, 8, B(big), 16, 16, 16, 64, 8, 1000, 1000, 1000, 4, 16, None, None, None) == \
         kk.KK_ERR_UNSUPPORTED
+
+
+def test_hier_pool_host_errors(kk):
+    """The shared-pool hierarchy: coarse row counts, and bad shares, sizes and dims rejected on the host."""
+    lib = kk._lib
+    assert lib.kk_hier_pool_coarse_rows(65536, 64, 8) == 1152  # 128 Grids + 1024 Chunks
+    assert lib.kk_hier_pool_coarse_rows(300, 8, 3) == 128      # 13 + 38, padded to a tile
+    assert lib.kk_hier_pool_coarse_rows(0, 64, 8) == 0
+    assert lib.kk_hier_pool_coarse_rows(1 << 20, 16, 8) == -1  # 65536 Chunks: too many
+    assert lib.kk_hier_pool_coarse_rows(10, 0, 8) == -1
+    assert lib.kk_hier_select_pool_workspace_bytes(4, 1 << 20, 16, 8) == 0
+    ok = (16, 16, 16)
+    args = lambda R, N, D, cp, gc, pm, K: (*ok, R, N, D, cp, gc, *pm, K, 16, None, None, 16, 1 << 30, None)
+    assert lib.kk_hier_select_pool(*args(4, 1000, 128, 64, 8, (0, 200, 100), 16)) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_select_pool(*args(4, 1000, 128, 64, 8, (500, 200, 1001), 16)) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_select_pool(*args(4, 1000, 128, 64, 8, (500, 200, 100), 0)) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_select_pool(*args(4, 1000, 128, 64, 8, (500, 200, 100), 257)) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_select_pool(*args(4, 1000, 128, 0, 8, (500, 200, 100), 16)) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_select_pool(*args(4, 1000, 96, 64, 8, (500, 200, 100), 16)) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_hier_select_pool(*args(4, 1 << 20, 128, 16, 8, (500, 200, 100), 16)) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_hier_select_pool(*args(0, 1000, 128, 64, 8, (500, 200, 100), 16)) == kk.KK_OK
+    assert lib.kk_hier_pool_reps(16, 1000, 64, 64, 8, None) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_hier_pool_reps(16, 1000, 128, 0, 8, None) == kk.KK_ERR_INVALID
+    assert lib.kk_hier_pool_reps(None, 0, 128, 64, 8, None) == kk.KK_OK

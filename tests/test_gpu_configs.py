@@ -2,6 +2,7 @@
 The oracle checks sampled outputs it can compute one by one (sampled blocks,
 sampled requests, sampled coarse groups); properties that hold at any size
 (planted-topic ranking, reblocking) cover the rest."""
+import dataclasses
 import gc
 
 import numpy as np
@@ -184,3 +185,39 @@ def test_shared_pool_full(kk):
         same = set(owned[v_spec.topics[owned] == a_spec.topics[r]].tolist())
         m = min(K, len(same))
         assert set(idx_h[r][:m].tolist()) <= same, f"row {r}"
+
+
+def test_shared_pool_hier_full(kk):
+    """The shared pool as documents, three levels in one product (256 anchors x
+    65536 blocks, Chunks of 64, Grids of 8 Chunks, 50 / 20 / 10 %), as bench.py
+    calls it: every coarse row against the oracle's means, sampled anchors
+    against the oracle's selection."""
+    from tests.test_gpu_hier_pool import check_against_oracle
+
+    v_spec, a_spec, mask, K = synth.shared_pool_hier()
+    R, N, cp, gc_, pm = a_spec.N, v_spec.N, 64, 8, (500, 200, 100)
+    H = kk.kk_hier_pool_coarse_rows(N, cp, gc_)
+    M = torch.zeros((H + N, 128), dtype=torch.int16, device="cuda")
+    M[H:] = synth.gen_rows_cuda(v_spec)
+    A = synth.gen_rows_cuda(a_spec)
+    kk.kk_hier_pool_reps(M, N, cp, gc_)
+    mt = torch.from_numpy(mask.view(np.int32)).cuda()
+    ws = torch.empty(kk.kk_hier_select_pool_workspace_bytes(R, N, cp, gc_), dtype=torch.uint8, device="cuda")
+    idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    top = torch.zeros((R, K), device="cuda")
+    kept = torch.zeros(R, dtype=torch.int32, device="cuda")
+    kk.kk_hier_select_pool(A, M, mt, N, cp, gc_, pm, idx, top, kept, ws)
+    assert kk.kk_device_error() == 0
+    M_h = M.cpu().numpy().view(np.uint16)
+    A_h = A.cpu().numpy().view(np.uint16)
+    V_h = M_h[H:]
+    head = dataclasses.replace(v_spec, N=4096, topics=v_spec.topics[:4096])
+    np.testing.assert_array_equal(V_h[:4096], synth.gen_rows_numpy(head))  # generator bits, GPU == numpy
+    chunks, grids = ko.hier_reps(ko.decode(V_h), cp, gc_)
+    G, C = len(grids), len(chunks)
+    for rows, ref in ((M_h[:G], grids), (M_h[G:G + C], chunks)):
+        np.testing.assert_array_less(np.abs(ko.decode(rows) - ref), 2.0**-7 * np.abs(ref) + 1e-6)
+    rows = np.random.default_rng(5).choice(R, size=8, replace=False)
+    check_against_oracle(A_h, M_h, G, C, H, mask, N, cp, gc_, pm, K, idx.cpu().numpy(), top.cpu().numpy(),
+                         kept.cpu().numpy(), rows=rows.tolist(), min_clear=0.5)
+    _free()
