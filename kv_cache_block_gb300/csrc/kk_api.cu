@@ -458,7 +458,7 @@ kk_status kk_hier_pool_reps(uint16_t* M, int32_t N, int32_t D, int32_t chunk_pag
 
 size_t kk_hier_select_pool_workspace_bytes(int32_t R, int32_t N, int32_t chunk_pages, int32_t grid_chunks) {
   if (R < 0 || !hier_pool_dims(N, chunk_pages, grid_chunks)) return 0;
-  return kk::batched_workspace_bytes(R, kk::hier_pool_coarse_rows(N, chunk_pages, grid_chunks) + N);
+  return kk::hier_pool_workspace_bytes(R, N, chunk_pages, grid_chunks);
 }
 
 kk_status kk_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32_t* mask, int32_t R, int32_t N,

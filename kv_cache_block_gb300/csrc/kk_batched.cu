@@ -31,7 +31,7 @@ constexpr int kD = 128;   // head_dim (two 64-element swizzle boxes)
 constexpr int kBoxBytes = 128 * 128;   // 128 rows x 128 bytes
 constexpr int kTileBytes = 2 * kBoxBytes;
 constexpr int kStages = 3;             // V tiles in flight
-constexpr int kGroups = 4;             // epilogue groups, each drains whole tiles
+constexpr int kGroups = kPoolGroups;   // epilogue groups, each drains whole tiles
 constexpr int kAccs = kGroups;         // TMEM accumulators (128 columns each), one per group
 constexpr int kGroupThreads = 128;     // four warps: one per TMEM lane quarter
 constexpr int kEpiThreads = kGroups * kGroupThreads;
@@ -47,9 +47,10 @@ struct GemmArgs {
   int R, N, mask_words, tiles;
   int coarse_rows;  // rows before the pool's blocks that every anchor scores (0: none)
   int coarse_tiles; // tiles holding them (their rows come first, 128 per tile)
-  int* counts;      // [R][P] owned candidates of each anchor in each CTA's tiles
-  uint64_t* cand;   // [R][P][cap] candidate keys, one segment per (anchor, CTA)
-  long long cap;    // 128 x the most tiles a CTA takes
+  float* coarse;    // [R][coarse_tiles * 128] their scores, dense
+  int* counts;      // [R][P][kGroups] candidates of each anchor in each epilogue group's tiles
+  uint64_t* cand;   // [R][P][kGroups][cap] candidate keys, one segment per (anchor, CTA, group)
+  long long cap;    // 128 x the most tiles an epilogue group takes
   int mask_vec;     // mask rows allow 16-byte loads of a tile's four words
   int* err;
 };
@@ -98,6 +99,7 @@ __device__ __forceinline__ float row_sq(const unsigned char* tile, int row) {
 // 64-bit key (score, pool id) into the anchor's segment for this CTA, in tile
 // order; the last group writes the segment's length. No atomics: every slot
 // has one writer.
+template <bool kCoarse>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     score_pool_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmV,
                       GemmArgs g) {
@@ -114,7 +116,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + kStages;       // [kStages] V tile released (MMA + the tile's group)
   uint64_t* acc_full = empty + kStages;   // [kAccs] accumulator ready
   uint64_t* acc_empty = acc_full + kAccs; // [kAccs] accumulator drained (the tile's group)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + kAccs);
+  uint64_t* epi_done = acc_empty + kAccs; // every epilogue warp has left its loop
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done + 1);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
   // the select kernel may be scheduled now; it waits for this grid's results
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kGroupThreads / 32);
     }
+    mbar_init(epi_done, kEpiThreads / 32);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -224,17 +228,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lo = range_lo(grp), len = range_len(grp);
     auto inv_norm = [](float sq) { return sq > 0.f ? 1.f / sqrtf(sq) : 0.f; };
     // ownership bits of this anchor's 128 columns of the CTA's local tile jj
-    // (limited to columns < N): one 16-byte load when the rows allow it. The
-    // tiles of coarse rows come first and take every row below coarse_rows.
+    // (one 16-byte load when the rows allow it), loaded a tile ahead and
+    // limited to columns < N only when the tile is drained, so that the load
+    // is not waited for early. Coarse tiles (first) have no mask.
     const uint32_t* mrow = g.mask + (long long)(r < g.R ? r : 0) * g.mask_words;
-    auto mask_words = [&](int jj, uint32_t (&w)[4]) {
+    auto mask_load = [&](int jj, uint32_t (&w)[4]) {
       const int tile = p + jj * P;
-      if (tile < g.coarse_tiles) {
+      if (kCoarse && tile < g.coarse_tiles) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int lim = g.coarse_rows - (tile * (kBN / 32) + c) * 32;
-          w[c] = (jj >= ntiles || r >= g.R || lim <= 0) ? 0u : (lim >= 32 ? kFull : (1u << lim) - 1u);
-        }
+        for (int c = 0; c < 4; ++c) w[c] = 0u;
         return;
       }
       const int wi0 = (tile - g.coarse_tiles) * (kBN / 32);
@@ -249,27 +251,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = 0; c < 4; ++c)
           w[c] = (jj < ntiles && r < g.R && wi0 + c < g.mask_words) ? mrow[wi0 + c] : 0u;
       }
+    };
+    auto mask_finish = [&](int jj, uint32_t (&w)[4]) {
+      const int wi0 = (p + jj * P - g.coarse_tiles) * (kBN / 32);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int lim = g.N - (wi0 + c) * 32;
         if (lim < 32) w[c] &= lim <= 0 ? 0u : ((1u << lim) - 1u);
       }
     };
-    auto owned = [](const uint32_t (&w)[4]) { return __popc(w[0]) + __popc(w[1]) + __popc(w[2]) + __popc(w[3]); };
-    // The anchor's keys from this CTA's tiles fill one segment in local tile
-    // order: this group's keys start after the owned columns of the tiles of
-    // the groups before it.
-    uint64_t* seg = g.cand + ((long long)r * P + p) * g.cap;
+    // The anchor's keys from this group's tiles fill the group's own segment
+    // in tile order.
+    uint64_t* seg = g.cand + (((long long)(r < g.R ? r : 0) * P + p) * kGroups + grp) * g.cap;
     int pre = 0;
-    for (int j0 = 0; j0 < lo; j0 += 4) {
-      uint32_t wb[4][4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) mask_words(j0 + x < lo ? j0 + x : ntiles, wb[x]);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) pre += owned(wb[x]);
-    }
+    const uint32_t dump0 = dump - (uint32_t)(lane * kDumpStride * 4);  // lane 0's dump row in this warp
     uint32_t w_next[4];
-    mask_words(len > 0 ? lo : ntiles, w_next);
+    mask_load(len > 0 ? lo : ntiles, w_next);
     bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
     if (!ok) fail(kErrTimeout);
     const float inv_a = ok ? inv_norm(row_sq(sA, row)) : 0.f;
@@ -285,7 +282,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t w[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) w[c] = w_next[c];
-      mask_words(i + 1 < len ? j + 1 : ntiles, w_next);
+      mask_load(i + 1 < len ? j + 1 : ntiles, w_next);
       // V-row norms of this tile (one row per thread), then release the
       // ring stage. The group leaves the loop together (a lone warp leaving
       // would strand the others at the named barrier).
@@ -300,6 +297,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
+      const bool coarse = kCoarse && tile < g.coarse_tiles;
+      if (!coarse) mask_finish(j, w);
       const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(grp * kBN);
       uint64_t* out = seg + pre;
       int k = 0;
@@ -313,48 +312,117 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[grp]);  // the accumulator may be reused
         }
-        uint32_t x = w[c];
-        if (x == 0u) continue;
-        // owned columns are sparse: dump the chunk to this thread's row of
-        // shared memory and visit only the set bits, the first four as
-        // independent slots (their loads and math overlap), then the rare
-        // remainder one by one
+        if (coarse) {
+          // every anchor scores every coarse row: the scores go out dense,
+          // 128 bytes a thread per chunk
+          if (r < g.R) {
+            float* dst = g.coarse + (long long)r * g.coarse_tiles * kBN + n0 + c * 32;
+            const float4* iv4 = reinterpret_cast<const float4*>(inv_v + c * 32);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) sts128(dump + e * 4, acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        int ib[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ib[u] = x ? __ffs(x) - 1 : -1;
-          x &= x - 1;
-        }
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = ib[u] >= 0 ? lds_f32(dump + ib[u] * 4) * inv_v[c * 32 + ib[u]] : 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (ib[u] >= 0) {
-            const float cosv = fminf(1.f, fmaxf(-1.f, v[u] * inv_a));
-            out[k + u] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + ib[u]));
+            for (int e = 0; e < 32; e += 4) {
+              const float4 iv = iv4[e / 4];
+              float4 sc;
+              sc.x = fmaf(0.5f, fminf(1.f, fmaxf(-1.f, __uint_as_float(acc[e]) * iv.x * inv_a)), 0.5f);
+              sc.y = fmaf(0.5f, fminf(1.f, fmaxf(-1.f, __uint_as_float(acc[e + 1]) * iv.y * inv_a)), 0.5f);
+              sc.z = fmaf(0.5f, fminf(1.f, fmaxf(-1.f, __uint_as_float(acc[e + 2]) * iv.z * inv_a)), 0.5f);
+              sc.w = fmaf(0.5f, fminf(1.f, fmaxf(-1.f, __uint_as_float(acc[e + 3]) * iv.w * inv_a)), 0.5f);
+              *reinterpret_cast<float4*>(dst + e) = sc;
+            }
           }
+          continue;
         }
-        k += (ib[0] >= 0) + (ib[1] >= 0) + (ib[2] >= 0) + (ib[3] >= 0);
+        uint32_t x = w[c];
+        const unsigned rows = __ballot_sync(kFull, x != 0u);
+        if (rows == 0u) continue;
+        // the chunk goes to this thread's row of shared memory, then either
+        // each thread writes its own row's keys (few per row), or, when the
+        // warp has fewer owning rows than its busiest row has keys, the lanes
+        // write one row at a time, lane e taking column e (coalesced)
+        if (x != 0u) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) sts128(dump + e * 4, acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        }
+        if (__popc(rows) <= __reduce_max_sync(kFull, (unsigned)__popc(x))) {
+          __syncwarp();
+          const float iv = inv_v[c * 32 + lane];
+          const unsigned long long my_out = reinterpret_cast<unsigned long long>(out + k);
+          const uint32_t below = (1u << lane) - 1u;
+          // four rows at a time, so their loads and math overlap
+          for (unsigned rr = rows; rr != 0u;) {
+            int qs[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              qs[u] = rr != 0u ? __ffs(rr) - 1 : -1;
+              rr &= rr - 1u;
+            }
+            uint32_t xq[4];
+            float aq[4], vq[4];
+            unsigned long long oq[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = qs[u] < 0 ? 0 : qs[u];
+              xq[u] = qs[u] < 0 ? 0u : __shfl_sync(kFull, x, q);
+              aq[u] = __shfl_sync(kFull, inv_a, q);
+              oq[u] = __shfl_sync(kFull, my_out, q);
+              vq[u] = ((xq[u] >> lane) & 1u) ? lds_f32(dump0 + (uint32_t)(q * kDumpStride * 4 + lane * 4)) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if ((xq[u] >> lane) & 1u) {
+                const float cosv = fminf(1.f, fmaxf(-1.f, vq[u] * iv * aq[u]));
+                reinterpret_cast<uint64_t*>(oq[u])[__popc(xq[u] & below)] =
+                    make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + lane));
+              }
+            }
+          }
+          k += __popc(x);
+          __syncwarp();  // the dump rows are rewritten by the next chunk
+          continue;
+        }
+        // this row's owned columns, four at a time (their loads and math
+        // overlap)
         while (x) {
-          const int e = __ffs(x) - 1;
-          x &= x - 1;
-          const float cosv = fminf(1.f, fmaxf(-1.f, lds_f32(dump + e * 4) * inv_v[c * 32 + e] * inv_a));
-          out[k++] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + e));
+          int ib[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            ib[u] = x ? __ffs(x) - 1 : -1;
+            x &= x - 1;
+          }
+          float v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] = ib[u] >= 0 ? lds_f32(dump + ib[u] * 4) * inv_v[c * 32 + ib[u]] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (ib[u] >= 0) {
+              const float cosv = fminf(1.f, fmaxf(-1.f, v[u] * inv_a));
+              out[k + u] = make_key(fmaf(0.5f, cosv, 0.5f), (uint32_t)(n0 + c * 32 + ib[u]));
+            }
+          }
+          k += (ib[0] >= 0) + (ib[1] >= 0) + (ib[2] >= 0) + (ib[3] >= 0);
         }
       }
-      pre += owned(w);
+      pre += k;
     }
-    // the last group's range ends at the CTA's last tile: its end is the total
-    if (grp == kGroups - 1 && r < g.R) g.counts[(long long)r * P + p] = pre;
+    // every group writes its count, also when it had no tile, and fills its
+    // segment's last 32-byte sector (the select reads whole sectors; one
+    // left partly written would be completed from DRAM)
+    if (r < g.R) {
+      g.counts[((long long)r * P + p) * kGroups + grp] = pre;
+      for (int i = pre; i & 3; ++i) seg[i] = 0ull;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(epi_done);  // this warp reads TMEM no more
   }
 
-  // teardown: every role has left its loop; no MMA or TMEM read is pending
+  // teardown: the TMEM is freed only after every epilogue warp has said (on
+  // an mbarrier) that it reads no more; warps 0 and 1 reconverge first, as
+  // lane 0 ran the producer / MMA loop alone
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    if (!mbar_wait_bounded(epi_done, 0, kWaitLimitNs)) flag_error(g.err, kErrTimeout);
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -362,8 +430,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---- per-anchor top-K ----------------------------------------------------
 constexpr int kSelThreads = 256;
-constexpr int kSelStage = 6144;                    // keys of a row held in shared memory (48 KB)
-constexpr int kRegKeys = kSelStage / kSelThreads;  // and then in registers, 24 per thread
+constexpr int kSelStage = 6144;                    // keys of a row held in registers,
+constexpr int kRegKeys = kSelStage / kSelThreads;  // 24 per thread
 constexpr int kMaxSegs = kPoolMaxSegs;             // segments (GEMM CTAs per M-tile) of a row
 constexpr int kBuckets = 2048;                     // linear buckets over a row's score range
 constexpr int kTieCap = 512;                       // boundary-bucket keys ranked exactly
@@ -403,10 +471,10 @@ __device__ __forceinline__ void for_each_segment_key(const SelArgs& a, const int
 // longer than the shared-memory copy take the same passes over the segments,
 // with a radix select on the 64-bit keys when a bucket holds too many ties.
 __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs a) {
-  extern __shared__ __align__(16) uint64_t s_keys[];  // [kSelStage]
   __shared__ int hist[kBuckets];
   __shared__ int s_cnt[kMaxSegs];
   __shared__ int s_off[kMaxSegs];
+  __shared__ int s_chunk_seg[kSelStage / 32];  // segment holding position 32 * c
   __shared__ int s_bin, s_above;
   __shared__ int s_sel_n, s_tie_n;
   __shared__ int s_wsum[kSelThreads / 32];
@@ -460,39 +528,35 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
     base += s_cnt[p];
   }
   const bool staged = n <= kSelStage;
+  if (staged)
+    for (int p = s_begin; p < s_end; ++p)
+      for (int c = (s_off[p] + 31) / 32; c * 32 < s_off[p] + s_cnt[p]; ++c) s_chunk_seg[c] = p;
   __syncthreads();
 
-  // ---- the compact copy: warp w takes segments w, w + 8, ...; two segments
-  // and 64 keys of each per round of loads (a segment holds about N / segs
-  // owned candidates, here ~54)
-  if (staged) {
-    for (int p0 = warp; p0 < a.segs; p0 += 2 * (kSelThreads / 32)) {
-      const int p1 = p0 + kSelThreads / 32;
-      const int c0 = s_cnt[p0], c1 = p1 < a.segs ? s_cnt[p1] : 0;
-      const uint64_t* g0 = row + p0 * a.cap;
-      const uint64_t* g1 = row + p1 * a.cap;
-      const uint64_t v0 = lane < c0 ? g0[lane] : 0ull, v1 = lane + 32 < c0 ? g0[lane + 32] : 0ull;
-      const uint64_t v2 = lane < c1 ? g1[lane] : 0ull, v3 = lane + 32 < c1 ? g1[lane + 32] : 0ull;
-      const int o0 = s_off[p0], o1 = p1 < a.segs ? s_off[p1] : 0;
-      if (lane < c0) s_keys[o0 + lane] = v0;
-      if (lane + 32 < c0) s_keys[o0 + lane + 32] = v1;
-      if (lane < c1) s_keys[o1 + lane] = v2;
-      if (lane + 32 < c1) s_keys[o1 + lane + 32] = v3;
-      for (int j = 64 + lane; j < c0; j += 32) s_keys[o0 + j] = g0[j];
-      for (int j = 64 + lane; j < c1; j += 32) s_keys[o1 + j] = g1[j];
-    }
-    __syncthreads();
-  }
-
-  // ---- this thread's keys (staged rows) and the row's key range
+  // ---- this thread's keys (rows of at most 24 keys a thread): warp w
+  // takes the 32-key chunks [w*W, (w+1)*W) of the row's compact order, lane
+  // l the l-th key of each (coalesced loads), straight from the segments
+  // into registers; a chunk's first segment comes from s_chunk_seg, so the
+  // rounds do not depend on one another
   uint64_t key[kRegKeys];
+  uint32_t vmask = 0u;  // bit u: key[u] holds a candidate
   uint64_t lo = ~0ull, hi = 0ull;
   if (staged) {
+    const int W = (n + kSelThreads - 1) / kSelThreads;  // chunks per warp, <= kRegKeys
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) {
-      const int i = tid + u * kSelThreads;
-      key[u] = i < n ? s_keys[i] : 0ull;
-      if (i < n) {
+      const int c = warp * W + u, pos = c * 32 + lane;
+      key[u] = 0ull;
+      if (u < W && pos < n) {
+        int sg = s_chunk_seg[c];
+        while (pos >= s_off[sg] + s_cnt[sg]) ++sg;
+        key[u] = row[sg * a.cap + (pos - s_off[sg])];
+        vmask |= 1u << u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) {
+      if ((vmask >> u) & 1u) {
         lo = key[u] < lo ? key[u] : lo;
         hi = key[u] > hi ? key[u] : hi;
       }
@@ -530,7 +594,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
   auto visit = [&](auto&& fn) {
     if (staged) {
 #pragma unroll
-      for (int u = 0; u < kRegKeys; ++u) fn(tid + u * kSelThreads < n, key[u]);
+      for (int u = 0; u < kRegKeys; ++u) fn(((vmask >> u) & 1u) != 0u, key[u]);
     } else {
       for_each_segment_key(a, s_cnt, row, fn);
     }
@@ -584,7 +648,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
       uint32_t m_above = 0, m_tie = 0;
 #pragma unroll
       for (int u = 0; u < kRegKeys; ++u) {
-        const int b = tid + u * kSelThreads < n ? bucket(key[u]) : -1;
+        const int b = ((vmask >> u) & 1u) ? bucket(key[u]) : -1;
         m_above |= (b > bstar ? 1u : 0u) << u;
         m_tie |= (b == bstar ? 1u : 0u) << u;
       }
@@ -757,10 +821,9 @@ cudaError_t setup_gemm() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!ready[dev]) {
-    e = cudaFuncSetAttribute(score_pool_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    e = cudaFuncSetAttribute(score_pool_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(uint64_t) * kSelStage));
+    e = cudaFuncSetAttribute(score_pool_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e != cudaSuccess) return e;
     ready[dev] = true;
   }
@@ -769,7 +832,8 @@ cudaError_t setup_gemm() {
 
 // Work split of the shared-pool scorer: MT M-tiles of 128 anchors, P CTAs
 // per M-tile (one CTA per SM in all), CTA p of an M-tile taking tiles p,
-// p + P, ...; each (anchor, CTA) segment holds up to `cap` keys.
+// p + P, ... (split into kGroups contiguous ranges); each (anchor, CTA,
+// group) segment holds up to `cap` keys.
 struct PoolLayout {
   int tiles, MT, P;
   long long cap;
@@ -780,10 +844,11 @@ PoolLayout pool_layout(int R, int N) {
   PoolLayout L;
   L.tiles = (N + kBN - 1) / kBN;
   L.MT = (R + kBM - 1) / kBM;
-  L.P = L.tiles == 0 ? 0 : std::max(1, std::min(std::min(L.tiles, kMaxSegs), sm_count() / std::max(1, L.MT)));
-  L.cap = L.P == 0 ? 0 : (long long)((L.tiles + L.P - 1) / L.P) * kBN;
-  L.counts_bytes = (sizeof(int) * (size_t)R * (size_t)L.P + 255) & ~size_t(255);
-  L.bytes = L.counts_bytes + sizeof(uint64_t) * (size_t)R * (size_t)L.P * (size_t)L.cap;
+  L.P = L.tiles == 0 ? 0
+                     : std::max(1, std::min(std::min(L.tiles, kMaxSegs / kGroups), sm_count() / std::max(1, L.MT)));
+  L.cap = L.P == 0 ? 0 : (long long)(((L.tiles + L.P - 1) / L.P + kGroups - 1) / kGroups) * kBN;
+  L.counts_bytes = (sizeof(int) * (size_t)R * (size_t)L.P * kGroups + 255) & ~size_t(255);
+  L.bytes = L.counts_bytes + sizeof(uint64_t) * (size_t)R * (size_t)L.P * kGroups * (size_t)L.cap;
   return L;
 }
 
@@ -792,11 +857,11 @@ PoolLayout pool_layout(int R, int N) {
 size_t batched_workspace_bytes(int R, int N) { return pool_layout(R, N).bytes; }
 
 cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, const uint32_t* mask, int R, int N,
-                             int coarse_rows, void* ws, int* err, cudaStream_t s, PoolSegments* out) {
+                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolSegments* out) {
   const PoolLayout L = pool_layout(R, rows);
   int* counts = static_cast<int*>(ws);
   uint64_t* cand = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + L.counts_bytes);
-  *out = PoolSegments{cand, counts, L.P, L.cap};
+  *out = PoolSegments{cand, counts, L.P * kGroups, L.cap, L.P, L.tiles};
   if (R == 0) return cudaSuccess;
   cudaError_t e = setup_gemm();
   if (e != cudaSuccess) return e;
@@ -805,8 +870,11 @@ cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, con
     if (!make_map(&ma, A, R) || !make_map(&mv, V, rows)) return cudaErrorInvalidValue;
     const int mask_words = (N + 31) / 32;
     const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
-    GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, counts, cand, L.cap, mask_vec, err};
-    score_pool_kernel<<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
+    GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, coarse, counts, cand, L.cap, mask_vec, err};
+    if (g.coarse_tiles > 0)
+      score_pool_kernel<true><<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
+    else
+      score_pool_kernel<false><<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -817,14 +885,14 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
                                       cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   PoolSegments seg;
-  cudaError_t e = launch_pool_gemm(A, V, N, mask, R, N, 0, ws, err, s, &seg);
+  cudaError_t e = launch_pool_gemm(A, V, N, mask, R, N, 0, nullptr, ws, err, s, &seg);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the select grid is scheduled while the
   // GEMM drains and waits (griddepcontrol.wait) for its results
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)R);
   cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = sizeof(uint64_t) * kSelStage;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

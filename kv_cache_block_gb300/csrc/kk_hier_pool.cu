@@ -32,6 +32,7 @@ constexpr int kRepSlots = kRepThreads / (kCols / 8);
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPageStage = 8192;  // active blocks of an anchor listed in shared memory
+constexpr int kChunkMap = 1024;   // 32-key chunks of a row mapped to their first segment
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   uint16_t h;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kRepThreads) pool_reps_kernel(uint16_t* M, int
 
 struct HierPoolArgs {
   PoolSegments seg;
+  const float* coarse;   // [R][H] scores of the coarse rows
   const uint32_t* mask;  // [R][ceil(N/32)]
   int N, G, C, H, cp, gc;
   int permille[3];
@@ -185,6 +187,8 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
   __shared__ uint32_t s_ckept[kHierPoolCoarseMax / 32];
   __shared__ uint32_t s_gkept[kHierPoolCoarseMax / 32];
   __shared__ int s_cnt[kPoolMaxSegs];
+  __shared__ int s_off[kPoolMaxSegs];
+  __shared__ int s_chunk_seg[kChunkMap];  // segment holding position 32 * c
   __shared__ int hist[256], s_pick[2], s_tmp[kWarps], s_np, s_nout;
   __shared__ uint64_t s_out[kMaxK];
   __shared__ uint64_t s_wl[kWarps][32];
@@ -221,28 +225,46 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
   // the keys come from the GEMM grid launched just before this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t* row = a.seg.cand + (long long)r * segs * cap;
-  for (int p = tid; p < segs; p += kThreads) {
-    int c = a.seg.counts[(long long)r * segs + p];
-    if (c < 0 || c > cap) {
-      flag_error(a.err, kErrBadIndex);
-      c = c < 0 ? 0 : (int)cap;
+  // segment counts and their offsets in the row's compact order: each thread
+  // scans a run of up to four segments, then the block
+  int ntot = 0;
+  {
+    const int spt = (segs + kThreads - 1) / kThreads;  // <= 4
+    const int s0 = min(segs, tid * spt), s1 = min(segs, s0 + spt);
+    int mine = 0;
+    for (int p = s0; p < s1; ++p) {
+      int c = a.seg.counts[(long long)r * segs + p];
+      if (c < 0 || c > cap) {
+        flag_error(a.err, kErrBadIndex);
+        c = c < 0 ? 0 : (int)cap;
+      }
+      s_cnt[p] = c;
+      mine += c;
     }
-    s_cnt[p] = c;
-  }
-  __syncthreads();
-  // Coarse row x lies in tile x / 128, which is GEMM CTA (tile % segs)'s
-  // local tile tile / segs; a CTA's coarse tiles are its first ones and all
-  // but the last coarse tile are full, so the key sits at a fixed place.
-  for (int x = tid; x < nco; x += kThreads) {
-    const int t = x / 128, p = t % segs;
-    const long long pos = (long long)(t / segs) * 128 + (x & 127);
-    uint64_t k = pos < s_cnt[p] ? row[p * cap + pos] : 0ull;
-    if (key_index(k) != (uint32_t)x) {
-      flag_error(a.err, kErrBadIndex);
-      k = 0ull;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
     }
-    s_ck[x] = k;
+    if (lane == 31) s_tmp[warp] = incl;
+    __syncthreads();
+    int base = incl - mine;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) base += s_tmp[w];
+      ntot += s_tmp[w];
+    }
+    for (int p = s0; p < s1; ++p) {
+      s_off[p] = base;
+      if (ntot <= kChunkMap * 32)
+        for (int c = (base + 31) / 32; c * 32 < base + s_cnt[p]; ++c) s_chunk_seg[c] = p;
+      base += s_cnt[p];
+    }
+    __syncthreads();
   }
+  // the coarse rows' scores, as keys (score, row)
+  for (int x = tid; x < nco; x += kThreads) s_ck[x] = make_key(a.coarse[(long long)r * a.H + x], (uint32_t)x);
   __syncthreads();
 
   // ---- Grids, then Chunks: keep ceil(n * permille / 1000) of the n active
@@ -271,30 +293,54 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
   level(0, G, [&](int g) { return bit(s_gall, g); }, s_gkept, a.permille[0]);
   level(G, C, [&](int c) { return bit(s_call, c) && bit(s_gkept, c / a.gc); }, s_ckept, a.permille[1]);
 
-  // ---- blocks: the allowed blocks of kept Chunks (their keys follow the
-  // coarse keys in each segment), listed in shared memory while they fit
-  auto coarse_in = [&](int p) {  // coarse keys at the head of segment p
-    int n = 0;
-    for (int t = p; t * 128 < nco; t += segs) n += min(128, nco - t * 128);
-    return n;
-  };
+  // ---- blocks: the allowed blocks of kept Chunks (the segments hold only
+  // blocks' keys), listed in shared memory while they fit
   auto page_active = [&](uint64_t k) {
     const long long i = (long long)key_index(k) - a.H;
     return i >= 0 && i < N && bit(s_ckept, (int)(i / a.cp));
   };
-  for (int p = warp; p < segs; p += kWarps) {
-    const int c = s_cnt[p];
-    for (int j0 = coarse_in(p); j0 < c; j0 += 32) {
-      const int j = j0 + lane;
-      const uint64_t k = j < c ? row[p * cap + j] : 0ull;
-      const bool act = j < c && page_active(k);
-      const unsigned bal = __ballot_sync(kFull, act);
-      int base = 0;
-      if (lane == 0 && bal) base = atomicAdd(&s_np, __popc(bal));
-      base = __shfl_sync(kFull, base, 0) + __popc(bal & ((1u << lane) - 1u));
-      if (act && base < kPageStage) s_pk[base] = k;
+  // Warp w takes the 32-key chunks [w*W, (w+1)*W) of the row's compact
+  // order, lane l the l-th
+  // key of each (coalesced), eight chunks' loads in flight; a chunk's first
+  // segment comes from s_chunk_seg (rows of up to kChunkMap chunks) or from a
+  // search.
+  const int W = ((ntot + 31) / 32 + kWarps - 1) / kWarps;  // chunks per warp
+  const bool mapped = ntot <= kChunkMap * 32;
+  auto seg_of_chunk = [&](int c) {
+    if (mapped) return s_chunk_seg[c];
+    int sg = 0;
+    for (int step = kPoolMaxSegs / 2; step > 0; step >>= 1)
+      if (sg + step < segs && s_off[sg + step] <= c * 32) sg += step;
+    return sg;
+  };
+  // visits this lane's positions: fn(active, key) for each
+  auto visit_run = [&](auto&& fn) {
+    constexpr int kBatch = 8;
+    for (int u0 = 0; u0 < W; u0 += kBatch) {
+      uint64_t v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = warp * W + u0 + u, pos = c * 32 + lane;
+        v[u] = 0ull;
+        if (u0 + u < W && pos < ntot) {
+          int sg = seg_of_chunk(c);
+          while (pos >= s_off[sg] + s_cnt[sg]) ++sg;
+          v[u] = row[sg * cap + (pos - s_off[sg])];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = warp * W + u0 + u;
+        if (u0 + u < W && c * 32 + lane < ntot) fn(page_active(v[u]), v[u]);
+      }
     }
-  }
+  };
+  visit_run([&](bool act, uint64_t k) {
+    if (act) {
+      const int q = atomicAdd(&s_np, 1);
+      if (q < kPageStage) s_pk[q] = k;
+    }
+  });
   __syncthreads();
   const int np = s_np;
   const bool staged = np <= kPageStage;
@@ -304,13 +350,7 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
     if (staged) {
       for (int i = tid; i < np; i += kThreads) fn(true, s_pk[i]);
     } else {
-      for (int p = warp; p < segs; p += kWarps) {
-        const int c = s_cnt[p];
-        for (int j = coarse_in(p) + lane; j < c; j += 32) {
-          const uint64_t k = row[p * cap + j];
-          fn(page_active(k), k);
-        }
-      }
+      visit_run(fn);
     }
   };
   if (m > 0) {
@@ -348,6 +388,12 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
 
 }  // namespace
 
+size_t hier_pool_workspace_bytes(int R, int N, int cp, int gc) {
+  const int H = hier_pool_coarse_rows(N, cp, gc);
+  const size_t gemm = (batched_workspace_bytes(R, H + N) + 255) & ~size_t(255);
+  return gemm + sizeof(float) * (size_t)R * (size_t)H;
+}
+
 int hier_pool_coarse_rows(int N, int cp, int gc) {
   if (N <= 0) return 0;
   const int C = (N + cp - 1) / cp, G = (C + gc - 1) / gc;
@@ -369,7 +415,9 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
   const int C = N > 0 ? (N + cp - 1) / cp : 0, G = C > 0 ? (C + gc - 1) / gc : 0;
   const int H = hier_pool_coarse_rows(N, cp, gc);
   PoolSegments seg;
-  cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, ws, err, s, &seg);
+  float* coarse = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                           ((batched_workspace_bytes(R, H + N) + 255) & ~size_t(255)));
+  cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, coarse, ws, err, s, &seg);
   if (e != cudaSuccess) return e;
   constexpr int kDyn = (int)sizeof(uint64_t) * (kHierPoolCoarseMax + kPageStage);
   static std::mutex mu;
@@ -383,7 +431,7 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  HierPoolArgs ha{seg, mask, N, G, C, H, cp, gc, {permille[0], permille[1], permille[2]}, K, idx, top, kept, err};
+  HierPoolArgs ha{seg, coarse, mask, N, G, C, H, cp, gc, {permille[0], permille[1], permille[2]}, K, idx, top, kept, err};
   // programmatic dependent launch: scheduled while the GEMM drains
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)R);

@@ -80,25 +80,33 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 
 // kk_batched.cu
 // Shared-pool GEMM (kk_batched.cu): the candidate keys of each anchor, one
-// segment per (anchor, GEMM CTA) holding `counts` keys (score, row) in row
-// order. V has `rows` rows: `rows - N` coarse rows (a multiple of 128, the
-// first `coarse_rows` of them scored for every anchor), then the N pool
-// blocks, which the mask (uint32 [R][ceil(N/32)]) filters.
+// segment per (anchor, GEMM CTA, epilogue group) holding `counts` keys
+// (score, row) in row order. V has `rows` rows: `rows - N` coarse rows (a
+// multiple of 128, scored for every anchor into `coarse`, float [R][rows -
+// N], dense, no keys), then the N pool blocks, which the mask (uint32
+// [R][ceil(N/32)]) filters; `coarse_rows` of the coarse rows are real.
+// GEMM CTA p (of P per anchor tile) takes the 128-row tiles p, p + P, ...,
+// its j-th tile going to group g when g*n/4 <= j < (g+1)*n/4 (n = its tiles);
+// segment s belongs to CTA s / 4, group s % 4.
 constexpr int kPoolMaxSegs = 1024;
+constexpr int kPoolGroups = 4;
 struct PoolSegments {
   const uint64_t* cand;  // [R][segs][cap]
   const int* counts;     // [R][segs]
-  int segs;
+  int segs;              // P * kPoolGroups
   long long cap;
+  int P;                 // GEMM CTAs per anchor tile
+  int tiles;             // 128-row tiles of V
 };
 size_t batched_workspace_bytes(int R, int N);
 cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, const uint32_t* mask, int R, int N,
-                             int coarse_rows, void* ws, int* err, cudaStream_t s, PoolSegments* out);
+                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolSegments* out);
 // Shared-pool hierarchy (kk_hier_pool.cu): coarse rows in front of the pool
 // (Grids, Chunks, zero padding to a multiple of 128), at most
 // kHierPoolCoarseMax Grids + Chunks.
 constexpr int kHierPoolCoarseMax = 4096;
 int hier_pool_coarse_rows(int N, int cp, int gc);
+size_t hier_pool_workspace_bytes(int R, int N, int cp, int gc);
 cudaError_t launch_hier_pool_reps(uint16_t* M, int N, int cp, int gc, cudaStream_t s);
 cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32_t* mask, int R, int N,
                                     int cp, int gc, const int* permille, int K, int* idx, float* top, int* kept,
