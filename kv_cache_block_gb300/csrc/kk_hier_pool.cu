@@ -31,7 +31,7 @@ constexpr int kRepThreads = 256;  // 16 column octets x 16 row slots
 constexpr int kRepSlots = kRepThreads / (kCols / 8);
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPageStage = 8192;  // active blocks of an anchor listed in shared memory
+constexpr int kPageStage = 4096;  // active blocks of an anchor listed in shared memory
 constexpr int kChunkMap = 1024;   // 32-key chunks of a row mapped to their first segment
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
@@ -180,8 +180,9 @@ __device__ uint64_t radix_kth(Visit&& visit, int k, int* hist, int* s_pick) {
 
 __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPoolArgs a) {
   extern __shared__ __align__(16) uint64_t s_dyn[];
-  uint64_t* s_ck = s_dyn;                    // [kHierPoolCoarseMax] coarse keys by row
-  uint64_t* s_pk = s_dyn + kHierPoolCoarseMax;  // [kPageStage] active block keys
+  uint64_t* s_pk = s_dyn;                                              // [kPageStage] active block keys
+  float* s_cs = reinterpret_cast<float*>(s_dyn + kPageStage);          // [kHierPoolCoarseMax] coarse scores
+  auto coarse_key = [&](int x) { return make_key(s_cs[x], (uint32_t)x); };
   __shared__ uint32_t s_call[kHierPoolCoarseMax / 32];  // Chunks covering an allowed block
   __shared__ uint32_t s_gall[kHierPoolCoarseMax / 32];  // Grids covering an allowed block
   __shared__ uint32_t s_ckept[kHierPoolCoarseMax / 32];
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
     __syncthreads();
   }
   // the coarse rows' scores, as keys (score, row)
-  for (int x = tid; x < nco; x += kThreads) s_ck[x] = make_key(a.coarse[(long long)r * a.H + x], (uint32_t)x);
+  for (int x = tid; x < nco; x += kThreads) s_cs[x] = a.coarse[(long long)r * a.H + x];
   __syncthreads();
 
   // ---- Grids, then Chunks: keep ceil(n * permille / 1000) of the n active
@@ -283,11 +284,11 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
     if (m == 0) return;
     const uint64_t T = radix_kth(
         [&](auto&& fn) {
-          for (int i = tid; i < n; i += kThreads) fn(active(i), s_ck[base + i]);
+          for (int i = tid; i < n; i += kThreads) fn(active(i), coarse_key(base + i));
         },
         m, hist, s_pick);
     for (int i = tid; i < n; i += kThreads)
-      if (active(i) && s_ck[base + i] >= T) atomicOr(&kept_bits[i >> 5], 1u << (i & 31));
+      if (active(i) && coarse_key(base + i) >= T) atomicOr(&kept_bits[i >> 5], 1u << (i & 31));
     __syncthreads();
   };
   level(0, G, [&](int g) { return bit(s_gall, g); }, s_gkept, a.permille[0]);
@@ -419,7 +420,7 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
                                            ((batched_workspace_bytes(R, H + N) + 255) & ~size_t(255)));
   cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, coarse, ws, err, s, &seg);
   if (e != cudaSuccess) return e;
-  constexpr int kDyn = (int)sizeof(uint64_t) * (kHierPoolCoarseMax + kPageStage);
+  constexpr int kDyn = (int)(sizeof(uint64_t) * kPageStage + sizeof(float) * kHierPoolCoarseMax);
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -428,6 +429,10 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
   std::lock_guard<std::mutex> lock(mu);
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(hier_pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+    if (e != cudaSuccess) return e;
+    // as much shared memory as the SM has, so that several anchors share an SM
+    e = cudaFuncSetAttribute(hier_pool_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }

@@ -195,7 +195,7 @@ def test_streamed_block_level(kk, pm):
     mask = np.full((R, (N + 31) // 32), 0xFFFFFFFF, dtype=np.uint32)
     mask[2, ::3] = 0
     g_idx, g_top, g_kept = _run(kk, A, M, mask, N, cp, gc, pm, K)
-    assert g_kept[0] > 8192  # past the shared-memory list
+    assert g_kept[0] > 4096  # more active blocks than the shared-memory list holds (4096)
     check_against_oracle(A, M, G, C, H, mask, N, cp, gc, pm, K, g_idx, g_top, g_kept)
 
 
