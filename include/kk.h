@@ -299,7 +299,7 @@ kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk
  * of the bf16 values; per anchor the top K pool ids (ordered as kk_topk) go
  * to idx [R][K] and top_scores [R][K] (nullable). D = 128, 1 <= K <= 256.
  * workspace: caller-owned device memory, 256-byte aligned, of at least
- * kk_score_pool_batched_workspace_bytes(R, N, K) bytes (about 8 * R * N plus
+ * kk_score_pool_batched_workspace_bytes(R, N, K) bytes (about 8 to 10 * R * N plus
  * counts); the size depends on the SM count of the current device, so query
  * it with the device that will run the call current. Concurrent calls need
  * separate workspaces.

@@ -5,13 +5,17 @@
 //
 // Kernel 1 is a persistent tcgen05 GEMM: TMA streams 128-block tiles of V
 // (128-byte swizzle) past a resident 128-anchor tile of A, one thread issues
-// eight 128x128x16 bf16 MMAs per tile into one of two TMEM fp32 accumulators,
-// and four epilogue warps read them back (tcgen05.ld), divide by the norms
-// (computed from the same shared-memory tiles), apply the ownership mask and write each
-// owned candidate as a 64-bit key (score, pool id) into the anchor's segment
-// for this tile, with the segment's count (no atomics: one writer each).
-// Kernel 2 selects each anchor's top K from its list by radix select over the
-// 64-bit keys (8-bit digits, most significant first), then sorts the K.
+// eight 128x128x16 bf16 MMAs per tile into one of four TMEM fp32
+// accumulators, and four epilogue groups of four warps read them back
+// (tcgen05.ld), divide by the norms (computed from the same shared-memory
+// tiles), apply the ownership mask and write each owned candidate as a 64-bit
+// key (score, pool id) into the segment of (anchor, CTA, group), with the
+// segment's count (no atomics: one writer each). Rows in front of the pool
+// that every anchor scores (the coarse levels of the hierarchy) are written
+// as a dense score matrix instead. Kernel 2 selects each anchor's top K from
+// its segments (linear buckets over the score range, exact ranking of the
+// boundary bucket, a radix select on the 64-bit keys for massive ties), then
+// sorts the K.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -96,9 +100,10 @@ __device__ __forceinline__ float row_sq(const unsigned char* tile, int row) {
 // round robin, so four tiles drain at once. A group computes its tile's V-row
 // norms from the ring (then releases the stage), reads the accumulator (one
 // anchor row per thread, tcgen05.ld), and writes each owned column as a
-// 64-bit key (score, pool id) into the anchor's segment for this CTA, in tile
-// order; the last group writes the segment's length. No atomics: every slot
-// has one writer.
+// 64-bit key (score, pool id) into its own segment of that anchor, in tile
+// order, and the segment's length at the end. No atomics: every slot has one
+// writer. kCoarse: the first tiles hold rows every anchor scores, written as
+// dense scores.
 template <bool kCoarse>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     score_pool_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmV,
@@ -463,13 +468,13 @@ __device__ __forceinline__ void for_each_segment_key(const SelArgs& a, const int
   }
 }
 
-// One CTA per anchor. The row's segments are copied into shared memory with
-// warp-wide coalesced loads, then into registers (24 keys a thread). One pass
-// of linear buckets over the row's score range finds the bucket holding the
-// K-th key; keys above it are selected, the boundary bucket's keys are ranked
-// exactly; the K winners are sorted (warp bitonic lists + merge ranks). Rows
-// longer than the shared-memory copy take the same passes over the segments,
-// with a radix select on the 64-bit keys when a bucket holds too many ties.
+// One CTA per anchor. The row's keys go from its segments straight into
+// registers (24 keys a thread, coalesced loads). One pass of linear buckets
+// over the row's score range finds the bucket holding the K-th key; keys
+// above it are selected, the boundary bucket's keys are ranked exactly; the K
+// winners are sorted (warp bitonic lists + merge ranks). Rows of more than 24
+// keys a thread take the same passes over the segments, with a radix select
+// on the 64-bit keys when a bucket holds too many ties.
 __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs a) {
   __shared__ int hist[kBuckets];
   __shared__ int s_cnt[kMaxSegs];

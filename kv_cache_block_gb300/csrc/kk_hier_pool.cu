@@ -11,13 +11,13 @@
 // once to bf16).
 //
 // The product is the shared-pool GEMM of kk_batched.cu with the coarse rows
-// in front: every anchor gets a key (score, row) for every coarse row and for
-// each block its mask allows. hier_pool_select_kernel then takes one anchor
-// per CTA: the coarse keys sit at known places of the anchor's segments; a
-// coarse member is active when it covers an allowed block (and, for a Chunk,
-// its Grid was kept); each level keeps ceil(n * permille / 1000) of its n
-// active members by a radix select on the 64-bit keys; the allowed blocks of
-// kept Chunks are listed in shared memory and the best of them written out.
+// in front: every anchor gets the scores of all coarse rows (a dense matrix)
+// and a key (score, row) for each block its mask allows.
+// hier_pool_select_kernel then takes one anchor per CTA: a coarse member is
+// active when it covers an allowed block (and, for a Chunk, its Grid was
+// kept); each level keeps ceil(n * permille / 1000) of its n active members
+// by a radix select on the 64-bit keys; the allowed blocks of kept Chunks are
+// listed in shared memory and the best of them written out.
 #include <mutex>
 
 #include "kk_device.cuh"
