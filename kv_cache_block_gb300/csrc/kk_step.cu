@@ -12,6 +12,7 @@
 // with no global scratch. Every stage can be switched off, which gives
 // kk_anchor, kk_score, kk_topk and kk_score_topk from the same code.
 #include <mutex>
+#include <type_traits>
 
 #include "kk_device.cuh"
 #include "kk_internal.h"
@@ -22,7 +23,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kThreads;  // candidates per top-K tile
-constexpr int kUnroll = 8;
 constexpr int kStage = 64;  // v_b rows staged in shared memory by bulk copies
 
 template <int D>
@@ -222,35 +222,53 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     const int vec = lane % V16, tl = lane / V16;
     const int LH = p.kc.L * p.kc.H;
 
+    // Warp w of CTA crank takes the (layer, head) slices crank + CL * (w +
+    // kWarps * k), two at a time: both slices' token rows are loaded before
+    // either is summed, so a warp waits for memory once per pair.
+    constexpr int kUnroll = 8;
     float acc[EPV];
 #pragma unroll
     for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
     const char* kbase = reinterpret_cast<const char*>(p.kc.base) + vec * 16;
-    for (int s = crank + CL * warp; s < LH; s += CL * kWarps) {
+    const int sstride = CL * kWarps;
+    for (int s = crank + CL * warp; s < LH; s += 2 * sstride) {
+      const int s2 = s + sstride;
+      const bool has2 = s2 < LH;
       const int l = s / p.kc.H, h = s - l * p.kc.H;
+      const int l2 = has2 ? s2 / p.kc.H : 0, h2 = has2 ? s2 - l2 * p.kc.H : 0;
       const char* sbase = kbase + ((long long)l * p.kc.sL + (long long)h * p.kc.sH) * ES;
-      float ps[EPV];
+      const char* sbase2 = kbase + ((long long)l2 * p.kc.sL + (long long)h2 * p.kc.sH) * ES;
+      float ps[EPV], ps2[EPV];
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) ps[e] = 0.f;
+      for (int e = 0; e < EPV; ++e) {
+        ps[e] = 0.f;
+        ps2[e] = 0.f;
+      }
       for (int i0 = 0; i0 < w_eff; i0 += kUnroll * RPW) {
-        uint4 v[kUnroll];
+        uint4 v[kUnroll], v2[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int i = i0 + u * RPW + tl;
           const long long o = (i < w_eff) ? sm.tok[i] : -1;
           v[u] = ld_stream16(sbase + (o >= 0 ? o : 0), o >= 0);
+          v2[u] = ld_stream16(sbase2 + (o >= 0 ? o : 0), has2 && o >= 0);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-          float f[EPV];
+          float f[EPV], f2[EPV];
           Vec16<T>::unpack(v[u], f);
+          Vec16<T>::unpack(v2[u], f2);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) ps[e] += f[e];
+          for (int e = 0; e < EPV; ++e) {
+            ps[e] += f[e];
+            ps2[e] += f2[e];
+          }
         }
       }
       const float wt = p.head_w ? sm.w[s] : 1.f;
+      const float wt2 = has2 ? (p.head_w ? sm.w[s2] : 1.f) : 0.f;
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) acc[e] = fmaf(wt, ps[e], acc[e]);
+      for (int e = 0; e < EPV; ++e) acc[e] = fmaf(wt2, ps2[e], fmaf(wt, ps[e], acc[e]));
     }
 #pragma unroll
     for (int e = 0; e < EPV; ++e)
@@ -297,6 +315,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   // ---- stage 2: scores and the CTA's top-K over its share of the blocks --
   // Running top-K list: sm.run[cur][0..Kp), descending, zero-padded.
   int run_n = 0, cur = 0;
+  // Few blocks per CTA: no per-CTA list; stage 3 all-gathers the raw keys
+  // and every CTA ranks its own by counting.
+  constexpr int kDirectMax = 64;
+  const bool direct = do_topk && CL > 1 && chunk <= kDirectMax;
   if (do_topk)
     for (int i = tid; i < Kp; i += kThreads) sm.run[0][i] = 0ull;
   if (do_score || from_scores) {
@@ -331,73 +353,83 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
           sm.pg[tid] = pg;
           __syncthreads();
         }
-        // warp w scores tile slots w, w + 8, w + 16, ...; kRows rows in flight
-        constexpr int kRows = D <= 128 ? 16 : 8;
-        for (int base = warp; base < tcount; base += kWarps * kRows) {
-          RowSlice<D> b[kRows];
+        // warp w scores tile slots w, w + 8, w + 16, ...; kRows rows in
+        // flight (4 when the tile has at most 4 rows a warp, so that small
+        // tiles do not pay for a 32-value reduction)
+        auto score_rows = [&](auto rows_c) {
+          constexpr int kRows = decltype(rows_c)::value;
+          for (int base = warp; base < tcount; base += kWarps * kRows) {
+            RowSlice<D> b[kRows];
 #pragma unroll
-          for (int u = 0; u < kRows; ++u) {
-            // always load (row 0 for empty slots, masked below): no branch, so
-            // all kRows rows are in flight together
-            const int slot = base + u * kWarps;
-            const int pg = slot < tcount ? sm.pg[slot] : -1;
-            const bool staged = first && slot < nstage;
-            if (staged) {
-              b[u].load(&sm.stage[slot][0], lane);  // bulk-copied into shared memory
-            } else {
-              b[u].load_global(p.vb + (long long)(pg < 0 ? 0 : pg) * D, lane);
-            }
-            if (pg < 0 || (staged && !staged_ok)) b[u].zero();
-          }
-          // per-lane partial dots and squared norms of the kRows rows, then
-          // one transposed reduction: lane u ends with row u's dot, lane
-          // kRows + u with its squared norm
-          float part[2 * kRows];
-#pragma unroll
-          for (int u = 0; u < kRows; ++u) {
-            float dot = 0.f, n2 = 0.f;
-#pragma unroll
-            for (int e = 0; e < RowSlice<D>::kPer; ++e) {
-              dot = fmaf(a.v[e], b[u].v[e], dot);
-              n2 = fmaf(b[u].v[e], b[u].v[e], n2);
-            }
-            part[u] = dot;
-            part[kRows + u] = n2;
-          }
-          warp_sum_transpose<2 * kRows>(part, lane);
-          const float n2 = __shfl_down_sync(kFull, part[0], kRows);
-          const int u = lane;
-          const int slot = base + u * kWarps;
-          if (u < kRows && slot < tcount) {
-            const float dot = part[0];
-            float cosv = 0.f;
-            if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
-            cosv = fminf(1.f, fmaxf(-1.f, cosv));
-            const float sc = fmaf(0.5f, cosv, 0.5f);
-            const int j = tile0 + slot;
-            if (p.scores_out) p.scores_out[off + j] = sc;
-            uint64_t key = 0ull;
-            if (sm.pg[slot] >= 0) {
-              if (p.hist) {
-                // stability filter: shift this step's bit into the block's window
-                const uint32_t wmask = p.stab_w >= 32 ? 0xFFFFFFFFu : ((1u << p.stab_w) - 1u);
-                const uint32_t h = ((p.hist[off + j] << 1) | (sc > p.stab_theta ? 1u : 0u)) & wmask;
-                p.hist[off + j] = h;
-                if (p.stab_out) p.stab_out[off + j] = (float)__popc(h) / (float)p.stab_w;
-                key = make_stab_key((uint32_t)__popc(h), sc, (uint32_t)j);
+            for (int u = 0; u < kRows; ++u) {
+              // always load (row 0 for empty slots, masked below): no branch, so
+              // all kRows rows are in flight together
+              const int slot = base + u * kWarps;
+              const int pg = slot < tcount ? sm.pg[slot] : -1;
+              const bool staged = first && slot < nstage;
+              if (staged) {
+                b[u].load(&sm.stage[slot][0], lane);  // bulk-copied into shared memory
+              } else if (slot >= tcount) {
+                b[u].load(sm.va, lane);  // an empty slot (zeroed below): no global round trip
               } else {
-                key = make_key(sc, (uint32_t)j);
+                b[u].load_global(p.vb + (long long)(pg < 0 ? 0 : pg) * D, lane);
               }
+              if (pg < 0 || (staged && !staged_ok)) b[u].zero();
             }
-            sm.keys[slot] = key;
+            // per-lane partial dots and squared norms of the kRows rows, then
+            // one transposed reduction: lane u ends with row u's dot, lane
+            // kRows + u with its squared norm
+            float part[2 * kRows];
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+              float dot = 0.f, n2 = 0.f;
+#pragma unroll
+              for (int e = 0; e < RowSlice<D>::kPer; ++e) {
+                dot = fmaf(a.v[e], b[u].v[e], dot);
+                n2 = fmaf(b[u].v[e], b[u].v[e], n2);
+              }
+              part[u] = dot;
+              part[kRows + u] = n2;
+            }
+            warp_sum_transpose<2 * kRows>(part, lane);
+            const float n2 = __shfl_down_sync(kFull, part[0], kRows);
+            const int u = lane;
+            const int slot = base + u * kWarps;
+            if (u < kRows && slot < tcount) {
+              const float dot = part[0];
+              float cosv = 0.f;
+              if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
+              cosv = fminf(1.f, fmaxf(-1.f, cosv));
+              const float sc = fmaf(0.5f, cosv, 0.5f);
+              const int j = tile0 + slot;
+              if (p.scores_out) p.scores_out[off + j] = sc;
+              uint64_t key = 0ull;
+              if (sm.pg[slot] >= 0) {
+                if (p.hist) {
+                  // stability filter: shift this step's bit into the block's window
+                  const uint32_t wmask = p.stab_w >= 32 ? 0xFFFFFFFFu : ((1u << p.stab_w) - 1u);
+                  const uint32_t h = ((p.hist[off + j] << 1) | (sc > p.stab_theta ? 1u : 0u)) & wmask;
+                  p.hist[off + j] = h;
+                  if (p.stab_out) p.stab_out[off + j] = (float)__popc(h) / (float)p.stab_w;
+                  key = make_stab_key((uint32_t)__popc(h), sc, (uint32_t)j);
+                } else {
+                  key = make_key(sc, (uint32_t)j);
+                }
+              }
+              sm.keys[slot] = key;
+            }
           }
-        }
+        };
+        if (tcount <= kWarps * 4)
+          score_rows(std::integral_constant<int, 4>());
+        else
+          score_rows(std::integral_constant<int, (D <= 128 ? 16 : 8)>());
       } else {
         const int j = tile0 + tid;
         sm.keys[tid] = (tid < tcount) ? make_key(p.scores_in[off + j], (uint32_t)j) : 0ull;
       }
       __syncthreads();
-      if (!do_topk) continue;
+      if (!do_topk || direct) continue;
       // merge this tile into the running list
       uint64_t key = tid < tcount ? sm.keys[tid] : 0ull;
       const uint64_t thr = (run_n == K) ? sm.run[cur][K - 1] : 0ull;
@@ -457,6 +489,52 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         const uint64_t k = have ? sm.run[cur][i] : 0ull;
         idx_out[i] = have ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
         if (top_out) top_out[i] = have ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
+      }
+    } else if (direct) {
+      if (!start_waited) {
+        cluster_wait_acquire();
+        start_waited = true;
+      }
+      // all-gather of the raw keys (zero for blocks with a bad page): CTA c's
+      // j1 - j0 keys at merge[c * chunk ...], its count of real keys in mcount
+      const int mine = j1 - j0;
+      if (mine > 0)
+        for (int f = tid; f < CL * mine; f += kThreads) {
+          const int dst = f / mine, i = f - dst * mine;
+          st_cluster_u64(map_to_rank(smem_u32(&sm.merge[crank * chunk + i]), dst), sm.keys[i]);
+        }
+      const int nv = __syncthreads_count(tid < mine && sm.keys[tid] != 0ull);
+      if (tid < CL) st_cluster_s32(map_to_rank(smem_u32(&sm.mcount[crank]), tid), nv);
+      cluster_arrive_release();
+      cluster_wait_acquire();
+      // rank of each own key = the keys above it in the union; tpk threads
+      // (consecutive lanes) per key split the count
+      int tpk = 1;
+      while (tpk < 32 && tpk * 2 * max(1, mine) <= kThreads) tpk <<= 1;
+      const int ki = tid / tpk, part = tid & (tpk - 1);
+      const uint64_t k = ki < mine ? sm.keys[ki] : 0ull;
+      // CTA c's keys end where CTA c + 1's begin, so the union is merge[0, nb)
+      int cnt = 0;
+      if (k != 0ull)
+        for (int j = part; j < nb; j += 8 * tpk) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int jj = j + u * tpk;
+            cnt += (jj < nb && sm.merge[jj] > k) ? 1 : 0;
+          }
+        }
+      for (int o = 1; o < tpk; o <<= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+      if (k != 0ull && part == 0 && cnt < K) {
+        idx_out[cnt] = (int)(stab ? stab_key_index(k) : key_index(k));
+        if (top_out) top_out[cnt] = stab ? stab_key_score(k) : key_score(k);
+      }
+      if (crank == 0) {
+        int total = 0;
+        for (int q = 0; q < CL; ++q) total += sm.mcount[q];
+        for (int i = total + tid; i < K; i += kThreads) {
+          idx_out[i] = -1;
+          if (top_out) top_out[i] = -__int_as_float(0x7f800000);
+        }
       }
     } else {
       if (!start_waited) {
