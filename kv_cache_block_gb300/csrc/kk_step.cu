@@ -369,8 +369,6 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
               const bool staged = first && slot < nstage;
               if (staged) {
                 b[u].load(&sm.stage[slot][0], lane);  // bulk-copied into shared memory
-              } else if (slot >= tcount) {
-                b[u].load(sm.va, lane);  // an empty slot (zeroed below): no global round trip
               } else {
                 b[u].load_global(p.vb + (long long)(pg < 0 ? 0 : pg) * D, lane);
               }
