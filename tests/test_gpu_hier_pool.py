@@ -219,3 +219,43 @@ def test_hier_pool_reps(kk, N, cp, gc):
         np.testing.assert_array_less(np.abs(g - ref), 2.0**-7 * np.abs(ref) + 1e-6, err_msg=name)
         exact = np.mean(rows == synth.bf16_rne(ref.astype(np.float32)))
         assert exact >= 0.99, f"{name}: only {exact:.4f} of the values round like the exact mean"
+
+
+def test_empty_pool_and_large_k(kk):
+    """N = 0: nothing is kept and every slot is padding; K larger than the
+    blocks kept: the kept blocks, then padding."""
+    R, K = 3, 256
+    A, _ = _rows(1, R, seed=2)
+    mask = np.zeros((R, 1), dtype=np.uint32)
+    M = np.zeros((0, 128), dtype=np.uint16)
+    At = torch.from_numpy(A.view(np.int16)).cuda()
+    Mt = torch.zeros((0, 128), dtype=torch.int16, device="cuda")
+    mt = torch.from_numpy(mask.view(np.int32)).cuda()
+    ws = torch.empty(max(1, kk.kk_hier_select_pool_workspace_bytes(R, 0, 64, 8)), dtype=torch.uint8, device="cuda")
+    idx = torch.full((R, K), 7, dtype=torch.int32, device="cuda")
+    top = torch.zeros((R, K), device="cuda")
+    kept = torch.full((R,), -3, dtype=torch.int32, device="cuda")
+    kk.kk_hier_select_pool(At, Mt, mt, 0, 64, 8, (500, 200, 100), idx, top, kept, ws)
+    assert kk.kk_device_error() == 0
+    assert np.all(idx.cpu().numpy() == -1) and np.all(np.isneginf(top.cpu().numpy()))
+    assert np.all(kept.cpu().numpy() == 0)
+    # a small pool where every level is kept whole: K exceeds the allowed blocks
+    N, cp, gc = 150, 16, 2
+    A, V = _rows(N, R, seed=5)
+    M, G, C, H = _matrix(kk, V, cp, gc)
+    mask = _mask("0.4", R, N, seed=6)
+    g_idx, g_top, g_kept = _run(kk, A, M, mask, N, cp, gc, (1000, 1000, 1000), K)
+    allowed = [int(_allowed(mask, r, N).sum()) for r in range(R)]
+    assert g_kept.tolist() == allowed and max(allowed) < K
+    check_against_oracle(A, M, G, C, H, mask, N, cp, gc, (1000, 1000, 1000), K, g_idx, g_top, g_kept)
+
+
+def test_single_anchor(kk):
+    """One anchor: the GEMM's anchor tile holds one real row of 128."""
+    N, cp, gc, K = 1000, 8, 4, 20
+    A, V = _rows(N, 1, seed=8)
+    M, G, C, H = _matrix(kk, V, cp, gc)
+    mask = _mask("0.5", 1, N, seed=9)
+    mask[0] = np.random.default_rng(3).integers(0, 2**32, size=mask.shape[1], dtype=np.uint64).astype(np.uint32)
+    g_idx, g_top, g_kept = _run(kk, A, M, mask, N, cp, gc, (500, 300, 200), K)
+    check_against_oracle(A, M, G, C, H, mask, N, cp, gc, (500, 300, 200), K, g_idx, g_top, g_kept)
