@@ -413,7 +413,7 @@ kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {
   (void)K;
   if (R < 0 || N < 0) return 0;
-  return kk::batched_workspace_bytes(R, N);
+  return kk::batched_workspace_bytes(R, N, N);
 }
 
 kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,
@@ -424,7 +424,7 @@ kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint
   if (R == 0) return KK_OK;
   if (D != 128) return KK_ERR_UNSUPPORTED;
   if (!idx || !workspace || (N > 0 && (!A || !V || !mask))) return KK_ERR_INVALID;
-  if (workspace_bytes < kk::batched_workspace_bytes(R, N)) return KK_ERR_INVALID;
+  if (workspace_bytes < kk::batched_workspace_bytes(R, N, N)) return KK_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(V) % 16 ||
       reinterpret_cast<uintptr_t>(workspace) % 256)
     return KK_ERR_UNSUPPORTED;

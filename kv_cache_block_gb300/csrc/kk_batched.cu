@@ -35,7 +35,7 @@ constexpr int kD = 128;   // head_dim (two 64-element swizzle boxes)
 constexpr int kBoxBytes = 128 * 128;   // 128 rows x 128 bytes
 constexpr int kTileBytes = 2 * kBoxBytes;
 constexpr int kStages = 3;             // V tiles in flight
-constexpr int kGroups = kPoolGroups;   // epilogue groups, each drains whole tiles
+constexpr int kGroups = 4;             // epilogue groups, each drains whole tiles
 constexpr int kAccs = kGroups;         // TMEM accumulators (128 columns each), one per group
 constexpr int kGroupThreads = 128;     // four warps: one per TMEM lane quarter
 constexpr int kEpiThreads = kGroups * kGroupThreads;
@@ -52,9 +52,9 @@ struct GemmArgs {
   int coarse_rows;  // rows before the pool's blocks that every anchor scores (0: none)
   int coarse_tiles; // tiles holding them (their rows come first, 128 per tile)
   float* coarse;    // [R][coarse_tiles * 128] their scores, dense
-  int* counts;      // [R][P][kGroups] candidates of each anchor in each epilogue group's tiles
-  uint64_t* cand;   // [R][P][kGroups][cap] candidate keys, one segment per (anchor, CTA, group)
-  long long cap;    // 128 x the most tiles an epilogue group takes
+  const int* offsets;  // [R][mtiles + 1] owned blocks of each anchor before each block tile, then the total
+  int mtiles;          // block tiles (128 pool blocks each)
+  uint64_t* keys;      // [R][N] each anchor's candidate keys, contiguous, in pool order
   int mask_vec;     // mask rows allow 16-byte loads of a tile's four words
   int* err;
 };
@@ -237,14 +237,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // limited to columns < N only when the tile is drained, so that the load
     // is not waited for early. Coarse tiles (first) have no mask.
     const uint32_t* mrow = g.mask + (long long)(r < g.R ? r : 0) * g.mask_words;
-    auto mask_load = [&](int jj, uint32_t (&w)[4]) {
+    const int* orow = g.offsets + (long long)(r < g.R ? r : 0) * (g.mtiles + 1);
+    auto mask_load = [&](int jj, uint32_t (&w)[4], int& o) {
       const int tile = p + jj * P;
+      o = 0;
       if (kCoarse && tile < g.coarse_tiles) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) w[c] = 0u;
         return;
       }
-      const int wi0 = (tile - g.coarse_tiles) * (kBN / 32);
+      const int mt = tile - g.coarse_tiles;
+      if (jj < ntiles && r < g.R) o = orow[mt];
+      const int wi0 = mt * (kBN / 32);
       if (g.mask_vec && jj < ntiles && r < g.R) {
         const uint4 x = *reinterpret_cast<const uint4*>(mrow + wi0);
         w[0] = x.x;
@@ -265,13 +269,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lim < 32) w[c] &= lim <= 0 ? 0u : ((1u << lim) - 1u);
       }
     };
-    // The anchor's keys from this group's tiles fill the group's own segment
-    // in tile order.
-    uint64_t* seg = g.cand + (((long long)(r < g.R ? r : 0) * P + p) * kGroups + grp) * g.cap;
-    int pre = 0;
+    // An anchor's keys go to its contiguous list, each tile's at the offset
+    // the offsets kernel (launched just before this grid) computed from the
+    // mask; only the epilogue waits for that grid.
+    uint64_t* list = g.keys + (long long)(r < g.R ? r : 0) * g.N;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t dump0 = dump - (uint32_t)(lane * kDumpStride * 4);  // lane 0's dump row in this warp
     uint32_t w_next[4];
-    mask_load(len > 0 ? lo : ntiles, w_next);
+    int o_next;
+    mask_load(len > 0 ? lo : ntiles, w_next, o_next);
     bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
     if (!ok) fail(kErrTimeout);
     const float inv_a = ok ? inv_norm(row_sq(sA, row)) : 0.f;
@@ -287,7 +293,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t w[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) w[c] = w_next[c];
-      mask_load(i + 1 < len ? j + 1 : ntiles, w_next);
+      const int o_tile = o_next;
+      mask_load(i + 1 < len ? j + 1 : ntiles, w_next, o_next);
       // V-row norms of this tile (one row per thread), then release the
       // ring stage. The group leaves the loop together (a lone warp leaving
       // would strand the others at the named barrier).
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool coarse = kCoarse && tile < g.coarse_tiles;
       if (!coarse) mask_finish(j, w);
       const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(grp * kBN);
-      uint64_t* out = seg + pre;
+      uint64_t* out = list + o_tile;
       int k = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -406,14 +413,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           k += (ib[0] >= 0) + (ib[1] >= 0) + (ib[2] >= 0) + (ib[3] >= 0);
         }
       }
-      pre += k;
-    }
-    // every group writes its count, also when it had no tile, and fills its
-    // segment's last 32-byte sector (the select reads whole sectors; one
-    // left partly written would be completed from DRAM)
-    if (r < g.R) {
-      g.counts[((long long)r * P + p) * kGroups + grp] = pre;
-      for (int i = pre; i & 3; ++i) seg[i] = 0ull;
     }
     tc_fence_before();
     __syncwarp();
@@ -437,14 +436,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 constexpr int kSelThreads = 256;
 constexpr int kSelStage = 6144;                    // keys of a row held in registers,
 constexpr int kRegKeys = kSelStage / kSelThreads;  // 24 per thread
-constexpr int kMaxSegs = kPoolMaxSegs;             // segments (GEMM CTAs per M-tile) of a row
 constexpr int kBuckets = 2048;                     // linear buckets over a row's score range
 constexpr int kTieCap = 512;                       // boundary-bucket keys ranked exactly
 
 struct SelArgs {
-  const uint64_t* cand;  // [R][segs][cap] keys, segment per (anchor, GEMM CTA)
-  const int* counts;     // [R][segs]
-  int segs;
+  const uint64_t* keys;  // [R][cap] each anchor's candidate keys, contiguous
+  const int* offsets;    // [R][mtiles + 1]: entry mtiles is the anchor's count
+  int mtiles;
   long long cap;
   int K;
   int* idx;
@@ -452,45 +450,38 @@ struct SelArgs {
   int* err;
 };
 
-// Visits every candidate key of a row straight from its segments,
-// warp-uniformly (every lane of a warp runs the same iterations; `active`
-// marks real keys): the path for rows longer than the shared-memory copy.
+// Visits every candidate key of a row, warp-uniformly (every lane of a warp
+// runs the same iterations; `active` marks real keys): the path for rows
+// longer than the register copy.
 template <typename F>
-__device__ __forceinline__ void for_each_segment_key(const SelArgs& a, const int* s_cnt, const uint64_t* row, F&& fn) {
+__device__ __forceinline__ void for_each_row_key(const uint64_t* row, int n, F&& fn) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int p = warp; p < a.segs; p += kSelThreads / 32) {
-    const int c = s_cnt[p];
-    for (int j0 = 0; j0 < c; j0 += 32) {
-      const int j = j0 + lane;
-      const bool active = j < c;
-      fn(active, active ? row[p * a.cap + j] : 0ull);
-    }
+  for (int j0 = warp * 32; j0 < n; j0 += kSelThreads) {
+    const int j = j0 + lane;
+    const bool active = j < n;
+    fn(active, active ? row[j] : 0ull);
   }
 }
 
-// One CTA per anchor. The row's keys go from its segments straight into
-// registers (24 keys a thread, coalesced loads). One pass of linear buckets
-// over the row's score range finds the bucket holding the K-th key; keys
-// above it are selected, the boundary bucket's keys are ranked exactly; the K
-// winners are sorted (warp bitonic lists + merge ranks). Rows of more than 24
-// keys a thread take the same passes over the segments, with a radix select
-// on the 64-bit keys when a bucket holds too many ties.
+// One CTA per anchor. The row's keys go straight into registers (24 keys a
+// thread, coalesced loads of the contiguous list). One pass of linear
+// buckets over the row's score range finds the bucket holding the K-th key;
+// keys above it are selected, the boundary bucket's keys are ranked exactly;
+// the K winners are sorted (warp bitonic lists + merge ranks). Rows of more
+// than 24 keys a thread take the same passes over the list, with a radix
+// select on the 64-bit keys when a bucket holds too many ties.
 __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs a) {
   __shared__ int hist[kBuckets];
-  __shared__ int s_cnt[kMaxSegs];
-  __shared__ int s_off[kMaxSegs];
-  __shared__ int s_chunk_seg[kSelStage / 32];  // segment holding position 32 * c
   __shared__ int s_bin, s_above;
   __shared__ int s_sel_n, s_tie_n;
   __shared__ int s_wsum[kSelThreads / 32];
   __shared__ uint64_t s_lo[kSelThreads / 32], s_hi[kSelThreads / 32];
   __shared__ uint64_t s_sel[kMaxK];
   __shared__ uint64_t s_tie[kTieCap];
-  __shared__ uint64_t s_wl[kSelThreads / 32][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   const int K = a.K;
-  const uint64_t* row = a.cand + (long long)r * a.segs * a.cap;
+  const uint64_t* row = a.keys + (long long)r * a.cap;
 
   for (int b = tid; b < kBuckets; b += kSelThreads) hist[b] = 0;
   if (tid == 0) {
@@ -499,65 +490,24 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
   }
   // the candidates come from the GEMM grid launched just before this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- segment counts and their offsets in the row's compact copy: each
-  // thread scans a run of up to four segments, then the block
-  const int spt = (a.segs + kSelThreads - 1) / kSelThreads;  // <= 4
-  const int s_begin = min(a.segs, tid * spt), s_end = min(a.segs, s_begin + spt);
-  int mine = 0;
-  for (int p = s_begin; p < s_end; ++p) {
-    int c = a.counts[(long long)r * a.segs + p];
-    if (c < 0 || c > a.cap) {
-      flag_error(a.err, kErrBadIndex);
-      c = c < 0 ? 0 : (int)a.cap;
-    }
-    s_cnt[p] = c;
-    mine += c;
-  }
-  int incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  int base = incl - mine, n = 0;
-#pragma unroll
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    if (w < warp) base += s_wsum[w];
-    n += s_wsum[w];
-  }
-  for (int p = s_begin; p < s_end; ++p) {
-    s_off[p] = base;
-    base += s_cnt[p];
+  int n = a.offsets[(long long)r * (a.mtiles + 1) + a.mtiles];
+  if (n < 0 || n > a.cap) {
+    if (tid == 0) flag_error(a.err, kErrBadIndex);
+    n = n < 0 ? 0 : (int)a.cap;
   }
   const bool staged = n <= kSelStage;
-  if (staged)
-    for (int p = s_begin; p < s_end; ++p)
-      for (int c = (s_off[p] + 31) / 32; c * 32 < s_off[p] + s_cnt[p]; ++c) s_chunk_seg[c] = p;
-  __syncthreads();
 
-  // ---- this thread's keys (rows of at most 24 keys a thread): warp w
-  // takes the 32-key chunks [w*W, (w+1)*W) of the row's compact order, lane
-  // l the l-th key of each (coalesced loads), straight from the segments
-  // into registers; a chunk's first segment comes from s_chunk_seg, so the
-  // rounds do not depend on one another
+  // ---- this thread's keys (rows of at most 24 keys a thread): keys tid,
+  // tid + 256, ... of the list (coalesced)
   uint64_t key[kRegKeys];
   uint32_t vmask = 0u;  // bit u: key[u] holds a candidate
   uint64_t lo = ~0ull, hi = 0ull;
   if (staged) {
-    const int W = (n + kSelThreads - 1) / kSelThreads;  // chunks per warp, <= kRegKeys
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) {
-      const int c = warp * W + u, pos = c * 32 + lane;
-      key[u] = 0ull;
-      if (u < W && pos < n) {
-        int sg = s_chunk_seg[c];
-        while (pos >= s_off[sg] + s_cnt[sg]) ++sg;
-        key[u] = row[sg * a.cap + (pos - s_off[sg])];
-        vmask |= 1u << u;
-      }
+      const int pos = tid + u * kSelThreads;
+      key[u] = pos < n ? row[pos] : 0ull;
+      vmask |= (pos < n ? 1u : 0u) << u;
     }
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) {
@@ -569,7 +519,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
   } else {
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) key[u] = 0ull;
-    for_each_segment_key(a, s_cnt, row, [&](bool active, uint64_t k) {
+    for_each_row_key(row, n, [&](bool active, uint64_t k) {
       if (active) {
         lo = k < lo ? k : lo;
         hi = k > hi ? k : hi;
@@ -595,13 +545,13 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
     hi = s_hi[w] > hi ? s_hi[w] : hi;
   }
   const int m = min(K, n);
-  // visits every key of the row warp-uniformly: registers, or the segments
+  // visits every key of the row warp-uniformly: registers, or the list
   auto visit = [&](auto&& fn) {
     if (staged) {
 #pragma unroll
       for (int u = 0; u < kRegKeys; ++u) fn(((vmask >> u) & 1u) != 0u, key[u]);
     } else {
-      for_each_segment_key(a, s_cnt, row, fn);
+      for_each_row_key(row, n, fn);
     }
   };
 
@@ -686,7 +636,7 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
         }
       }
     } else {
-      for_each_segment_key(a, s_cnt, row, [&](bool active, uint64_t k) {
+      for_each_row_key(row, n, [&](bool active, uint64_t k) {
         const int b = active ? bucket(k) : -1;
         const unsigned ab = __ballot_sync(kFull, b > bstar), ti = __ballot_sync(kFull, b == bstar);
         int p_sel = 0, p_tie = 0;
@@ -774,24 +724,15 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
     __syncthreads();
   }
   const int sel = m;
-  // ---- sort the selected keys: warp-sorted lists of 32, then rank in the union
-  uint64_t mine_key = tid < sel ? s_sel[tid] : 0ull;
-  mine_key = warp_sort_desc(mine_key, lane);
-  s_wl[warp][lane] = mine_key;
-  __syncthreads();
+  // ---- order the selected keys: a key's place is the number of selected
+  // keys above it (each thread reads the list in step, so the loads broadcast)
   int* io = a.idx + (long long)r * K;
   float* to = a.top ? a.top + (long long)r * K : nullptr;
-  if (mine_key != 0ull) {
-    int pos[kSelThreads / 32];
-#pragma unroll
-    for (int w = 0; w < kSelThreads / 32; ++w) pos[w] = 0;
-#pragma unroll
-    for (int step = 16; step > 0; step >>= 1)
-#pragma unroll
-      for (int w = 0; w < kSelThreads / 32; ++w) pos[w] += (s_wl[w][pos[w] + step] > mine_key) ? step : 0;
+  if (tid < sel) {
+    const uint64_t mine_key = s_sel[tid];
     int rank = 0;
-#pragma unroll
-    for (int w = 0; w < kSelThreads / 32; ++w) rank += (s_wl[w][0] > mine_key) ? pos[w] + 1 : 0;
+#pragma unroll 8
+    for (int q = 0; q < sel; ++q) rank += s_sel[q] > mine_key ? 1 : 0;
     if (rank < K) {
       io[rank] = (int)key_index(mine_key);
       if (to) to[rank] = key_score(mine_key);
@@ -835,52 +776,111 @@ cudaError_t setup_gemm() {
   return cudaSuccess;
 }
 
+// Owned blocks of each anchor before each 128-block tile, and its total:
+// offsets[r][t] = popcount of mask row r over tiles 0 .. t-1 (bits < N),
+// offsets[r][mtiles] = the row's total. One CTA per anchor, a contiguous run
+// of tiles per thread, then a block scan. This is where the GEMM's epilogue
+// writes each tile's keys in the anchor's contiguous list.
+__global__ void __launch_bounds__(kSelThreads) pool_offsets_kernel(const uint32_t* mask, int N, int mask_words,
+                                                                   int mtiles, int* offsets) {
+  __shared__ int s_wsum[kSelThreads / 32];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t* mrow = mask + (long long)r * mask_words;
+  int* orow = offsets + (long long)r * (mtiles + 1);
+  auto tile_count = [&](int t) {
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < kBN / 32; ++q) {
+      const int wi = t * (kBN / 32) + q;
+      const int lim = N - wi * 32;
+      if (lim <= 0) break;
+      const uint32_t x = __ldg(mrow + wi);
+      c += __popc(lim >= 32 ? x : (x & ((1u << lim) - 1u)));
+    }
+    return c;
+  };
+  const int per = (mtiles + kSelThreads - 1) / kSelThreads;
+  const int t0 = min(mtiles, tid * per), t1 = min(mtiles, t0 + per);
+  int mine = 0;
+  for (int t = t0; t < t1; ++t) mine += tile_count(t);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int base = incl - mine, total = 0;
+#pragma unroll
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    if (w < warp) base += s_wsum[w];
+    total += s_wsum[w];
+  }
+  for (int t = t0; t < t1; ++t) {
+    orow[t] = base;
+    base += tile_count(t);
+  }
+  if (tid == 0) orow[mtiles] = total;
+}
+
 // Work split of the shared-pool scorer: MT M-tiles of 128 anchors, P CTAs
 // per M-tile (one CTA per SM in all), CTA p of an M-tile taking tiles p,
-// p + P, ... (split into kGroups contiguous ranges); each (anchor, CTA,
-// group) segment holds up to `cap` keys.
+// p + P, ... (split into kGroups contiguous ranges). The workspace holds the
+// offsets [R][mtiles + 1], then each anchor's list of up to N keys.
 struct PoolLayout {
-  int tiles, MT, P;
-  long long cap;
-  size_t counts_bytes, bytes;
+  int tiles, MT, P, mtiles;
+  size_t offsets_bytes, bytes;
 };
 
-PoolLayout pool_layout(int R, int N) {
+PoolLayout pool_layout(int R, int rows, int N) {
   PoolLayout L;
-  L.tiles = (N + kBN - 1) / kBN;
+  L.tiles = (rows + kBN - 1) / kBN;
+  L.mtiles = (N + kBN - 1) / kBN;
   L.MT = (R + kBM - 1) / kBM;
-  L.P = L.tiles == 0 ? 0
-                     : std::max(1, std::min(std::min(L.tiles, kMaxSegs / kGroups), sm_count() / std::max(1, L.MT)));
-  L.cap = L.P == 0 ? 0 : (long long)(((L.tiles + L.P - 1) / L.P + kGroups - 1) / kGroups) * kBN;
-  L.counts_bytes = (sizeof(int) * (size_t)R * (size_t)L.P * kGroups + 255) & ~size_t(255);
-  L.bytes = L.counts_bytes + sizeof(uint64_t) * (size_t)R * (size_t)L.P * kGroups * (size_t)L.cap;
+  L.P = L.tiles == 0 ? 0 : std::max(1, std::min(L.tiles, sm_count() / std::max(1, L.MT)));
+  L.offsets_bytes = (sizeof(int) * (size_t)R * (size_t)(L.mtiles + 1) + 255) & ~size_t(255);
+  L.bytes = L.offsets_bytes + sizeof(uint64_t) * (size_t)R * (size_t)N;
   return L;
 }
 
 }  // namespace
 
-size_t batched_workspace_bytes(int R, int N) { return pool_layout(R, N).bytes; }
+size_t batched_workspace_bytes(int R, int rows, int N) { return pool_layout(R, rows, N).bytes; }
 
 cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, const uint32_t* mask, int R, int N,
-                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolSegments* out) {
-  const PoolLayout L = pool_layout(R, rows);
-  int* counts = static_cast<int*>(ws);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + L.counts_bytes);
-  *out = PoolSegments{cand, counts, L.P * kGroups, L.cap, L.P, L.tiles};
+                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolLists* out) {
+  const PoolLayout L = pool_layout(R, rows, N);
+  int* offsets = static_cast<int*>(ws);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + L.offsets_bytes);
+  *out = PoolLists{keys, offsets, L.mtiles, (long long)N};
   if (R == 0) return cudaSuccess;
   cudaError_t e = setup_gemm();
   if (e != cudaSuccess) return e;
+  const int mask_words = (N + 31) / 32;
+  pool_offsets_kernel<<<R, kSelThreads, 0, s>>>(mask, N, mask_words, L.mtiles, offsets);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.P > 0) {
     CUtensorMap ma, mv;
     if (!make_map(&ma, A, R) || !make_map(&mv, V, rows)) return cudaErrorInvalidValue;
-    const int mask_words = (N + 31) / 32;
     const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
-    GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, coarse, counts, cand, L.cap, mask_vec, err};
-    if (g.coarse_tiles > 0)
-      score_pool_kernel<true><<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
-    else
-      score_pool_kernel<false><<<L.MT * L.P, kGemmThreads, kGemmSmem, s>>>(ma, mv, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, coarse, offsets, L.mtiles, keys,
+               mask_vec, err};
+    // programmatic dependent launch: the GEMM's producer and MMA start while
+    // the offsets kernel runs; the epilogue waits for it (griddepcontrol.wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(L.MT * L.P));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = g.coarse_tiles > 0 ? cudaLaunchKernelEx(&cfg, score_pool_kernel<true>, ma, mv, g)
+                           : cudaLaunchKernelEx(&cfg, score_pool_kernel<false>, ma, mv, g);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -889,8 +889,8 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
                                       int N, int K, int* idx, float* top, void* ws, int* err,
                                       cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  PoolSegments seg;
-  cudaError_t e = launch_pool_gemm(A, V, N, mask, R, N, 0, nullptr, ws, err, s, &seg);
+  PoolLists lists;
+  cudaError_t e = launch_pool_gemm(A, V, N, mask, R, N, 0, nullptr, ws, err, s, &lists);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the select grid is scheduled while the
   // GEMM drains and waits (griddepcontrol.wait) for its results
@@ -904,7 +904,7 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const SelArgs sa{seg.cand, seg.counts, seg.segs, seg.cap, K, idx, top, err};
+  const SelArgs sa{lists.keys, lists.offsets, lists.mtiles, lists.cap, K, idx, top, err};
   return cudaLaunchKernelEx(&cfg, select_rows_kernel, sa);
 }
 

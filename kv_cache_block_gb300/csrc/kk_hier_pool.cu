@@ -32,7 +32,6 @@ constexpr int kRepSlots = kRepThreads / (kCols / 8);
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPageStage = 4096;  // active blocks of an anchor listed in shared memory
-constexpr int kChunkMap = 1024;   // 32-key chunks of a row mapped to their first segment
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   uint16_t h;
@@ -103,7 +102,7 @@ __global__ void __launch_bounds__(kRepThreads) pool_reps_kernel(uint16_t* M, int
 }
 
 struct HierPoolArgs {
-  PoolSegments seg;
+  PoolLists lists;
   const float* coarse;   // [R][H] scores of the coarse rows
   const uint32_t* mask;  // [R][ceil(N/32)]
   int N, G, C, H, cp, gc;
@@ -187,15 +186,10 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
   __shared__ uint32_t s_gall[kHierPoolCoarseMax / 32];  // Grids covering an allowed block
   __shared__ uint32_t s_ckept[kHierPoolCoarseMax / 32];
   __shared__ uint32_t s_gkept[kHierPoolCoarseMax / 32];
-  __shared__ int s_cnt[kPoolMaxSegs];
-  __shared__ int s_off[kPoolMaxSegs];
-  __shared__ int s_chunk_seg[kChunkMap];  // segment holding position 32 * c
   __shared__ int hist[256], s_pick[2], s_tmp[kWarps], s_np, s_nout;
   __shared__ uint64_t s_out[kMaxK];
-  __shared__ uint64_t s_wl[kWarps][32];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = a.G, C = a.C, N = a.N, segs = a.seg.segs;
-  const long long cap = a.seg.cap;
+  const int G = a.G, C = a.C, N = a.N;
   const int nco = G + C;
   const int cwords = (C + 31) / 32, gwords = (G + 31) / 32;
   for (int w = tid; w < cwords; w += kThreads) {
@@ -225,44 +219,11 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
 
   // the keys come from the GEMM grid launched just before this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint64_t* row = a.seg.cand + (long long)r * segs * cap;
-  // segment counts and their offsets in the row's compact order: each thread
-  // scans a run of up to four segments, then the block
-  int ntot = 0;
-  {
-    const int spt = (segs + kThreads - 1) / kThreads;  // <= 4
-    const int s0 = min(segs, tid * spt), s1 = min(segs, s0 + spt);
-    int mine = 0;
-    for (int p = s0; p < s1; ++p) {
-      int c = a.seg.counts[(long long)r * segs + p];
-      if (c < 0 || c > cap) {
-        flag_error(a.err, kErrBadIndex);
-        c = c < 0 ? 0 : (int)cap;
-      }
-      s_cnt[p] = c;
-      mine += c;
-    }
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_tmp[warp] = incl;
-    __syncthreads();
-    int base = incl - mine;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < warp) base += s_tmp[w];
-      ntot += s_tmp[w];
-    }
-    for (int p = s0; p < s1; ++p) {
-      s_off[p] = base;
-      if (ntot <= kChunkMap * 32)
-        for (int c = (base + 31) / 32; c * 32 < base + s_cnt[p]; ++c) s_chunk_seg[c] = p;
-      base += s_cnt[p];
-    }
-    __syncthreads();
+  const uint64_t* row = a.lists.keys + (long long)r * a.lists.cap;
+  int ntot = a.lists.offsets[(long long)r * (a.lists.mtiles + 1) + a.lists.mtiles];
+  if (ntot < 0 || ntot > a.lists.cap) {
+    if (tid == 0) flag_error(a.err, kErrBadIndex);
+    ntot = ntot < 0 ? 0 : (int)a.lists.cap;
   }
   // the coarse rows' scores, as keys (score, row)
   for (int x = tid; x < nco; x += kThreads) s_cs[x] = a.coarse[(long long)r * a.H + x];
@@ -300,40 +261,20 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
     const long long i = (long long)key_index(k) - a.H;
     return i >= 0 && i < N && bit(s_ckept, (int)(i / a.cp));
   };
-  // Warp w takes the 32-key chunks [w*W, (w+1)*W) of the row's compact
-  // order, lane l the l-th
-  // key of each (coalesced), eight chunks' loads in flight; a chunk's first
-  // segment comes from s_chunk_seg (rows of up to kChunkMap chunks) or from a
-  // search.
-  const int W = ((ntot + 31) / 32 + kWarps - 1) / kWarps;  // chunks per warp
-  const bool mapped = ntot <= kChunkMap * 32;
-  auto seg_of_chunk = [&](int c) {
-    if (mapped) return s_chunk_seg[c];
-    int sg = 0;
-    for (int step = kPoolMaxSegs / 2; step > 0; step >>= 1)
-      if (sg + step < segs && s_off[sg + step] <= c * 32) sg += step;
-    return sg;
-  };
-  // visits this lane's positions: fn(active, key) for each
+  // Each thread takes keys tid, tid + 256, ... of the anchor's list
+  // (coalesced), eight loads in flight.
   auto visit_run = [&](auto&& fn) {
     constexpr int kBatch = 8;
-    for (int u0 = 0; u0 < W; u0 += kBatch) {
+    for (int p0 = tid; p0 < ntot; p0 += kBatch * kThreads) {
       uint64_t v[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int c = warp * W + u0 + u, pos = c * 32 + lane;
-        v[u] = 0ull;
-        if (u0 + u < W && pos < ntot) {
-          int sg = seg_of_chunk(c);
-          while (pos >= s_off[sg] + s_cnt[sg]) ++sg;
-          v[u] = row[sg * cap + (pos - s_off[sg])];
-        }
+        const int pos = p0 + u * kThreads;
+        v[u] = pos < ntot ? row[pos] : 0ull;
       }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int c = warp * W + u0 + u;
-        if (u0 + u < W && c * 32 + lane < ntot) fn(page_active(v[u]), v[u]);
-      }
+      for (int u = 0; u < kBatch; ++u)
+        if (p0 + u * kThreads < ntot) fn(page_active(v[u]), v[u]);
     }
   };
   visit_run([&](bool act, uint64_t k) {
@@ -364,21 +305,22 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
     });
     __syncthreads();
   }
-  // ---- the m winners in order: warp-sorted lists of 32, then merge ranks
+  // ---- the m winners in order: a key's place is the number of winners
+  // above it (each thread reads the list in step, so the loads broadcast)
   const int got = min(s_nout, kMaxK);
   if (tid == 0 && got != m) flag_error(a.err, kErrBadIndex);  // the select lost or gained a key
-  uint64_t mine = tid < min(m, got) ? s_out[tid] : 0ull;
-  mine = warp_sort_desc(mine, lane);
-  s_wl[warp][lane] = mine;
-  __syncthreads();
   int* io = a.idx + (long long)r * a.K;
   float* to = a.top ? a.top + (long long)r * a.K : nullptr;
-  int rank = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) rank += count_greater_pow2(s_wl[w], 32, mine);
-  if (mine != 0ull && rank < a.K) {
-    io[rank] = (int)(key_index(mine) - (uint32_t)a.H);
-    if (to) to[rank] = key_score(mine);
+  const int mm = min(m, got);
+  if (tid < mm) {
+    const uint64_t mine = s_out[tid];
+    int rank = 0;
+#pragma unroll 8
+    for (int q = 0; q < mm; ++q) rank += s_out[q] > mine ? 1 : 0;
+    if (rank < a.K) {
+      io[rank] = (int)(key_index(mine) - (uint32_t)a.H);
+      if (to) to[rank] = key_score(mine);
+    }
   }
   for (int i = m + tid; i < a.K; i += kThreads) {
     io[i] = -1;
@@ -391,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) hier_pool_select_kernel(const HierPo
 
 size_t hier_pool_workspace_bytes(int R, int N, int cp, int gc) {
   const int H = hier_pool_coarse_rows(N, cp, gc);
-  const size_t gemm = (batched_workspace_bytes(R, H + N) + 255) & ~size_t(255);
+  const size_t gemm = (batched_workspace_bytes(R, H + N, N) + 255) & ~size_t(255);
   return gemm + sizeof(float) * (size_t)R * (size_t)H;
 }
 
@@ -415,10 +357,10 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
   if (R == 0) return cudaSuccess;
   const int C = N > 0 ? (N + cp - 1) / cp : 0, G = C > 0 ? (C + gc - 1) / gc : 0;
   const int H = hier_pool_coarse_rows(N, cp, gc);
-  PoolSegments seg;
+  PoolLists lists;
   float* coarse = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                           ((batched_workspace_bytes(R, H + N) + 255) & ~size_t(255)));
-  cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, coarse, ws, err, s, &seg);
+                                           ((batched_workspace_bytes(R, H + N, N) + 255) & ~size_t(255)));
+  cudaError_t e = launch_pool_gemm(A, M, H + N, mask, R, N, G + C, coarse, ws, err, s, &lists);
   if (e != cudaSuccess) return e;
   constexpr int kDyn = (int)(sizeof(uint64_t) * kPageStage + sizeof(float) * kHierPoolCoarseMax);
   static std::mutex mu;
@@ -436,7 +378,7 @@ cudaError_t launch_hier_select_pool(const uint16_t* A, const uint16_t* M, const 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  HierPoolArgs ha{seg, coarse, mask, N, G, C, H, cp, gc, {permille[0], permille[1], permille[2]}, K, idx, top, kept, err};
+  HierPoolArgs ha{lists, coarse, mask, N, G, C, H, cp, gc, {permille[0], permille[1], permille[2]}, K, idx, top, kept, err};
   // programmatic dependent launch: scheduled while the GEMM drains
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)R);

@@ -79,28 +79,22 @@ struct StepParams {
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 
 // kk_batched.cu
-// Shared-pool GEMM (kk_batched.cu): the candidate keys of each anchor, one
-// segment per (anchor, GEMM CTA, epilogue group) holding `counts` keys
-// (score, row) in row order. V has `rows` rows: `rows - N` coarse rows (a
-// multiple of 128, scored for every anchor into `coarse`, float [R][rows -
-// N], dense, no keys), then the N pool blocks, which the mask (uint32
-// [R][ceil(N/32)]) filters; `coarse_rows` of the coarse rows are real.
-// GEMM CTA p (of P per anchor tile) takes the 128-row tiles p, p + P, ...,
-// its j-th tile going to group g when g*n/4 <= j < (g+1)*n/4 (n = its tiles);
-// segment s belongs to CTA s / 4, group s % 4.
-constexpr int kPoolMaxSegs = 1024;
-constexpr int kPoolGroups = 4;
-struct PoolSegments {
-  const uint64_t* cand;  // [R][segs][cap]
-  const int* counts;     // [R][segs]
-  int segs;              // P * kPoolGroups
+// Shared-pool GEMM (kk_batched.cu): each anchor's candidate keys (score,
+// row), contiguous in pool order, up to `cap` = N of them; offsets[r][mtiles]
+// is the count (offsets[r][t] the keys before block tile t). V has `rows`
+// rows: `rows - N` coarse rows (a multiple of 128, scored for every anchor
+// into `coarse`, float [R][rows - N], dense, no keys), then the N pool
+// blocks, which the mask (uint32 [R][ceil(N/32)]) filters; `coarse_rows` of
+// the coarse rows are real.
+struct PoolLists {
+  const uint64_t* keys;  // [R][cap]
+  const int* offsets;    // [R][mtiles + 1]
+  int mtiles;            // 128-block tiles of the pool
   long long cap;
-  int P;                 // GEMM CTAs per anchor tile
-  int tiles;             // 128-row tiles of V
 };
-size_t batched_workspace_bytes(int R, int N);
+size_t batched_workspace_bytes(int R, int rows, int N);
 cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, const uint32_t* mask, int R, int N,
-                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolSegments* out);
+                             int coarse_rows, float* coarse, void* ws, int* err, cudaStream_t s, PoolLists* out);
 // Shared-pool hierarchy (kk_hier_pool.cu): coarse rows in front of the pool
 // (Grids, Chunks, zero padding to a multiple of 128), at most
 // kHierPoolCoarseMax Grids + Chunks.
