@@ -782,27 +782,44 @@ cudaError_t setup_gemm() {
 // of tiles per thread, then a block scan. This is where the GEMM's epilogue
 // writes each tile's keys in the anchor's contiguous list.
 __global__ void __launch_bounds__(kSelThreads) pool_offsets_kernel(const uint32_t* mask, int N, int mask_words,
-                                                                   int mtiles, int* offsets) {
+                                                                   int mtiles, int mask_vec, int* offsets) {
+  constexpr int kTilesPerThread = 4;  // a run of tiles loaded together (more: a second round)
   __shared__ int s_wsum[kSelThreads / 32];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t* mrow = mask + (long long)r * mask_words;
   int* orow = offsets + (long long)r * (mtiles + 1);
+  // owned blocks of tile t: its four mask words (one 16-byte load when the
+  // rows allow it), bits past N dropped
   auto tile_count = [&](int t) {
+    uint32_t w[4];
+    if (mask_vec) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(mrow) + t);
+      w[0] = x.x;
+      w[1] = x.y;
+      w[2] = x.z;
+      w[3] = x.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[q] = t * 4 + q < mask_words ? __ldg(mrow + t * 4 + q) : 0u;
+    }
     int c = 0;
 #pragma unroll
-    for (int q = 0; q < kBN / 32; ++q) {
-      const int wi = t * (kBN / 32) + q;
-      const int lim = N - wi * 32;
-      if (lim <= 0) break;
-      const uint32_t x = __ldg(mrow + wi);
-      c += __popc(lim >= 32 ? x : (x & ((1u << lim) - 1u)));
+    for (int q = 0; q < 4; ++q) {
+      const int lim = N - (t * 4 + q) * 32;
+      c += lim <= 0 ? 0 : __popc(lim >= 32 ? w[q] : (w[q] & ((1u << lim) - 1u)));
     }
     return c;
   };
   const int per = (mtiles + kSelThreads - 1) / kSelThreads;
   const int t0 = min(mtiles, tid * per), t1 = min(mtiles, t0 + per);
+  int cnt[kTilesPerThread];
   int mine = 0;
-  for (int t = t0; t < t1; ++t) mine += tile_count(t);
+#pragma unroll
+  for (int u = 0; u < kTilesPerThread; ++u) {
+    cnt[u] = t0 + u < t1 ? tile_count(t0 + u) : 0;
+    mine += cnt[u];
+  }
+  for (int t = t0 + kTilesPerThread; t < t1; ++t) mine += tile_count(t);
   int incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -817,7 +834,14 @@ __global__ void __launch_bounds__(kSelThreads) pool_offsets_kernel(const uint32_
     if (w < warp) base += s_wsum[w];
     total += s_wsum[w];
   }
-  for (int t = t0; t < t1; ++t) {
+#pragma unroll
+  for (int u = 0; u < kTilesPerThread; ++u) {
+    if (t0 + u < t1) {
+      orow[t0 + u] = base;
+      base += cnt[u];
+    }
+  }
+  for (int t = t0 + kTilesPerThread; t < t1; ++t) {
     orow[t] = base;
     base += tile_count(t);
   }
@@ -858,12 +882,12 @@ cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, con
   cudaError_t e = setup_gemm();
   if (e != cudaSuccess) return e;
   const int mask_words = (N + 31) / 32;
-  pool_offsets_kernel<<<R, kSelThreads, 0, s>>>(mask, N, mask_words, L.mtiles, offsets);
+  const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
+  pool_offsets_kernel<<<R, kSelThreads, 0, s>>>(mask, N, mask_words, L.mtiles, mask_vec, offsets);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.P > 0) {
     CUtensorMap ma, mv;
     if (!make_map(&ma, A, R) || !make_map(&mv, V, rows)) return cudaErrorInvalidValue;
-    const int mask_vec = (mask_words % 4 == 0 && reinterpret_cast<uintptr_t>(mask) % 16 == 0) ? 1 : 0;
     GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, coarse, offsets, L.mtiles, keys,
                mask_vec, err};
     // programmatic dependent launch: the GEMM's producer and MMA start while
