@@ -299,10 +299,9 @@ kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk
  * of the bf16 values; per anchor the top K pool ids (ordered as kk_topk) go
  * to idx [R][K] and top_scores [R][K] (nullable). D = 128, 1 <= K <= 256.
  * workspace: caller-owned device memory, 256-byte aligned, of at least
- * kk_score_pool_batched_workspace_bytes(R, N, K) bytes (about 8 to 10 * R * N plus
- * counts); the size depends on the SM count of the current device, so query
- * it with the device that will run the call current. Concurrent calls need
- * separate workspaces.
+ * kk_score_pool_batched_workspace_bytes(R, N, K) bytes (8 * R * N bytes of
+ * candidate keys plus R * (ceil(N/128) + 1) int32 offsets). Concurrent calls
+ * need separate workspaces.
  */
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K);
 kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint32_t* mask,
@@ -339,8 +338,8 @@ kk_status kk_score_pool_batched(const uint16_t* A, const uint16_t* V, const uint
  * exceed K). 1 <= K <= 256, permille in 1..1000, D = 128, G + C <= 4096.
  * workspace: device memory, 256-byte aligned, of at least
  * kk_hier_select_pool_workspace_bytes(R, N, chunk_pages, grid_chunks) bytes
- * (depends on the SM count of the current device); concurrent calls need
- * separate workspaces. Returns KK_ERR_UNSUPPORTED beyond the limits above.
+ * (the flat call's plus 4 * R * H for the coarse scores); concurrent calls
+ * need separate workspaces. Returns KK_ERR_UNSUPPORTED beyond the limits above.
  */
 int32_t kk_hier_pool_coarse_rows(int32_t N, int32_t chunk_pages, int32_t grid_chunks);
 kk_status kk_hier_pool_reps(uint16_t* M, int32_t N, int32_t D, int32_t chunk_pages, int32_t grid_chunks,
