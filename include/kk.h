@@ -24,6 +24,11 @@
  *    float32, accumulated in float32.
  *  - The first call on a device looks up the device error word's address;
  *    make that first call outside CUDA stream capture.
+ *  - The decode-step calls (kk_select_step, kk_score_topk, kk_topk and their
+ *    stable forms) may split each of up to 64 very long requests over several
+ *    clusters of CTAs, which meet in a fixed 512 KB device buffer of the
+ *    library: on one device, issue those calls in stream order (one stream,
+ *    or streams ordered by events), never two at once.
  */
 #ifndef KK_H_
 #define KK_H_

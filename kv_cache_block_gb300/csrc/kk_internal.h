@@ -75,6 +75,7 @@ struct StepParams {
   int stab_w;
   float stab_theta;
   int* err;
+  int splits;  // clusters per request (set by the launcher; > 1 for very long requests)
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 

@@ -11,6 +11,7 @@
 // its own candidates in the union and writes them. A whole step is one launch
 // with no global scratch. Every stage can be switched off, which gives
 // kk_anchor, kk_score, kk_topk and kk_score_topk from the same code.
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -20,10 +21,20 @@
 namespace kk {
 namespace {
 
+// Very long requests are split over several clusters: each writes its sorted
+// top-K list here, and the last one to finish (a per-request counter) merges
+// the lists into the request's output and resets the counter. Calls that
+// split a request share this scratch, so they must not run concurrently.
+constexpr int kSplitKeys = 65536;  // requests x splits x Kp
+constexpr int kSplitReq = 64;      // requests
+__device__ uint64_t g_split_keys[kSplitKeys];
+__device__ int g_split_count[kSplitReq];
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kThreads;  // candidates per top-K tile
 constexpr int kStage = 64;  // v_b rows staged in shared memory by bulk copies
+static_assert(kMergeSlots % kThreads == 0, "the split merge holds kMergeSlots / kThreads keys a thread");
 
 template <int D>
 struct StepSmem {
@@ -125,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   StepSmem<D>& sm = *reinterpret_cast<StepSmem<D>*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = blockIdx.y;
+  const int S = p.splits;  // clusters per request
+  const int r = blockIdx.y / S, sp = blockIdx.y - r * S;
   const int CL = (int)cluster_size();
   const int crank = CL > 1 ? (int)cluster_rank() : 0;
   const bool do_anchor = p.flags & kStepAnchor;
@@ -159,9 +171,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     nb = 0;
     T_r = 0;
   }
-  const int chunk = (nb + CL - 1) / CL;
-  const int j0 = min(nb, crank * chunk);
-  const int j1 = min(nb, j0 + chunk);
+  // this cluster's blocks (split sp of S), then this CTA's share of them
+  const int span = (nb + S - 1) / S;
+  const int s0 = min(nb, sp * span), sn = min(nb, s0 + span) - s0;
+  const int chunk = (sn + CL - 1) / CL;
+  const int j0 = s0 + min(sn, crank * chunk);
+  const int j1 = s0 + min(sn, crank * chunk + chunk);
 
   // ---- prefetch: one round of page-id loads for the anchor's token rows and
   // the first tile's blocks, then bulk copies of that tile's v_b rows -------
@@ -304,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       for (int q = 0; q < CL; ++q) v += sm.part[q][tid];
       v *= scale;
       sm.va[tid] = v;
-      if (crank == 0 && p.va_out) p.va_out[(long long)r * D + tid] = v;
+      if (crank == 0 && sp == 0 && p.va_out) p.va_out[(long long)r * D + tid] = v;
     }
     __syncthreads();
   } else if (do_score) {
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   // Few blocks per CTA: no per-CTA list; stage 3 all-gathers the raw keys
   // and every CTA ranks its own by counting.
   constexpr int kDirectMax = 64;
-  const bool direct = do_topk && CL > 1 && chunk <= kDirectMax;
+  const bool direct = do_topk && CL > 1 && S == 1 && chunk <= kDirectMax;
   if (do_topk)
     for (int i = tid; i < Kp; i += kThreads) sm.run[0][i] = 0ull;
   if (do_score || from_scores) {
@@ -481,13 +496,30 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   if (do_topk) {
     int* idx_out = p.idx_out + (long long)r * K;
     float* top_out = p.top_out ? p.top_out + (long long)r * K : nullptr;
-    if (CL == 1) {
-      for (int i = tid; i < K; i += kThreads) {
-        const bool have = i < run_n;
-        const uint64_t k = have ? sm.run[cur][i] : 0ull;
-        idx_out[i] = have ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
-        if (top_out) top_out[i] = have ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
+    // the place of a ranked key: the request's output, or (a split request)
+    // this cluster's sorted list in the scratch
+    uint64_t* slist = S > 1 ? g_split_keys + ((long long)r * S + sp) * Kp : nullptr;
+    auto emit = [&](int rank, uint64_t k) {
+      if (slist) {
+        slist[rank] = k;
+      } else {
+        idx_out[rank] = (int)(stab ? stab_key_index(k) : key_index(k));
+        if (top_out) top_out[rank] = stab ? stab_key_score(k) : key_score(k);
       }
+    };
+    auto pad = [&](int from) {
+      if (slist) {
+        for (int i = from + tid; i < Kp; i += kThreads) slist[i] = 0ull;
+      } else {
+        for (int i = from + tid; i < K; i += kThreads) {
+          idx_out[i] = -1;
+          if (top_out) top_out[i] = -__int_as_float(0x7f800000);
+        }
+      }
+    };
+    if (CL == 1) {
+      for (int i = tid; i < run_n; i += kThreads) emit(i, sm.run[cur][i]);
+      pad(run_n);
     } else if (direct) {
       if (!start_waited) {
         cluster_wait_acquire();
@@ -557,17 +589,71 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         const uint64_t k = have ? sm.merge[crank * Kp + c] : ~0ull;
         int cnt = count_greater_pow2(&sm.merge[list * Kp], Kp, k);
         for (int o = 1; o < CL; o <<= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
-        if (have && list == 0 && cnt < K) {
-          idx_out[cnt] = (int)(stab ? stab_key_index(k) : key_index(k));
-          if (top_out) top_out[cnt] = stab ? stab_key_score(k) : key_score(k);
-        }
+        if (have && list == 0 && cnt < K) emit(cnt, k);
       }
       if (crank == 0) {
         int total = 0;
         for (int q = 0; q < CL; ++q) total += sm.mcount[q];
-        for (int i = total + tid; i < K; i += kThreads) {
-          idx_out[i] = -1;
-          if (top_out) top_out[i] = -__int_as_float(0x7f800000);
+        pad(min(total, K));
+      }
+    }
+    if (S > 1) {
+      // Every CTA has written its part of this cluster's list: fence, meet,
+      // then one thread counts this cluster in. The last cluster of the
+      // request merges the S sorted lists and resets the counter.
+      __threadfence();
+      if (CL > 1) {
+        if (!start_waited) {
+          cluster_wait_acquire();
+          start_waited = true;
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+      } else {
+        __syncthreads();
+      }
+      if (crank == 0) {
+        if (tid == 0) sm.wn[0] = atomicAdd(&g_split_count[r], 1) == S - 1 ? 1 : 0;
+        __syncthreads();
+        if (sm.wn[0]) {
+          __threadfence();
+          const uint64_t* lists = g_split_keys + (long long)r * S * Kp;
+          for (int f = tid; f < S * Kp; f += kThreads) sm.merge[f] = __ldcg(lists + f);
+          __syncthreads();
+          // pairwise rounds: lists q and q ^ 1 become list q / 2, cut to Kp
+          // keys (the top K of a union lies in the union of its parts' top K);
+          // a key's place in the pair is its own position plus the number of
+          // larger keys in the other list
+          constexpr int kPer = kMergeSlots / kThreads;  // keys a thread holds
+          const int kp_log = __ffs(Kp) - 1;
+          for (int n = S; n > 1; n = (n + 1) >> 1) {
+            uint64_t key[kPer];
+            int at[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+              const int f = tid + u * kThreads;
+              key[u] = f < (n << kp_log) ? sm.merge[f] : 0ull;
+              at[u] = -1;
+              if (key[u] != 0ull) {
+                const int q = f >> kp_log, o = q ^ 1;
+                const int rank = (f & (Kp - 1)) + (o < n ? count_greater_pow2(&sm.merge[o << kp_log], Kp, key[u]) : 0);
+                if (rank < Kp) at[u] = ((q >> 1) << kp_log) + rank;
+              }
+            }
+            __syncthreads();
+            for (int f = tid; f < (((n + 1) >> 1) << kp_log); f += kThreads) sm.merge[f] = 0ull;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kPer; ++u)
+              if (at[u] >= 0) sm.merge[at[u]] = key[u];
+            __syncthreads();
+          }
+          for (int i = tid; i < K; i += kThreads) {
+            const uint64_t k = sm.merge[i];
+            idx_out[i] = k ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
+            if (top_out) top_out[i] = k ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
+          }
+          if (tid == 0) g_split_count[r] = 0;
         }
       }
     }
@@ -632,9 +718,10 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
   const int Kp = p.K <= 1 ? 1 : 1 << (32 - __builtin_clz(p.K - 1));
   // Measured on GB300: past 8 CTAs the cluster's list exchange costs more
   // than the extra SMs return (7B: 10.5 us at 8 vs 11.3 at 16; 8 x 1024
-  // blocks: 13.7 vs 18.5), except for a few very long requests that would
-  // otherwise leave most SMs idle.
-  const int cap = ((long long)p.bt.R * kMaxCluster <= sm_count() && p.bt.max_blocks >= 4096) ? kMaxCluster : 8;
+  // blocks: 13.7 vs 18.5). A few very long requests take more SMs by
+  // splitting over several clusters instead (one request of 65536 blocks:
+  // 28.5 us at 16 CTAs x 16 clusters, 24.1 at 8 x 32).
+  const int cap = 8;
   int best = 1;
   for (int cl = 2; cl <= cap; cl <<= 1) {
     if (caps.active[cl] < p.bt.R) break;
@@ -645,14 +732,32 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
   return best;
 }
 
+// Clusters per request: a few long requests leave most SMs idle at one
+// cluster each, so their blocks are split over as many clusters as stay
+// resident together, each keeping at least kSplitMinBlocks blocks per CTA
+// (every cluster recomputes the anchor), within the scratch and the final
+// merge buffer.
+int pick_splits(const StepParams& p, const ClusterCaps& caps, int CL) {
+  constexpr int kSplitMinBlocks = 256;
+  if (!(p.flags & (kStepScore | kStepTopK)) || p.bt.R > kSplitReq) return 1;
+  const int Kp = p.K <= 1 ? 1 : 1 << (32 - __builtin_clz(p.K - 1));
+  int S = caps.active[CL] / p.bt.R;
+  S = std::min(S, p.bt.max_blocks / (CL * kSplitMinBlocks));
+  S = std::min(S, kMergeSlots / Kp);
+  S = std::min(S, kSplitKeys / (p.bt.R * Kp));
+  return std::max(S, 1);
+}
+
 template <typename T, int D>
-cudaError_t launch_typed(const StepParams& p, cudaStream_t s) {
+cudaError_t launch_typed(const StepParams& p0, cudaStream_t s) {
   ClusterCaps caps;
   cudaError_t e = setup_device<T, D>(&caps);
   if (e != cudaSuccess) return e;
+  StepParams p = p0;
   const int CL = pick_cluster(p, caps);
+  p.splits = pick_splits(p, caps, CL);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, p.bt.R);
+  cfg.gridDim = dim3(CL, p.bt.R * p.splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = sizeof(StepSmem<D>);
   cfg.stream = s;

@@ -160,6 +160,38 @@ def test_write_stress_pool_and_coarse(kk, bs):
     _free()
 
 
+def test_write_stress_select_step(kk):
+    """One request of 65536 blocks (2^20 tokens at block size 16): long
+    enough that its blocks are split over several clusters, the last of
+    which merges their lists. The anchor against the oracle's over the last
+    W tokens, sampled scores against the oracle's, and the top-K exactly the
+    ranking of the returned scores, the same on repeated calls."""
+    dev = DeviceCache(synth.write_stress(16))
+    sp = dev.spec
+    vb = _pool_all(kk, dev)
+    idx, top, va, scores = _step(kk, dev, vb)
+    T, nb = sp.seq_lens[0], sp.nb[0]
+    last = np.arange((T - min(sp.W, T)) // sp.bs, nb)
+    local = np.zeros(nb, dtype=np.int64)
+    local[last] = np.arange(len(last))
+    va_o = ko.anchor(dev.host_pages(sp.pages[last]), local, T, sp.bs, sp.W)
+    assert_vec_close(va[0], va_o, "write16 va")
+    rng = np.random.default_rng(16)
+    blocks = np.unique(np.concatenate([[0, nb - 1], rng.choice(nb, 40, replace=False), idx[0][:8]]))
+    vb_o = ko.pool_blocks(dev.host_pages(sp.pages[blocks]), np.arange(len(blocks)), sp.n_valid[blocks])
+    assert_scores_close(scores[blocks], ko.affinity(vb_o, va_o), "write16 sampled scores")
+    want_idx, want_val = ko.topk(scores[:nb], sp.K)
+    np.testing.assert_array_equal(idx[0], want_idx)
+    np.testing.assert_array_equal(top[0], want_val.astype(np.float32))
+    _check_planted(dev, idx)
+    for _ in range(3):
+        idx2, top2, _, _ = _step(kk, dev, vb)
+        np.testing.assert_array_equal(idx2, idx)
+        np.testing.assert_array_equal(top2, top)
+    del dev, vb
+    _free()
+
+
 def test_shared_pool_full(kk):
     from tests.test_gpu_parity import check_batched_against_oracle
 

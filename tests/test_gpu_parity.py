@@ -194,6 +194,30 @@ def test_topk_exact_with_ties_and_many_tiles(kk):
             np.testing.assert_array_equal(top.cpu().numpy()[r], want_val.astype(np.float32))
 
 
+@pytest.mark.parametrize("sizes", [[65536], [100003, 0, 70001], [40000, 30000, 1], [9000] * 5 + [300000]])
+def test_topk_split_long_requests(kk, sizes):
+    """Requests long enough that their candidates are split over several
+    clusters (each ranks its share; the last to finish merges the lists):
+    exact against the oracle with many ties, an empty and a one-candidate
+    request among them, K up to 256, and repeated calls (the per-request
+    arrival counters must be back at zero after every call)."""
+    rng = np.random.default_rng(len(sizes) * 7 + sizes[0])
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    scores = rng.integers(0, 4000, size=offsets[-1]).astype(np.float32) / 4000
+    s_gpu = torch.from_numpy(scores).cuda()
+    off_gpu = torch.from_numpy(offsets).cuda()
+    for K in (1, 100, 256):
+        want = [ko.topk(scores[offsets[r]:offsets[r + 1]], K) for r in range(len(sizes))]
+        for rep in range(3):
+            idx = torch.full((len(sizes), K), 7, dtype=torch.int32, device="cuda")
+            top = torch.zeros((len(sizes), K), device="cuda")
+            kk.kk_topk(s_gpu, off_gpu, max(sizes), K, idx, top)
+            assert kk.kk_device_error() == 0
+            for r in range(len(sizes)):
+                np.testing.assert_array_equal(idx.cpu().numpy()[r], want[r][0], err_msg=f"r={r} K={K} call {rep}")
+                np.testing.assert_array_equal(top.cpu().numpy()[r], want[r][1].astype(np.float32))
+
+
 def test_coarse_means(kk, dev):
     sp = dev.spec
     rows = synth.RowsSpec(N=sp.num_pages, D=sp.D, num_topics=3, scale=1.0, sigma=0.5, seed=12, stream=6)
