@@ -3,19 +3,21 @@
 // masked): R anchors against N pooled block vectors, each anchor restricted to
 // the blocks its mask marks, top K per anchor.
 //
-// Kernel 1 is a persistent tcgen05 GEMM: TMA streams 128-block tiles of V
-// (128-byte swizzle) past a resident 128-anchor tile of A, one thread issues
-// eight 128x128x16 bf16 MMAs per tile into one of four TMEM fp32
-// accumulators, and four epilogue groups of four warps read them back
-// (tcgen05.ld), divide by the norms (computed from the same shared-memory
-// tiles), apply the ownership mask and write each owned candidate as a 64-bit
-// key (score, pool id) into the segment of (anchor, CTA, group), with the
-// segment's count (no atomics: one writer each). Rows in front of the pool
-// that every anchor scores (the coarse levels of the hierarchy) are written
-// as a dense score matrix instead. Kernel 2 selects each anchor's top K from
-// its segments (linear buckets over the score range, exact ranking of the
-// boundary bucket, a radix select on the 64-bit keys for massive ties), then
-// sorts the K.
+// Kernel 1 counts each anchor's owned blocks before every 128-block tile
+// (prefix popcounts of the mask). Kernel 2 is a persistent tcgen05 GEMM: TMA
+// streams 128-block tiles of V (128-byte swizzle) past a resident 128-anchor
+// tile of A, one thread issues eight 128x128x16 bf16 MMAs per tile into one
+// of four TMEM fp32 accumulators, and four epilogue groups of four warps read
+// them back (tcgen05.ld), divide by the norms (computed from the same
+// shared-memory tiles), apply the ownership mask and write each owned
+// candidate as a 64-bit key (score, pool id) into the anchor's contiguous
+// list, at the tile's offset from kernel 1 (no atomics: one writer a slot).
+// Rows in front of the pool that every anchor scores (the coarse levels of
+// the hierarchy) are written as a dense score matrix instead. Kernel 3
+// selects each anchor's top K from its list (linear buckets over the score
+// range, exact ranking of the boundary bucket, a radix select on the 64-bit
+// keys for massive ties), then orders the K by counting. The three are
+// chained by programmatic dependent launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -137,7 +139,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (ntiles == 0) return;
   const int m0 = m * kBM;
 
+  // The CTA's local tiles 0 .. ntiles-1 (global tile p + j * P) are split
+  // into four contiguous ranges, one per epilogue group, and each group has
+  // its own TMEM accumulator. The producer and the MMA issuer visit the
+  // ranges round robin (sequence k: group k % 4, its (k / 4)-th tile), so
+  // four tiles drain at once; q counts the tiles issued (its ring stage).
+  auto range_lo = [&](int gg) { return gg * ntiles / kGroups; };
+  auto range_len = [&](int gg) { return (gg + 1) * ntiles / kGroups - gg * ntiles / kGroups; };
+
   if (tid == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmV);
     mbar_init(bar_a, 1);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full[st], 1);
@@ -150,6 +162,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(epi_done, kEpiThreads / 32);
     *s_abort = 0;
     fence_mbar_init();
+    // the A tile goes out before the TMEM allocation and the block barrier
+    // (this thread is the producer)
+    mbar_arrive_expect_tx(bar_a, kTileBytes);
+    tma_load_2d(sA, &tmA, 0, m0, bar_a);
+    tma_load_2d(sA + kBoxBytes, &tmA, 64, m0, bar_a);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -165,19 +182,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     flag_error(g.err, code);
   };
 
-  // The CTA's local tiles 0 .. ntiles-1 (global tile p + j * P) are split
-  // into four contiguous ranges, one per epilogue group, and each group has
-  // its own TMEM accumulator. The producer and the MMA issuer visit the
-  // ranges round robin (sequence k: group k % 4, its (k / 4)-th tile), so
-  // four tiles drain at once; q counts the tiles issued (its ring stage).
-  auto range_lo = [&](int gg) { return gg * ntiles / kGroups; };
-  auto range_len = [&](int gg) { return (gg + 1) * ntiles / kGroups - gg * ntiles / kGroups; };
-
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_a, kTileBytes);
-      tma_load_2d(sA, &tmA, 0, m0, bar_a);
-      tma_load_2d(sA + kBoxBytes, &tmA, 64, m0, bar_a);
       for (int k = 0, q = 0; q < ntiles && !*abort_flag; ++k) {
         const int gg = k % kGroups, i = k / kGroups;
         if (i >= range_len(gg)) continue;
@@ -785,6 +791,9 @@ __global__ void __launch_bounds__(kSelThreads) pool_offsets_kernel(const uint32_
                                                                    int mtiles, int mask_vec, int* offsets) {
   constexpr int kTilesPerThread = 4;  // a run of tiles loaded together (more: a second round)
   __shared__ int s_wsum[kSelThreads / 32];
+  // the GEMM may be scheduled now: only its epilogue reads these offsets,
+  // after waiting for this grid (griddepcontrol.wait)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t* mrow = mask + (long long)r * mask_words;
   int* orow = offsets + (long long)r * (mtiles + 1);

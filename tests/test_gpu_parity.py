@@ -333,3 +333,45 @@ def test_score_pool_batched_small(kk, R, N, K, owned):
     np.testing.assert_array_equal(results[0][0], results[1][0])
     np.testing.assert_array_equal(results[0][1], results[1][1])
     check_batched_against_oracle(A, V, mask, K, *results[0])
+
+
+@pytest.mark.parametrize("K", [1, 5, 128, 256])
+def test_score_pool_batched_exact_ties(kk, K):
+    """Pools of repeated rows, so whole groups of candidates score exactly
+    alike and the order falls to the lower pool index. (a) Every row is the
+    anchor's own vector: one score for all, so the select goes straight to
+    the radix digits of the 64-bit keys; the top K are the K lowest owned
+    indices. (b) Rows 0..31 mod 256 point away from the anchor, the rest are
+    the anchor's vector: two scores, the boundary bucket holds more ties than
+    are ranked exactly, and the radix select finishes; the top K are the K
+    lowest high rows."""
+    rng = np.random.default_rng(K)
+    R, N = 3, 2048
+    a = rng.standard_normal(128).astype(np.float32)
+    a_bits = (torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    A = np.tile(a_bits, (R, 1))
+    neg = a_bits ^ np.uint16(0x8000)
+    full = np.full((R, N // 32), 0xFFFFFFFF, dtype=np.uint32)
+    cases = []
+    # (a) all rows alike, a random ownership per anchor
+    mask_a = synth.owned_mask(R, N, 700, 17)
+    cases.append((np.tile(a_bits, (N, 1)), mask_a,
+                  [np.flatnonzero((mask_a[r, np.arange(N) // 32] >> (np.arange(N) % 32).astype(np.uint32)) & 1)[:K]
+                   for r in range(R)]))
+    # (b) the low rows are the negated anchor, every block owned
+    low = (np.arange(N) % 256) < 32
+    Vb = np.where(low[:, None], neg[None, :], a_bits[None, :]).astype(np.uint16)
+    cases.append((Vb, full, [np.flatnonzero(~low)[:K]] * R))
+    for V, mask, want in cases:
+        At = torch.from_numpy(A.view(np.int16)).cuda()
+        Vt = torch.from_numpy(V.view(np.int16)).cuda()
+        Mt = torch.from_numpy(mask.view(np.int32)).cuda()
+        ws = torch.empty(kk.kk_score_pool_batched_workspace_bytes(R, N, K), dtype=torch.uint8, device="cuda")
+        idx = torch.full((R, K), 7, dtype=torch.int32, device="cuda")
+        top = torch.zeros((R, K), device="cuda")
+        kk.kk_score_pool_batched(At, Vt, Mt, K, idx, top, ws)
+        assert kk.kk_device_error() == 0
+        g_idx, g_top = idx.cpu().numpy(), top.cpu().numpy()
+        for r in range(R):
+            np.testing.assert_array_equal(g_idx[r], want[r], err_msg=f"row {r}")
+            assert np.all(g_top[r] == g_top[r][0]) and abs(g_top[r][0] - 1.0) < 1e-5
