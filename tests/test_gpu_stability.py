@@ -143,3 +143,46 @@ def test_stable_matches_plain_when_every_block_is_equally_stable(kk):
     assert kk.kk_device_error() == 0
     assert torch.equal(i1, i2) and torch.equal(t1, t2)
     assert np.all(hist.cpu().numpy() == 1)
+
+
+def test_score_topk_stable_long_request_split(kk):
+    """A request of 70000 blocks (split over several clusters of CTAs, the
+    last of which merges their lists) beside a short one, over several steps:
+    sampled scores against the oracle, and the ranking exactly the oracle's
+    (stability, score, index) order of the returned scores, whose threshold
+    decisions both sides take in float32."""
+    sizes = [70000, 300]
+    R, D, K, W, steps = len(sizes), 64, 64, 4, 6
+    n = sum(sizes)
+    rows = synth.RowsSpec(N=n, D=D, num_topics=6, scale=1.0, sigma=0.4, seed=21, stream=7)
+    vb_np = synth.gen_rows_numpy(rows)
+    rng = np.random.default_rng(21)
+    pages = rng.permutation(n).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    vb = torch.from_numpy(vb_np).cuda()
+    bt = kk.BlockTable(torch.from_numpy(pages).cuda(), torch.from_numpy(offsets).cuda(),
+                       torch.tensor(sizes, dtype=torch.int32, device="cuda"), max(sizes))
+    theta = float(np.float32(0.5))
+    hist = torch.zeros(n, dtype=torch.int32, device="cuda")
+    stab = torch.zeros(n, device="cuda")
+    scores = torch.zeros(n, device="cuda")
+    idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    top = torch.zeros((R, K), device="cuda")
+    g_hist = []
+    for t in range(steps):
+        va_np = (rng.standard_normal((R, D)) + 2.0 * rows.cs[rng.integers(0, 6, R)]).astype(np.float32)
+        kk.kk_score_topk_stable(vb, bt, torch.from_numpy(va_np).cuda(), K, W, theta, hist, idx, stab=stab,
+                                top_scores=top, scores=scores)
+        assert kk.kk_device_error() == 0
+        g_sc, g_idx, g_top, g_stab = scores.cpu().numpy(), idx.cpu().numpy(), top.cpu().numpy(), stab.cpu().numpy()
+        g_hist.append(g_sc)
+        for r in range(R):
+            blk = slice(offsets[r], offsets[r + 1])
+            sample = rng.choice(sizes[r], min(200, sizes[r]), replace=False)
+            s_o = ko.affinity(vb_np[pages[blk][sample]], va_np[r].astype(np.float64))
+            assert_scores_close(g_sc[blk][sample], s_o, f"step {t} r={r} sampled scores")
+            st = ko.stability([h[blk] for h in g_hist], W, theta)
+            np.testing.assert_array_equal(g_stab[blk], st.astype(np.float32), err_msg=f"step {t} r={r} stability")
+            want_idx, want_val = ko.stable_topk(st, g_sc[blk], K)
+            np.testing.assert_array_equal(g_idx[r], want_idx, err_msg=f"step {t} r={r}")
+            np.testing.assert_array_equal(g_top[r], want_val.astype(np.float32))
