@@ -27,6 +27,7 @@ namespace {
 // split a request share this scratch, so they must not run concurrently.
 constexpr int kSplitKeys = 65536;  // requests x splits x Kp
 constexpr int kSplitReq = 64;      // requests
+constexpr int kSplitPerWarp = 8;   // lists each warp folds in the final merge of K <= 32
 __device__ uint64_t g_split_keys[kSplitKeys];
 __device__ int g_split_count[kSplitReq];
 
@@ -35,6 +36,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kThreads;  // candidates per top-K tile
 constexpr int kStage = 64;  // v_b rows staged in shared memory by bulk copies
 static_assert(kMergeSlots % kThreads == 0, "the split merge holds kMergeSlots / kThreads keys a thread");
+static_assert(kSplitPerWarp * 32 * kWarps <= kMergeSlots, "the final fold stages its lists in the merge buffer");
 
 template <int D>
 struct StepSmem {
@@ -618,42 +620,79 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         if (sm.wn[0]) {
           __threadfence();
           const uint64_t* lists = g_split_keys + (long long)r * S * Kp;
-          for (int f = tid; f < S * Kp; f += kThreads) sm.merge[f] = __ldcg(lists + f);
-          __syncthreads();
-          // pairwise rounds: lists q and q ^ 1 become list q / 2, cut to Kp
-          // keys (the top K of a union lies in the union of its parts' top K);
-          // a key's place in the pair is its own position plus the number of
-          // larger keys in the other list
-          constexpr int kPer = kMergeSlots / kThreads;  // keys a thread holds
-          const int kp_log = __ffs(Kp) - 1;
-          for (int n = S; n > 1; n = (n + 1) >> 1) {
-            uint64_t key[kPer];
-            int at[kPer];
+          if (Kp <= 32) {
+            // each warp folds lists warp, warp + 8, ... (up to kSplitPerWarp,
+            // loaded together into its shared-memory slots) into one
+            // descending 32-key list, keeping the larger 32 of each pair;
+            // then the eight results fold as a tree (4, 2, 1 warps). The
+            // folds are loops, not unrolled: this code runs once per call,
+            // from a cold instruction cache.
+            uint64_t* mine = &sm.merge[warp * kSplitPerWarp * 32];
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              const int f = tid + u * kThreads;
-              key[u] = f < (n << kp_log) ? sm.merge[f] : 0ull;
-              at[u] = -1;
-              if (key[u] != 0ull) {
-                const int q = f >> kp_log, o = q ^ 1;
-                const int rank = (f & (Kp - 1)) + (o < n ? count_greater_pow2(&sm.merge[o << kp_log], Kp, key[u]) : 0);
-                if (rank < Kp) at[u] = ((q >> 1) << kp_log) + rank;
+            for (int u = 0; u < kSplitPerWarp; ++u) {
+              const int q = warp + u * kWarps;
+              mine[u * 32 + lane] = (q < S && lane < Kp) ? __ldcg(lists + q * Kp + lane) : 0ull;
+            }
+            __syncwarp();
+            const int nl = S > warp ? (S - warp + kWarps - 1) / kWarps : 0;  // this warp's lists
+            uint64_t acc = mine[lane];
+#pragma unroll 1
+            for (int u = 1; u < nl; ++u) acc = warp_merge_top32(acc, mine[u * 32 + lane], lane);
+            sm.wl[warp][lane] = acc;
+#pragma unroll 1
+            for (int h = kWarps / 2; h > 0; h >>= 1) {
+              __syncthreads();
+              if (warp < h) {
+                acc = warp_merge_top32(acc, sm.wl[warp + h][lane], lane);
+                sm.wl[warp][lane] = acc;
               }
             }
+            if (warp == 0) {
+              if (lane < K) {
+                idx_out[lane] = acc ? (int)(stab ? stab_key_index(acc) : key_index(acc)) : -1;
+                if (top_out)
+                  top_out[lane] = acc ? (stab ? stab_key_score(acc) : key_score(acc)) : -__int_as_float(0x7f800000);
+              }
+            }
+            if (tid == 0) g_split_count[r] = 0;
+          } else {
+            for (int f = tid; f < S * Kp; f += kThreads) sm.merge[f] = __ldcg(lists + f);
             __syncthreads();
-            for (int f = tid; f < (((n + 1) >> 1) << kp_log); f += kThreads) sm.merge[f] = 0ull;
-            __syncthreads();
+            // pairwise rounds: lists q and q ^ 1 become list q / 2, cut to Kp
+            // keys (the top K of a union lies in the union of its parts' top K);
+            // a key's place in the pair is its own position plus the number of
+            // larger keys in the other list
+            constexpr int kPer = kMergeSlots / kThreads;  // keys a thread holds
+            const int kp_log = __ffs(Kp) - 1;
+            for (int n = S; n > 1; n = (n + 1) >> 1) {
+              uint64_t key[kPer];
+              int at[kPer];
 #pragma unroll
-            for (int u = 0; u < kPer; ++u)
-              if (at[u] >= 0) sm.merge[at[u]] = key[u];
-            __syncthreads();
+              for (int u = 0; u < kPer; ++u) {
+                const int f = tid + u * kThreads;
+                key[u] = f < (n << kp_log) ? sm.merge[f] : 0ull;
+                at[u] = -1;
+                if (key[u] != 0ull) {
+                  const int q = f >> kp_log, o = q ^ 1;
+                  const int rank = (f & (Kp - 1)) + (o < n ? count_greater_pow2(&sm.merge[o << kp_log], Kp, key[u]) : 0);
+                  if (rank < Kp) at[u] = ((q >> 1) << kp_log) + rank;
+                }
+              }
+              __syncthreads();
+              for (int f = tid; f < (((n + 1) >> 1) << kp_log); f += kThreads) sm.merge[f] = 0ull;
+              __syncthreads();
+#pragma unroll
+              for (int u = 0; u < kPer; ++u)
+                if (at[u] >= 0) sm.merge[at[u]] = key[u];
+              __syncthreads();
+            }
+            for (int i = tid; i < K; i += kThreads) {
+              const uint64_t k = sm.merge[i];
+              idx_out[i] = k ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
+              if (top_out) top_out[i] = k ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
+            }
+            if (tid == 0) g_split_count[r] = 0;
           }
-          for (int i = tid; i < K; i += kThreads) {
-            const uint64_t k = sm.merge[i];
-            idx_out[i] = k ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
-            if (top_out) top_out[i] = k ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
-          }
-          if (tid == 0) g_split_count[r] = 0;
         }
       }
     }
@@ -745,6 +784,7 @@ int pick_splits(const StepParams& p, const ClusterCaps& caps, int CL) {
   S = std::min(S, p.bt.max_blocks / (CL * kSplitMinBlocks));
   S = std::min(S, kMergeSlots / Kp);
   S = std::min(S, kSplitKeys / (p.bt.R * Kp));
+  S = std::min(S, kSplitPerWarp * kWarps);
   return std::max(S, 1);
 }
 
