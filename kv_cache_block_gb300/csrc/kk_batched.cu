@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     score_pool_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmV,
                       GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* base =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned (the 128-byte swizzle atom); offset arithmetic on the
+  // shared array keeps every derived pointer in the shared address space
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* sA = base;               // A tile: two boxes (dims 0-63, 64-127)
   unsigned char* sV = base + kTileBytes;  // kStages V tiles
   float* s_dump = reinterpret_cast<float*>(base + kTileBytes * (1 + kStages));  // [thread][36]
