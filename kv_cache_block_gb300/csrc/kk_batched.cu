@@ -61,6 +61,12 @@ struct GemmArgs {
   int* err;
 };
 
+// Starts fetching a tensor map (a __grid_constant__ kernel parameter) into
+// the TMA unit's descriptor cache, so that the first copy does not wait for it.
+__device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");

@@ -112,20 +112,6 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {
   return x;
 }
 
-// The 32 largest of two descending warp-wide lists (one key per lane, lane 0
-// largest), descending: pairing a[i] with b[31 - i] and keeping the larger
-// gives a bitonic sequence that holds the 32 largest; a bitonic merge sorts it.
-__device__ __forceinline__ uint64_t warp_merge_top32(uint64_t a, uint64_t b, int lane) {
-  const uint64_t br = __shfl_sync(kFull, b, 31 - lane);
-  uint64_t x = a > br ? a : br;
-#pragma unroll
-  for (int j = 16; j > 0; j >>= 1) {
-    const uint64_t o = __shfl_xor_sync(kFull, x, j);
-    x = (lane & j) == 0 ? (x > o ? x : o) : (x < o ? x : o);
-  }
-  return x;
-}
-
 // Number of entries greater than `key` (> 0) in a descending list of distinct
 // keys stored in `cap` slots (cap a power of two), unused slots holding 0.
 // Branch-free with a fixed number of steps, so searches in several lists can

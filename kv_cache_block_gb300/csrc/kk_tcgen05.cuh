@@ -90,11 +90,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---- TMA ------------------------------------------------------------------
-// Starts fetching a tensor map (a __grid_constant__ kernel parameter) into
-// the TMA unit's descriptor cache, so that the first copy does not wait for it.
-__device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
-}
 // 2-D tiled load of the box at (x, y) of `tmap` into shared memory, completing
 // as transaction bytes on `bar`. x (elements) must keep 16-byte alignment.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
