@@ -126,20 +126,63 @@ __device__ __forceinline__ void sort_desc(uint64_t* keys_ptr, int n) {
 }
 
 // The smallest key T such that exactly k of keys[0..n) (distinct, in shared
-// memory) are >= T: a radix select on 8-bit digits, most significant first,
-// stopping as soon as a digit's bucket holds exactly the keys still needed.
-// `hist` is 256 ints of shared memory, `s_sel` two ints; k in [1, n].
+// memory) are >= T. Up to one key a thread: T is the key with k - 1 keys
+// above it (one pass of counting). Longer lists: a radix select on 8-bit
+// digits, the first just below the bits every key shares (found by a min /
+// max pass, so no pass is spent on a digit every key has in common), stopping
+// as soon as a digit's bucket holds exactly the keys still needed. `hist` is
+// 256 ints of shared memory, `s_sel` two ints; k in [1, n].
 __device__ __forceinline__ uint64_t kth_largest(const uint64_t* keys_ptr, int n, int k, int* hist, int* s_sel) {
+  __shared__ uint64_t s_lo[kWarps], s_hi[kWarps], s_res;
   const uint32_t keys = smem_u32(keys_ptr);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint64_t prefix = 0ull, pmask = 0ull;
+  if (n <= kThreads) {
+    if (tid < n) {
+      const uint64_t key = lds_u64(keys + tid * 8);
+      int above = 0;
+#pragma unroll 8
+      for (int q = 0; q < n; ++q) above += lds_u64(keys + q * 8) > key ? 1 : 0;
+      if (above == k - 1) s_res = key;
+    }
+    __syncthreads();
+    const uint64_t res = s_res;
+    __syncthreads();  // s_res is rewritten by the next call
+    return res;
+  }
+  uint64_t lo = ~0ull, hi = 0ull;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint64_t key = lds_u64(keys + i * 8);
+    lo = key < lo ? key : lo;
+    hi = key > hi ? key : hi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t x = __shfl_xor_sync(kFull, lo, o), y = __shfl_xor_sync(kFull, hi, o);
+    lo = x < lo ? x : lo;
+    hi = y > hi ? y : hi;
+  }
+  if (lane == 0) {
+    s_lo[warp] = lo;
+    s_hi[warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = s_lo[w] < lo ? s_lo[w] : lo;
+    hi = s_hi[w] > hi ? s_hi[w] : hi;
+  }
+  if (lo == hi) return lo;
+  const int common = __clzll(lo ^ hi);  // leading bits every key shares
+  uint64_t pmask = common == 0 ? 0ull : ~0ull << (64 - common);
+  uint64_t prefix = hi & pmask;
   int need = k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (int shift = 56 - common;; shift -= 8) {
+    const int sh = shift < 0 ? 0 : shift;  // the last digit may overlap bits already fixed
     for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {
       const uint64_t key = lds_u64(keys + i * 8);
-      if ((key & pmask) == prefix) atomicAdd(&hist[(int)((key >> shift) & 255)], 1);
+      if ((key & pmask) == prefix) atomicAdd(&hist[(int)((key >> sh) & 255)], 1);
     }
     __syncthreads();
     if (warp == 0) {
@@ -166,11 +209,11 @@ __device__ __forceinline__ uint64_t kth_largest(const uint64_t* keys_ptr, int n,
     __syncthreads();
     const int b = s_sel[0];
     need -= s_sel[1];
-    prefix |= (uint64_t)b << shift;
-    pmask |= (uint64_t)0xFF << shift;
+    prefix = (prefix & ~((uint64_t)0xFF << sh)) | ((uint64_t)b << sh);
+    pmask |= (uint64_t)0xFF << sh;
     const bool exact = hist[b] == need;  // every key of this bucket is needed
     __syncthreads();
-    if (exact) break;
+    if (exact || sh == 0) break;
   }
   return prefix;
 }
