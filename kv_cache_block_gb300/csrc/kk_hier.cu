@@ -18,6 +18,7 @@
 
 #include "kk_device.cuh"
 #include "kk_internal.h"
+#include "kk_warp.cuh"
 
 namespace kk {
 namespace {
@@ -349,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
       }
       __syncwarp();
       const uint64_t key = score_keys16(rows, ids);
-      if (lane < 16 && i0 + lane < i_hi) st_cluster_u64(keys0 + (uint32_t)((i0 + lane) * 8), key);
+      if (lane < 16 && i0 + lane < i_hi) {
+        st_cluster_u64(keys0 + (uint32_t)((i0 + lane) * 8), key);
+        s_keys[i0 + lane] = key;  // this CTA's own copy of its share (the leader's is the same slot)
+      }
     }
     cluster_arrive_release();
     cluster_wait_acquire();
@@ -396,13 +400,56 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
         return a.vb + (long long)pg * D;
       },
       nullptr, 0, a.permille[2]);
-  if (crank != 0) return;
-  // the first m = min(K, kp) blocks of the last level in kk_topk order: the
-  // m largest keys, each written at its rank among them
+  // the first m = min(K, kp) blocks of the last level in kk_topk order
   int* io = a.idx + (long long)r * a.K;
   float* to = a.top ? a.top + (long long)r * a.K : nullptr;
   const int m = min(a.K, kp);
   const int n3 = n_last;
+  if (m > 0 && m <= 32 && CL > 1 && n3 > kThreads) {
+    // The 32 largest keys of a long list scored by a cluster: every CTA
+    // folds the share it scored into one descending 32-key list (runs of 32
+    // sorted by warps, the larger 32 of each pair kept, then a tree over the
+    // warps) and sends it to the leader, which folds the CL lists the same
+    // way. (A short list is ranked at the leader in one counting pass.)
+    __shared__ uint64_t s_wl[kWarps][32];
+    uint64_t* inbox = s_keys + kHierMax;  // [CL][32] at the leader
+    const int i_lo = (int)((long long)n3 * crank / CL), i_hi = (int)((long long)n3 * (crank + 1) / CL);
+    uint64_t acc = 0ull;
+    for (int c0 = i_lo + warp * 32; c0 < i_hi; c0 += kWarps * 32) {
+      const uint64_t k = c0 + lane < i_hi ? s_keys[c0 + lane] : 0ull;
+      acc = warp_merge_top32(acc, warp_sort_desc(k, lane), lane);
+    }
+    auto fold_warps = [&]() {
+      s_wl[warp][lane] = acc;
+      for (int h = kWarps / 2; h > 0; h >>= 1) {
+        __syncthreads();
+        if (warp < h) {
+          acc = warp_merge_top32(acc, s_wl[warp + h][lane], lane);
+          s_wl[warp][lane] = acc;
+        }
+      }
+    };
+    fold_warps();
+    if (warp == 0) st_cluster_u64(map_to_rank(smem_u32(&inbox[crank * 32 + lane]), 0), acc);
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (crank != 0) return;
+    acc = 0ull;
+    for (int q = warp; q < CL; q += kWarps) acc = warp_merge_top32(acc, inbox[q * 32 + lane], lane);
+    fold_warps();
+    if (warp == 0 && lane < a.K) {
+      const bool have = lane < m;
+      io[lane] = have ? (int)key_index(acc) : -1;
+      if (to) to[lane] = have ? key_score(acc) : -__int_as_float(0x7f800000);
+    }
+    for (int i = 32 + tid; i < a.K; i += kThreads) {
+      io[i] = -1;
+      if (to) to[i] = -__int_as_float(0x7f800000);
+    }
+    if (tid == 0 && a.kept) a.kept[r] = kp;
+    return;
+  }
+  if (crank != 0) return;
   if (m > 0 && m <= kHierOut) {
     // the m largest keys, staged past the level's list, each written at its
     // rank among them
