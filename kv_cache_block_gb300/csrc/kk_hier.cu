@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
   // them in `bits` (when given) and copies those words to every CTA. Returns
   // the number kept.
   int n_last = 0;  // members of the most recent level
-  auto level = [&](int n_parents, int fan, int n_members, const uint32_t* pbits, auto&& row_of, uint32_t* bits,
-                   int n_bits, int permille) -> int {
+  auto level = [&](int n_parents, int fan, int n_members, const uint32_t* pbits, auto&& row_of, auto&& prep,
+                   uint32_t* bits, int n_bits, int permille) -> int {
     // list the active members' indices in s_keys (each slot becomes the
     // member's key below): one thread per parent, a block scan of the counts
     int n = 0;
@@ -329,7 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
         total += s_wsum[w];
       }
       const int slot = n + before + incl - cnt;
-      for (int c = 0; c < cnt; ++c) s_keys[slot + c] = (uint64_t)(uint32_t)(p * fan + c);  // index for now
+      if (fan >= 32) {
+        // wide parents: the warp writes each listed parent's members together
+        for (unsigned todo = __ballot_sync(kFull, cnt > 0); todo != 0u; todo &= todo - 1u) {
+          const int src = __ffs(todo) - 1;
+          const int c_src = __shfl_sync(kFull, cnt, src), s_src = __shfl_sync(kFull, slot, src);
+          const int m0 = __shfl_sync(kFull, p, src) * fan;
+          for (int c = lane; c < c_src; c += 32) s_keys[s_src + c] = (uint64_t)(uint32_t)(m0 + c);
+        }
+      } else {
+        for (int c = 0; c < cnt; ++c) s_keys[slot + c] = (uint64_t)(uint32_t)(p * fan + c);  // index for now
+      }
       n += total;
       __syncthreads();
     }
@@ -339,14 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
     // score this CTA's share, sixteen members per warp at a time
     const int i_lo = (int)((long long)n * crank / CL), i_hi = (int)((long long)n * (crank + 1) / CL);
     const uint32_t keys0 = map_to_rank(smem_u32(s_keys), 0);
+    prep(i_lo, i_hi);
     for (int i0 = i_lo + warp * 16; i0 < i_hi; i0 += kWarps * 16) {
       const float* rows[16];
       uint32_t ids[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const bool have = i0 + u < i_hi;
-        ids[u] = have ? (uint32_t)s_keys[i0 + u] : 0u;
-        rows[u] = have ? row_of((int)ids[u]) : nullptr;
+        const uint64_t e = have ? s_keys[i0 + u] : 0ull;
+        ids[u] = (uint32_t)e;
+        rows[u] = have ? row_of(e) : nullptr;
       }
       __syncwarp();
       const uint64_t key = score_keys16(rows, ids);
@@ -385,19 +397,41 @@ __global__ void __launch_bounds__(kThreads, 1) hier_select_kernel(const HierArgs
     return k;
   };
 
+  // A list entry holds the member's index in its low half; the block level
+  // first loads the CTA's share of page ids together into the high halves,
+  // so that scoring does not wait for them one group at a time.
   const long long rrow = (long long)r;
-  level(G, 1, G, nullptr, [&](int g) { return a.grid + (rrow * a.g_max + g) * D; }, s_gbits, G, a.permille[0]);
-  level(G, a.grid_chunks, C, s_gbits, [&](int c) { return a.chunk + (rrow * a.c_max + c) * D; }, s_cbits, C,
-        a.permille[1]);
+  auto no_prep = [](int, int) {};
+  level(G, 1, G, nullptr, [&](uint64_t e) { return a.grid + (rrow * a.g_max + (uint32_t)e) * D; }, no_prep, s_gbits,
+        G, a.permille[0]);
+  level(G, a.grid_chunks, C, s_gbits, [&](uint64_t e) { return a.chunk + (rrow * a.c_max + (uint32_t)e) * D; },
+        no_prep, s_cbits, C, a.permille[1]);
   const int kp = level(
       C, a.chunk_pages, nb, s_cbits,
-      [&](int j) -> const float* {
-        const int pg = a.bt.pages[off + j];
+      [&](uint64_t e) -> const float* {
+        const int pg = (int)(uint32_t)(e >> 32);
         if (pg < 0 || pg >= a.vb_rows) {
           flag_error(a.err, kErrBadIndex);
           return nullptr;
         }
         return a.vb + (long long)pg * D;
+      },
+      [&](int i_lo, int i_hi) {
+        constexpr int kBatch = 4;
+        for (int i0 = i_lo + tid; i0 < i_hi; i0 += kBatch * kThreads) {
+          int pg[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kThreads;
+            pg[u] = i < i_hi ? a.bt.pages[off + (int)(uint32_t)s_keys[i]] : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kThreads;
+            if (i < i_hi) s_keys[i] = (uint64_t)(uint32_t)s_keys[i] | ((uint64_t)(uint32_t)pg[u] << 32);
+          }
+        }
+        __syncthreads();
       },
       nullptr, 0, a.permille[2]);
   // the first m = min(K, kp) blocks of the last level in kk_topk order
