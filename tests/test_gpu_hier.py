@@ -67,9 +67,25 @@ def _cuts_are_clear(vb_l, va, cp, gc, pm):
     (16, 4, (300, 300, 500), 5),
 ])
 def test_hier_select(kk, cp, gc, pm, K):
-    nb = [1024, 300, 77, 1, 2048, 0]
-    D = 128
-    offsets, pages, vb, va = _case(nb, D, seed=cp * 100 + gc)
+    _check_hier(kk, [1024, 300, 77, 1, 2048, 0], 128, cp, gc, pm, K, seed=cp * 100 + gc)
+
+
+@pytest.mark.parametrize("cp,gc,pm,K,seed", [
+    (16, 4, (500, 400, 300), 32, 46),
+    (16, 4, (500, 400, 300), 10, 46),
+    (16, 4, (500, 400, 5), 32, 41),
+    (64, 8, (500, 200, 100), 40, 41),
+])
+def test_hier_select_long_requests(kk, cp, gc, pm, K, seed):
+    """Two long requests, so each is scored by a cluster of CTAs: with at
+    most 32 blocks out of a last level of thousands, every CTA folds its
+    share to a 32-key list for the leader (K 32, K 10, and a level that keeps
+    fewer blocks than K); with more, the leader's radix select (K 40)."""
+    _check_hier(kk, [20000, 16000], 128, cp, gc, pm, K, seed)
+
+
+def _check_hier(kk, nb, D, cp, gc, pm, K, seed):
+    offsets, pages, vb, va = _case(nb, D, seed=seed)
     R = len(nb)
     bt = kk.BlockTable(_i32(pages), _i32(offsets), None, max(nb))
     C_max = -(-max(nb) // cp)
