@@ -12,8 +12,11 @@
 // few long requests leave SMs idle): every CTA lists the level's active
 // members, scores its share (sixteen per warp, one transposed reduction) and
 // stores the 64-bit keys (score, index) into the leader's shared memory; the
-// leader sorts them, keeps the best share and sends the kept bitmap to every
-// CTA; the last level's kept blocks are written in kk_topk order.
+// leader finds the k-th largest key (one counting pass for short lists, else
+// a radix select), keeps the best share and sends the kept bitmap to every
+// CTA. The last level's first K kept blocks are written in kk_topk order:
+// ranked at the leader, or, when a cluster scored a long last level and at
+// most 32 are written, folded from every CTA's top-32 list.
 #include <mutex>
 
 #include "kk_device.cuh"

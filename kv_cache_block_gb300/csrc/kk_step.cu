@@ -8,8 +8,10 @@
 // bulk-copying (TMA) the v_b rows of its blocks into shared memory, so that
 // gather overlaps the anchor. Partial anchors, and each CTA's sorted top-K
 // list, are exchanged through distributed shared memory; every CTA then ranks
-// its own candidates in the union and writes them. A whole step is one launch
-// with no global scratch. Every stage can be switched off, which gives
+// its own candidates in the union and writes them. A few very long requests
+// are split over several clusters each: every cluster writes its sorted top-K
+// list to a fixed device buffer and the last one to finish merges the lists.
+// A whole step is one launch. Every stage can be switched off, which gives
 // kk_anchor, kk_score, kk_topk and kk_score_topk from the same code.
 #include <algorithm>
 #include <mutex>
