@@ -106,3 +106,15 @@ def test_clock_summary_uses_the_timed_window():
     s = bench.summarize_clocks(lines, 1.3, 1.4)  # window shorter than the period: next sample, flagged
     assert s["samples"] == 1 and s["sm_mhz"] == 900 and not s["in_window"]
     assert bench.summarize_clocks([], 0, 1)["samples"] == 0
+
+
+def test_pool_profile_is_of_the_current_sources():
+    """The bench reports the pool kernel's DRAM traffic from the committed ncu
+    summary only while the kernel's sources hash to the profiled ones: a
+    change to those sources needs the counters taken again."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    traffic = bench.profiled_traffic("7b")
+    assert traffic is not None, "profiles/pool_kernel_7b.md was taken on other pool kernel sources"
+    assert 7.0e9 < traffic < 8.0e9  # one launch reads the 7.52 GB of K once
