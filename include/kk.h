@@ -115,6 +115,10 @@ kk_status kk_pool_blocks(const kk_kcache_desc* kc, const int32_t* pages, const i
  * request's seq_lens[r] tokens, and head_w_out[r][l*H+h] = Var / sum Var
  * (uniform 1/(L*H) if every Var is 0). head_w_out: device [R][L*H].
  * Needs kk_head_variance_workspace_bytes() bytes of device workspace.
+ * total_blocks must be offsets[R]; a request whose table reaches past it is
+ * skipped (its weights and blocks are not written) and reported through the
+ * device error word, as is a block with a page id out of range (its Keys
+ * count as zero in the request's variance).
  */
 size_t kk_head_variance_workspace_bytes(const kk_kcache_desc* kc, int32_t total_blocks,
                                         int32_t num_requests);
@@ -146,11 +150,16 @@ kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table
  *   R); above 32 MiB the call returns KK_ERR_UNSUPPORTED and launches nothing.
  * - It allocates nothing: no cudaMalloc or cudaFree, no allocating library
  *   call. The first call on a device looks up the array's device address (and
- *   the error word's); make that first call before any stream capture.
+ *   the error word's) and keeps it for the life of the process; make that
+ *   first call before any stream capture, and do not reset the device
+ *   (cudaDeviceReset) after it: the kept address would then be stale.
  * - Every call shares the one array. Calls that overlap on the GPU (on two
  *   streams, or from two threads) race on it and give wrong results; order
  *   them on one stream. Nothing needs clearing between calls: each call
- *   writes every scratch byte before reading it.
+ *   writes every scratch byte before reading it (a block whose page id is out
+ *   of range has its sums written as zero, and the call reports
+ *   KK_ERR_BAD_INDEX). A table that reaches past total_blocks is reported and
+ *   its requests are skipped; the kernels never index past the array.
  * Results are the same as kk_pool_blocks_weighted's.
  */
 kk_status kk_pool_blocks_weighted_static(const kk_kcache_desc* kc, const kk_block_table* bt,

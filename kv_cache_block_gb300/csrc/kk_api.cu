@@ -153,9 +153,9 @@ static kk_status variance_common(const kk_kcache_desc* kc, const kk_block_table*
   if (!err) return KK_ERR_CUDA;
   VarWorkspace w = carve(ws, LH, c.D, total_blocks);
   cudaError_t e = kk::launch_pool_slices(c, t, total_blocks, w.S, w.Q, err, stream);
-  if (e == cudaSuccess) e = kk::launch_head_var(c, t, w.S, w.Q, w.var, err, stream);
-  if (e == cudaSuccess) e = kk::launch_finalize_weights(c, t, w.var, head_w_out, stream);
-  if (e == cudaSuccess && vb) e = kk::launch_combine(c, t, w.S, head_w_out, vb, err, stream);
+  if (e == cudaSuccess) e = kk::launch_head_var(c, t, total_blocks, w.S, w.Q, w.var, err, stream);
+  if (e == cudaSuccess) e = kk::launch_finalize_weights(c, t, total_blocks, w.var, head_w_out, stream);
+  if (e == cudaSuccess && vb) e = kk::launch_combine(c, t, total_blocks, w.S, head_w_out, vb, err, stream);
   return from_cuda(e);
 }
 

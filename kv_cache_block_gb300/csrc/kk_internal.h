@@ -37,12 +37,14 @@ cudaError_t launch_pool_direct(const KCache& kc, const int* pages, const int* n_
                                int* err, cudaStream_t s);
 cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, long long total_blocks, float* S, float* Q,
                                int* err, cudaStream_t s);
-cudaError_t launch_head_var(const KCache& kc, const Table& bt, const float* S, const float* Q,
-                            double* var, int* err, cudaStream_t s);
-cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, const double* var,
+// total_blocks: rows of the S / Q scratch; a request whose table reaches
+// past it is skipped and reported (the kernels never index past the scratch)
+cudaError_t launch_head_var(const KCache& kc, const Table& bt, long long total_blocks, const float* S,
+                            const float* Q, double* var, int* err, cudaStream_t s);
+cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, long long total_blocks, const double* var,
                                     float* head_w_out, cudaStream_t s);
-cudaError_t launch_combine(const KCache& kc, const Table& bt, const float* S, const float* head_w,
-                           float* vb, int* err, cudaStream_t s);
+cudaError_t launch_combine(const KCache& kc, const Table& bt, long long total_blocks, const float* S,
+                           const float* head_w, float* vb, int* err, cudaStream_t s);
 
 // kk_step.cu
 enum StepFlags {

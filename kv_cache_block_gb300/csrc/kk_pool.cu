@@ -34,6 +34,7 @@ struct PoolArgs {
   const int* offsets;
   const int* seq_lens;
   int max_blocks;
+  long long total;  // rows of S / Q (blocks of the whole table)
   float* S;  // [total_blocks][L*H][D] token sums per (layer, head)
   float* Q;  // [total_blocks][L*H] sums of squares over tokens and dims
   int* err;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
     const int nb = a.offsets[r + 1] - off;
     if (j >= nb) return;
     const int T_r = a.seq_lens[r];
-    if (nb > a.max_blocks || T_r < 0 || nb != (T_r + a.bs - 1) / a.bs) {
+    if (off < 0 || nb > a.max_blocks || (long long)off + nb > a.total || T_r < 0 || nb != (T_r + a.bs - 1) / a.bs) {
       if (threadIdx.x == 0 && j == 0) flag_error(a.err, kErrBadIndex);
       return;
     }
@@ -107,7 +108,11 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
     page = a.bt_pages[g];
     n = min(a.bs, T_r - j * a.bs);
     if (page < 0 || page >= a.num_pages) {
+      // the block's sums read as zero: the request's variance sums never see
+      // what an earlier call left in the scratch
       if (threadIdx.x == 0) flag_error(a.err, kErrBadIndex);
+      for (int i = threadIdx.x; i < LH * D; i += kThreads) a.S[(long long)g * LH * D + i] = 0.f;
+      for (int i = threadIdx.x; i < LH; i += kThreads) a.Q[(long long)g * LH + i] = 0.f;
       return;
     }
   } else {
@@ -215,14 +220,14 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(PoolArgs a) {
 __global__ void __launch_bounds__(kThreads) head_var_kernel(const float* S, const float* Q,
                                                             const int* offsets, const int* seq_lens,
                                                             int bs, int LH, int D, int max_blocks,
-                                                            double* var, int* err) {
+                                                            long long total, double* var, int* err) {
   __shared__ double s_sum[kThreads * 4];  // [row group][D]: kThreads / (D/4) groups of D
   __shared__ double s_q[kThreads];
   const int s = blockIdx.x, r = blockIdx.y;
   const int off = offsets[r];
   const int nb = offsets[r + 1] - off;
   const int T_r = seq_lens[r];
-  if (nb < 0 || nb > max_blocks || T_r < 0 || nb != (T_r + bs - 1) / bs) {
+  if (off < 0 || nb < 0 || nb > max_blocks || (long long)off + nb > total || T_r < 0 || nb != (T_r + bs - 1) / bs) {
     if (threadIdx.x == 0 && s == 0) flag_error(err, kErrBadIndex);
     return;
   }
@@ -285,12 +290,15 @@ __global__ void __launch_bounds__(kThreads) head_var_kernel(const float* S, cons
 __global__ void __launch_bounds__(kThreads) finalize_weights_kernel(const double* var, int LH,
                                                                     const int* offsets,
                                                                     const int* seq_lens, int bs,
-                                                                    int max_blocks, float* out) {
+                                                                    int max_blocks, long long total,
+                                                                    float* out) {
   __shared__ double s_part[kThreads];
   const int r = blockIdx.x;
-  const int nb = offsets[r + 1] - offsets[r];
+  const int off = offsets[r];
+  const int nb = offsets[r + 1] - off;
   const int T_r = seq_lens[r];
-  if (nb < 0 || nb > max_blocks || T_r < 0 || nb != (T_r + bs - 1) / bs) return;  // flagged upstream
+  if (off < 0 || nb < 0 || nb > max_blocks || (long long)off + nb > total || T_r < 0 || nb != (T_r + bs - 1) / bs)
+    return;  // flagged upstream
   double acc = 0.0;
   for (int s = threadIdx.x; s < LH; s += kThreads) acc += var[(long long)r * LH + s];
   s_part[threadIdx.x] = acc;
@@ -310,15 +318,17 @@ __global__ void __launch_bounds__(kThreads) finalize_weights_kernel(const double
 __global__ void __launch_bounds__(kThreads) combine_kernel(const float* S, const float* head_w,
                                                            const int* pages, const int* offsets,
                                                            const int* seq_lens, int bs, int LH,
-                                                           int D, int max_blocks, int num_pages,
-                                                           float* vb) {
+                                                           int D, int max_blocks, long long total,
+                                                           int num_pages, float* vb) {
   __shared__ float s_w[kMaxLH];
   __shared__ float4 s_part[kThreads];
   const int j = blockIdx.x, r = blockIdx.y;
   const int off = offsets[r];
   const int nb = offsets[r + 1] - off;
   const int T_r = seq_lens[r];
-  if (j >= nb || nb > max_blocks || T_r < 0 || nb != (T_r + bs - 1) / bs) return;  // flagged upstream
+  if (j >= nb || off < 0 || nb > max_blocks || (long long)off + nb > total || T_r < 0 ||
+      nb != (T_r + bs - 1) / bs)
+    return;  // flagged upstream
   const int page = pages[off + j];
   if (page < 0 || page >= num_pages) return;  // flagged by the slice kernel
   for (int s = threadIdx.x; s < LH; s += kThreads) s_w[s] = head_w[(long long)r * LH + s];
@@ -444,34 +454,35 @@ cudaError_t launch_pool_slices(const KCache& kc, const Table& bt, long long tota
   a.offsets = bt.offsets;
   a.seq_lens = bt.seq_lens;
   a.max_blocks = bt.max_blocks;
+  a.total = total_blocks;
   a.S = S;
   a.Q = Q;
   return dispatch_pool<true>(kc, a, dim3(bt.max_blocks, bt.R), 1, s);
 }
 
-cudaError_t launch_head_var(const KCache& kc, const Table& bt, const float* S, const float* Q,
-                            double* var, int* err, cudaStream_t s) {
+cudaError_t launch_head_var(const KCache& kc, const Table& bt, long long total_blocks, const float* S,
+                            const float* Q, double* var, int* err, cudaStream_t s) {
   if (bt.R == 0) return cudaSuccess;
   head_var_kernel<<<dim3(kc.L * kc.H, bt.R), kThreads, 0, s>>>(
-      S, Q, bt.offsets, bt.seq_lens, kc.bs, kc.L * kc.H, kc.D, bt.max_blocks, var, err);
+      S, Q, bt.offsets, bt.seq_lens, kc.bs, kc.L * kc.H, kc.D, bt.max_blocks, total_blocks, var, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, const double* var,
+cudaError_t launch_finalize_weights(const KCache& kc, const Table& bt, long long total_blocks, const double* var,
                                     float* head_w_out, cudaStream_t s) {
   if (bt.R == 0) return cudaSuccess;
   finalize_weights_kernel<<<bt.R, kThreads, 0, s>>>(var, kc.L * kc.H, bt.offsets, bt.seq_lens,
-                                                    kc.bs, bt.max_blocks, head_w_out);
+                                                    kc.bs, bt.max_blocks, total_blocks, head_w_out);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const KCache& kc, const Table& bt, const float* S, const float* head_w,
-                           float* vb, int* err, cudaStream_t s) {
+cudaError_t launch_combine(const KCache& kc, const Table& bt, long long total_blocks, const float* S,
+                           const float* head_w, float* vb, int* err, cudaStream_t s) {
   (void)err;
   if (bt.R == 0 || bt.max_blocks == 0) return cudaSuccess;
   combine_kernel<<<dim3(bt.max_blocks, bt.R), kThreads, 0, s>>>(S, head_w, bt.pages, bt.offsets,
                                                             bt.seq_lens, kc.bs, kc.L * kc.H, kc.D,
-                                                            bt.max_blocks, kc.num_pages, vb);
+                                                            bt.max_blocks, total_blocks, kc.num_pages, vb);
   return cudaGetLastError();
 }
 

@@ -284,21 +284,24 @@ struct SliceTmaArgs {
 struct SliceBlock {
   int page, n;
   bool ok, bad;
+  bool zero;  // a valid table entry whose page id is out of range: its sums are written as zero
 };
 
 // Block g of the table; r is the request holding it, advanced monotonically.
 __device__ __forceinline__ SliceBlock slice_block(const SliceTmaArgs& a, long long g, int& r) {
   while (r < a.bt.R && a.bt.offsets[r + 1] <= g) ++r;
-  SliceBlock m{0, 0, false, false};
+  SliceBlock m{0, 0, false, false, false};
   if (r >= a.bt.R) return m;
   const int off = a.bt.offsets[r], nb = a.bt.offsets[r + 1] - off, T = a.bt.seq_lens[r];
-  if (nb < 0 || nb > a.bt.max_blocks || T < 0 || nb != (T + a.bs - 1) / a.bs || g < off) {
+  if (off < 0 || nb < 0 || nb > a.bt.max_blocks || (long long)off + nb > a.total || T < 0 ||
+      nb != (T + a.bs - 1) / a.bs || g < off) {
     m.bad = true;
     return m;
   }
   m.page = a.bt.pages[g];
   m.n = min(a.bs, T - (int)(g - off) * a.bs);
   m.bad = m.page < 0 || m.page >= a.num_pages;
+  m.zero = m.bad;
   m.ok = !m.bad && m.n > 0;
   return m;
 }
@@ -394,6 +397,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const SliceBlock m = slice_block(a, g, r);
     if (!m.ok) {
       if (m.bad && cw == 0 && lane == 0) flag_error(a.err, kErrBadIndex);
+      if (m.zero) {
+        // the request's variance sums read this block as zero rather than
+        // whatever an earlier call left in the scratch
+        const int ct = tid - 32;
+        for (int i = ct; i < LH * D; i += kConsumers) a.S[g * LH * D + i] = 0.f;
+        for (int i = ct; i < LH; i += kConsumers) a.Q[g * LH + i] = 0.f;
+      }
       continue;
     }
     const int nt = (m.n + a.tb - 1) / a.tb;

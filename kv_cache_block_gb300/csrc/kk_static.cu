@@ -65,8 +65,8 @@ extern "C" kk_status kk_pool_blocks_weighted_static(const kk_kcache_desc* kc,
   float* Q = reinterpret_cast<float*>(base + s_bytes);
   double* var = reinterpret_cast<double*>(base + s_bytes + q_bytes);
   cudaError_t e = kk::launch_pool_slices(c, t, total_blocks, S, Q, err, stream);
-  if (e == cudaSuccess) e = kk::launch_head_var(c, t, S, Q, var, err, stream);
-  if (e == cudaSuccess) e = kk::launch_finalize_weights(c, t, var, head_w_out, stream);
-  if (e == cudaSuccess) e = kk::launch_combine(c, t, S, head_w_out, vb, err, stream);
+  if (e == cudaSuccess) e = kk::launch_head_var(c, t, total_blocks, S, Q, var, err, stream);
+  if (e == cudaSuccess) e = kk::launch_finalize_weights(c, t, total_blocks, var, head_w_out, stream);
+  if (e == cudaSuccess) e = kk::launch_combine(c, t, total_blocks, S, head_w_out, vb, err, stream);
   return e == cudaSuccess ? KK_OK : KK_ERR_CUDA;
 }

@@ -118,6 +118,15 @@ def test_host_argument_errors(kk):
     assert lib.kk_head_variance(B(d), B(t), 4, 16, 256, 1, None) == kk.KK_ERR_INVALID
     assert lib.kk_head_variance(B(d), B(t), 4, None, 256, 1 << 30, None) == kk.KK_ERR_INVALID
     assert lib.kk_pool_blocks_weighted(B(d), B(t), 4, 16, None, 256, 1 << 30, None) == kk.KK_ERR_INVALID
+    # kk_pool_blocks_weighted_static: missing outputs, negative size, scratch above its 32 MiB
+    # (rejected before any CUDA call)
+    assert lib.kk_pool_blocks_weighted_static(B(d), B(t), 4, None, 16, None) == kk.KK_ERR_INVALID
+    assert lib.kk_pool_blocks_weighted_static(B(d), B(t), 4, 16, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_pool_blocks_weighted_static(B(d), B(t), -1, 16, 16, None) == kk.KK_ERR_INVALID
+    assert lib.kk_pool_blocks_weighted_static(None, B(t), 4, 16, 16, None) == kk.KK_ERR_INVALID
+    assert lib.kk_pool_blocks_weighted_static(B(d), None, 4, 16, 16, None) == kk.KK_ERR_INVALID
+    assert lib.kk_pool_blocks_weighted_static(B(d), B(t), 1 << 20, 16, 16, None) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_pool_blocks_weighted_static(B(d), B(_table(kk, R=0)), 4, 16, 16, None) == kk.KK_OK
     ws = lib.kk_head_variance_workspace_bytes(B(d), 4, 1)
     assert ws >= 4 * 4 * 128 * 4 + 4 * 4 * 4 + 4 * 8
     assert lib.kk_head_variance(B(d), B(t), 4, 16, 256 + 8, ws, None) == kk.KK_ERR_UNSUPPORTED

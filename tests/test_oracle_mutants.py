@@ -47,6 +47,33 @@ def m_pool_sum_not_mean(o):
     o.pool_block = pool_block
 
 
+def m_decode_shift_15(o):
+    def decode(x):
+        x = np.asarray(x)
+        if x.dtype == np.uint16:
+            return (x.astype(np.uint32) << 15).view(np.float32).astype(np.float64)
+        return x.astype(np.float64)
+    o.decode = decode
+
+
+def m_decode_reads_fp16(o):
+    def decode(x):
+        x = np.asarray(x)
+        if x.dtype == np.uint16:
+            return x.view(np.float16).astype(np.float64)
+        return x.astype(np.float64)
+    o.decode = decode
+
+
+def m_decode_drops_sign(o):
+    def decode(x):
+        x = np.asarray(x)
+        if x.dtype == np.uint16:
+            return ((x.astype(np.uint32) & 0x7FFF) << 16).view(np.float32).astype(np.float64)
+        return x.astype(np.float64)
+    o.decode = decode
+
+
 def m_affinity_not_halved(o):
     base = ko.affinity
     o.affinity = lambda vb, va: 2.0 * base(vb, va)
@@ -307,6 +334,7 @@ def m_hier_pool_share_of_allowed(o):
 
 
 MUTANTS = [
+    m_decode_shift_15, m_decode_reads_fp16, m_decode_drops_sign,
     m_pool_divides_by_heads_only, m_pool_weights_transposed, m_pool_sum_not_mean,
     m_affinity_not_halved, m_affinity_raw_dot, m_affinity_zero_vector_scores_zero,
     m_topk_ties_to_higher_index, m_topk_ascending, m_anchor_first_tokens,

@@ -40,6 +40,16 @@ def check_pool_golden(o):
     np.testing.assert_array_equal(o.pool_block(K[:, :, :0, :]), [0.0, 0.0])
 
 
+def check_decode_golden(o):
+    # bf16 bit patterns and their exact values, worked out from the format's bit fields
+    for c in gold("bf16_decode.json")["cases"]:
+        got = float(o.decode(np.array([int(c["bits"], 16)], dtype=np.uint16))[0])
+        want = float(c["value"]) if c["value"] in ("inf", "-inf") else float.fromhex(c["value"])
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (c, got)
+    # float32 and float64 inputs are taken as they are
+    np.testing.assert_array_equal(o.decode(np.array([1.5, -2.25], dtype=np.float32)), [1.5, -2.25])
+
+
 def check_affinity_golden(o):
     for c in gold("affinity.json")["cases"]:
         s = o.affinity(np.array([c["vb"]], float), np.array(c["va"], float))[0]
@@ -432,6 +442,7 @@ def check_hier_pool_bruteforce(o):
 
 
 ALL_CHECKS = [
+    check_decode_golden,
     check_pool_golden, check_affinity_golden, check_topk_golden, check_anchor_golden,
     check_variance_golden, check_coarse_golden, check_batched_golden, check_bruteforce,
     check_batched_bruteforce, check_reblocking, check_linearity_and_symmetry, check_page_shuffle,

@@ -81,3 +81,46 @@ def test_static_scratch_rejects_oversized_workloads(kk):
     assert status == kk.KK_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.all(vb == -1.0)  # nothing was launched
+
+
+def test_static_scratch_bounds_and_bad_pages(kk):
+    """A block table that reaches past total_blocks is reported and skipped
+    (nothing is indexed past the array), and a block with an out-of-range page
+    counts as zero in its request's variance instead of whatever an earlier
+    call left in the array: the static form then equals the workspace form."""
+    # 300 blocks: more than one per SM, so the persistent slice kernel runs
+    spec = synth.qwen7b(L=6, H=4, bs=32, seq_lens=[32 * 200 + 3, 32 * 100], num_topics=4, sigma_range=(0.5, 3.0),
+                        shuffle_pages=True, seed=44)
+    dev = DeviceCache(spec)
+    sp = dev.spec
+    # fill the array with this cache's sums first
+    status, _, _ = _static_through_c_abi(kk, dev)
+    assert status == kk.KK_OK and kk.kk_device_error() == 0
+    # total_blocks short of offsets[R]: both requests reported, no output written
+    lib = ctypes.CDLL(kk.LIB_PATH)
+    fn = lib.kk_pool_blocks_weighted_static
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(kk.kk_kcache_desc), ctypes.POINTER(kk.kk_block_table), ctypes.c_int32,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    w = torch.full((sp.R, sp.L * sp.H), -1.0, device="cuda")
+    vb = torch.full((sp.num_pages, sp.D), -1.0, device="cuda")
+    status = fn(ctypes.byref(dev.desc), ctypes.byref(dev.bt.c), sp.nb[0] - 1, w.data_ptr(), vb.data_ptr(),
+                torch.cuda.current_stream().cuda_stream)
+    assert status == kk.KK_OK
+    assert kk.kk_device_error() == kk.KK_ERR_BAD_INDEX
+    assert torch.all(w == -1.0) and torch.all(vb == -1.0)
+    # one page id out of range in request 1
+    pages = dev.pages.clone()
+    pages[sp.offsets[1] + 7] = sp.num_pages + 5
+    bad = DeviceCache.__new__(DeviceCache)
+    bad.__dict__.update(dev.__dict__)
+    bad.pages = pages
+    bad.bt = kk.BlockTable(pages, dev.offsets, dev.seq_lens, max(sp.nb))
+    w_ref, vb_ref = _with_workspace(kk, bad)
+    assert kk.kk_device_error() == kk.KK_ERR_BAD_INDEX
+    status, w, vb = _static_through_c_abi(kk, bad)
+    assert status == kk.KK_OK
+    assert kk.kk_device_error() == kk.KK_ERR_BAD_INDEX
+    assert_vec_close(w.cpu().numpy(), w_ref.cpu().numpy(), "head weights with a bad page")
+    good = np.setdiff1d(sp.pages, [sp.pages[sp.offsets[1] + 7]])
+    assert_vec_close(vb.cpu().numpy()[good], vb_ref.cpu().numpy()[good], "weighted vb with a bad page")
