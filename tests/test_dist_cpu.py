@@ -109,12 +109,13 @@ def test_clock_summary_uses_the_timed_window():
 
 
 def test_pool_profile_is_of_the_current_sources():
-    """The bench reports the pool kernel's DRAM traffic from the committed ncu
-    summary only while the kernel's sources hash to the profiled ones: a
+    """The bench reports the headline pool's DRAM traffic from the committed
+    ncu summary only while the kernels' sources hash to the profiled ones: a
     change to those sources needs the counters taken again."""
     sys.path.insert(0, ROOT)
     import bench
 
-    traffic = bench.profiled_traffic("7b")
-    assert traffic is not None, "profiles/pool_kernel_7b.md was taken on other pool kernel sources"
-    assert 7.0e9 < traffic < 8.0e9  # one launch reads the 7.52 GB of K once
+    traffic = bench.profiled_traffic(bench.DEFAULT_WORKLOAD)
+    assert traffic is not None, "the weighted pool's ncu summary was taken on other kernel sources"
+    # one weighted pool call reads the 120.26 GB of K once, plus its 1/64-size slice sums
+    assert 1.20e11 < traffic < 1.30e11
