@@ -402,10 +402,24 @@ def b2b_us(fn, dev, stream, n: int = 200, warm: int = 5):
     return e0.elapsed_time(e1) * 1e3 / n
 
 
+class L2Flush:
+    """Evicts L2 between timed calls by reading a buffer twice its size. A
+    read leaves clean lines behind; a flush that wrote the buffer would leave
+    L2 full of dirty lines, and the timed call would pay for writing them back
+    (about 129 MB, some 19 us of HBM write time)."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.sum()
+
+
 def per_call_ms(fn, dev, stream, n: int, warm: int, flush=None):
-    """CUDA-event time of each of ``n`` calls of ``fn``; with ``flush`` (a
-    device buffer larger than L2) the buffer is rewritten before every call,
-    outside the timed interval."""
+    """CUDA-event time of each of ``n`` calls of ``fn``; with ``flush`` (an
+    L2Flush) L2 is evicted before every call, outside the timed interval."""
     import torch
 
     for _ in range(warm):
@@ -414,7 +428,7 @@ def per_call_ms(fn, dev, stream, n: int, warm: int, flush=None):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
         if flush is not None:
-            flush.fill_(i & 255)
+            flush()
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
@@ -449,6 +463,15 @@ class PagedRun:
         # kernels launched by one pool call (the weighted pool: slice sums,
         # variances, weights, combine)
         self.pool_launches = 4 if spec.weighted else 1
+        # the workspace that lets very long requests split over several clusters
+        nws = kk.kk_select_step_workspace_bytes(spec.R, max(spec.nb), spec.K)
+        self.step_ws = torch.zeros(nws, dtype=torch.uint8, device=dev) if nws else None  # zeroed once
+        # the anchor ring of the last W tokens (filled from the cache once the
+        # cache is written; kept by kk_append_tokens in the decode step)
+        self.ring = kk.AnchorRing(spec.R, spec.W, spec.D, device=dev)
+
+    def fill_ring(self):
+        self.kk.kk_anchor_ring_fill(self.desc, self.bt, self.ring, head_w=self.head_w)
 
     def pool(self):
         sp = self.spec
@@ -459,21 +482,34 @@ class PagedRun:
 
     def select(self):
         sp = self.spec
-        self.kk.kk_select_step(self.desc, self.bt, sp.W, self.vb, sp.K, self.idx, self.top, head_w=self.head_w)
+        self.kk.kk_select_step(self.desc, self.bt, sp.W, self.vb, sp.K, self.idx, self.top, head_w=self.head_w,
+                               workspace=self.step_ws)
+
+    def select_ring(self):
+        sp = self.spec
+        self.kk.kk_select_step(self.desc, self.bt, sp.W, self.vb, sp.K, self.idx, self.top, head_w=self.head_w,
+                               ring=self.ring, workspace=self.step_ws)
 
 
-def select_record(run, dev, stream, peak_gbs: float):
+def select_record(run, dev, stream, peak_gbs: float, ring: bool = False):
     """Latency of one selector step over all requests (anchor, scores, top-K
     in one launch), back to back and as a CUDA graph, with its roofline
-    fraction against the step's algorithmic bytes."""
+    fraction against the step's algorithmic bytes (the anchor's token rows
+    and every candidate's v_b row read once). With ``ring`` the anchor comes
+    from the anchor ring (W rows of D floats a request) instead of the
+    token rows; the fraction keeps the same algorithmic bytes."""
     sp = run.spec
-    b2b = b2b_us(run.select, dev, stream)
-    graph = graph_time_us(run.select, dev, stream)
+    fn = run.select_ring if ring else run.select
+    if ring:
+        run.fill_ring()
+    b2b = b2b_us(fn, dev, stream)
+    graph = graph_time_us(fn, dev, stream)
     nbytes = step_bytes(sp)
     frac = lambda us: None if us is None else nbytes / (us * 1e-6) / 1e9 / peak_gbs  # noqa: E731
     return {"us_back_to_back": b2b, "us_cuda_graph": graph, "algorithmic_bytes": nbytes,
             "roofline_frac_back_to_back": frac(b2b), "roofline_frac_cuda_graph": frac(graph),
-            "blocks_scored_per_s_cuda_graph": None if graph is None else sp.total_blocks / (graph * 1e-6)}
+            "blocks_scored_per_s_cuda_graph": None if graph is None else sp.total_blocks / (graph * 1e-6),
+            "anchor": "anchor ring (kk_append_tokens / kk_anchor_ring_fill)" if ring else "K cache token rows"}
 
 
 def pool_record(run, dev, stream, peak_gbs: float, steps: int, warmup: int, flush=None):
@@ -548,7 +584,8 @@ def main_extras(args, run, dev, stream, peak_gbs):
     from kv_cache_block_gb300 import kk
 
     sp = run.spec
-    out = {"select": select_record(run, dev, stream, peak_gbs)}
+    out = {"select": select_record(run, dev, stream, peak_gbs),
+           "select_ring": select_record(run, dev, stream, peak_gbs, ring=True)}
     va = torch.zeros((sp.R, sp.D), device=dev)
 
     def anchor_then_score():
@@ -559,9 +596,9 @@ def main_extras(args, run, dev, stream, peak_gbs):
     hist = torch.zeros(sp.total_blocks, dtype=torch.int32, device=dev)
     stab = torch.zeros(sp.total_blocks, device=dev)
 
-    def select_stable():
+    def select_stable(ring=None):
         kk.kk_select_step_stable(run.desc, run.bt, sp.W, run.vb, sp.K, 20, 0.5, hist, run.idx, stab=stab,
-                                 top_scores=run.top, head_w=run.head_w)
+                                 top_scores=run.top, head_w=run.head_w, ring=ring, workspace=run.step_ws)
 
     out["stable_us"] = b2b_us(select_stable, dev, stream)
     # hierarchical Grid -> Chunk -> Page (64 blocks a Chunk, 8 Chunks a Grid,
@@ -581,24 +618,40 @@ def main_extras(args, run, dev, stream, peak_gbs):
 
     out["hier_us"] = b2b_us(hier_select, dev, stream)
     out["hier_kept"] = int(h_kept.sum().item())
-    # one whole decode step as a CUDA graph: each request's new token written
-    # into its block with v_b kept current (kk_append_tokens), the
-    # stability-filtered selection and the table of selected pages
+    out["decode_step_us"] = decode_step_us(run, dev, stream)
+    if kk.kk_device_error() != 0:
+        raise RuntimeError("device error in the selector legs")
+    return out
+
+
+def decode_step_us(run, dev, stream):
+    """One whole decode step as a CUDA graph: each request's new token
+    written into its block with v_b and the anchor ring kept current
+    (kk_append_tokens), the stability-filtered selection with the anchor from
+    the ring (kk_select_step_stable) and the table of selected pages
+    (kk_compact_table). The token is written at position seq_len - 1 (its
+    block exists in this fixed-size cache)."""
+    import torch
+
+    from kv_cache_block_gb300 import kk
+
+    sp = run.spec
     k_new = torch.randn((sp.R, sp.L, sp.H, sp.D), device=dev)
     k_new = k_new.to(torch.bfloat16).view(torch.int16) if sp.dtype == "bf16" else k_new
     block_sum = torch.zeros((sp.num_pages, sp.D), device=dev)
     sel_pages = torch.zeros((sp.R, sp.K), dtype=torch.int32, device=dev)
     sel_count = torch.zeros(sp.R, dtype=torch.int32, device=dev)
+    hist = torch.zeros(sp.total_blocks, dtype=torch.int32, device=dev)
+    stab = torch.zeros(sp.total_blocks, device=dev)
 
     def decode_step():
-        kk.kk_append_tokens(run.desc, run.bt, k_new, block_sum, run.vb, head_w=run.head_w)
-        select_stable()
+        kk.kk_append_tokens(run.desc, run.bt, k_new, block_sum, run.vb, head_w=run.head_w, ring=run.ring)
+        kk.kk_select_step_stable(run.desc, run.bt, sp.W, run.vb, sp.K, 20, 0.5, hist, run.idx, stab=stab,
+                                 top_scores=run.top, head_w=run.head_w, ring=run.ring, workspace=run.step_ws)
         kk.kk_compact_table(run.idx, run.bt, sel_pages, sel_count=sel_count)
 
-    out["decode_step_us"] = graph_time_us(decode_step, dev, stream)
-    if kk.kk_device_error() != 0:
-        raise RuntimeError("device error in the selector legs")
-    return out
+    run.fill_ring()
+    return graph_time_us(decode_step, dev, stream)
 
 
 def e2e_leg(args, run, dev, stream):
@@ -662,13 +715,15 @@ def record_paged(name, dev, stream, peak_gbs, steps, warmup, flush, coarse=False
            "requests": spec.R, "dtype": spec.dtype}
     fits_l2 = spec.k_bytes() < L2_FLUSH_BYTES
     rec["pool"] = pool_record(run, dev, stream, peak_gbs, steps, warmup, flush if fits_l2 else None)
-    rec["pool"]["l2"] = "flushed (256 MB write) before every call" if fits_l2 else "inputs larger than L2"
+    rec["pool"]["l2"] = "flushed (256 MB read) before every call" if fits_l2 else "inputs larger than L2"
     rec["pool"]["kernel"] = "kk_pool_blocks" + (" (4 launches)" if spec.weighted else "")
     if fits_l2:
         warm = pool_record(run, dev, stream, peak_gbs, steps, warmup, None)
         warm["l2"] = "warm: back to back, the 50 MB cache stays in the 129 MB L2 (a frac above 1 is L2 bandwidth)"
         rec["pool_warm_l2"] = warm
     rec["select"] = select_record(run, dev, stream, peak_gbs)
+    rec["select_ring"] = select_record(run, dev, stream, peak_gbs, ring=True)
+    rec["decode_step_us_cuda_graph"] = decode_step_us(run, dev, stream)
     if coarse:
         for group in (64, 512):
             out = torch.zeros((spec.R, -(-max(spec.nb) // group), spec.D), device=dev)
@@ -677,7 +732,7 @@ def record_paged(name, dev, stream, peak_gbs, steps, warmup, flush, coarse=False
             nbytes = spec.total_blocks * spec.D * 4 + out.numel() * 4
             rec[f"coarse_means_{group}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
                                             "frac": nbytes / (us * 1e-6) / 1e9 / peak_gbs,
-                                            "l2": "flushed before every call"}
+                                            "l2": "flushed (256 MB read) before every call"}
     if kk.kk_device_error() != 0:
         raise RuntimeError(f"device error in workload {name}")
     del run
@@ -687,7 +742,7 @@ def record_paged(name, dev, stream, peak_gbs, steps, warmup, flush, coarse=False
 
 def run_pool_gpu(dev, warmup: int, steps: int, peaks):
     """Shared-pool scoring: kk_score_pool_batched over the whole pool, L2
-    flushed (256 MB write) before every timed call; only the call is timed.
+    flushed (256 MB read) before every timed call; only the call is timed.
     Then the pool as documents through the three-level selection."""
     import torch
 
@@ -701,7 +756,7 @@ def run_pool_gpu(dev, warmup: int, steps: int, peaks):
     ws = torch.empty(kk.kk_score_pool_batched_workspace_bytes(R, N, K), dtype=torch.uint8, device=dev)
     idx = torch.zeros((R, K), dtype=torch.int32, device=dev)
     top = torch.zeros((R, K), device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     call = lambda: kk.kk_score_pool_batched(A, V, Mt, K, idx, top, ws)  # noqa: E731
     with ClockSampler(dev.index or 0) as clocks:
@@ -719,7 +774,7 @@ def run_pool_gpu(dev, warmup: int, steps: int, peaks):
     tflops = flops / (med * 1e-3) / 1e12
     nbytes = in_bytes + idx.numel() * 8
     return {"workload": WORKLOAD_NAMES["pool"], "us": med * 1e3, "us_warm_l2": warm_ms * 1e3,
-            "l2": "flushed (256 MB write) before every timed call", "blocks_scored_per_s": owned / (med * 1e-3),
+            "l2": "flushed (256 MB read) before every timed call", "blocks_scored_per_s": owned / (med * 1e-3),
             "tensor": {"flops": flops, "tflops": tflops, "peak_tflops": float(peaks["bf16_tflops"]),
                        "frac": tflops / float(peaks["bf16_tflops"])},
             "hbm": {"bytes": nbytes, "gbs": nbytes / (med * 1e-3) / 1e9,
@@ -765,7 +820,7 @@ def sub_records(args, dev, peaks):
 
     stream = torch.cuda.current_stream(dev)
     peak = float(peaks["hbm_gbs"])
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     recs = {}
     steps, warm = max(args.steps, 10), max(args.warmup, 3)
     recs["tiny"] = record_paged("tiny", dev, stream, peak, max(steps, 50), warm, flush)
@@ -877,6 +932,7 @@ def main():
                                 "frac_in_step": step_bytes(spec) / (res["select_ms"] * 1e-3) / 1e9 / peak,
                                 "frac_back_to_back": sel["roofline_frac_back_to_back"],
                                 "frac_cuda_graph": sel["roofline_frac_cuda_graph"]},
+        "score_topk_ring": res["select_ring"],
         "anchor_then_score_topk_us_cuda_graph": res["two_launch_us"],
         "score_topk_stable_us_back_to_back": res["stable_us"],
         "decode_step_us_cuda_graph": res["decode_step_us"],

@@ -25,10 +25,9 @@
  *  - The first call on a device looks up the device error word's address;
  *    make that first call outside CUDA stream capture.
  *  - The decode-step calls (kk_select_step, kk_score_topk, kk_topk and their
- *    stable forms) may split each of up to 64 very long requests over several
- *    clusters of CTAs, which meet in a fixed 512 KB device buffer of the
- *    library: on one device, issue those calls in stream order (one stream,
- *    or streams ordered by events), never two at once.
+ *    stable forms) keep no state in the library: calls on different streams
+ *    may run at once as long as they do not share a workspace (see
+ *    kk_step_options).
  */
 #ifndef KK_H_
 #define KK_H_
@@ -88,6 +87,24 @@ typedef struct kk_block_table {
   int32_t num_requests;    /* R */
   int32_t max_blocks;      /* host bound of nb_r */
 } kk_block_table;
+
+/*
+ * Diagnostics for failure-detection tests (no part of the method). Every spin
+ * of a kernel on an mbarrier is bounded: past the limit it records
+ * KK_ERR_TIMEOUT in the device error word, waits (again bounded) for the
+ * copies it has in flight, frees what it holds and returns, so the context
+ * stays usable.
+ * kk_debug_set_wait_limit: the limit, in ns, of every wait of the launches
+ *   that follow (0 restores the default of 1 s). Launches already captured in
+ *   a CUDA graph keep the limit they were captured with.
+ * kk_debug_skip_pool_copy: the next launch of the persistent pool kernel
+ *   (kk_pool_blocks on at least one block per SM) issues no copy for TMA box
+ *   `box` of its first CTA (counted from 0 in that CTA's issue order), so the
+ *   wait for that box runs out; -1 cancels. The request is used up by that
+ *   launch. KK_ERR_INVALID for box < -1.
+ */
+kk_status kk_debug_set_wait_limit(uint64_t ns);
+kk_status kk_debug_skip_pool_copy(int64_t box);
 
 /* Name of a status code (static string). */
 const char* kk_status_str(kk_status s);
@@ -187,6 +204,67 @@ kk_status kk_score(const float* vb, int32_t D, int32_t num_pages, const kk_block
                    const float* va, float* scores, cudaStream_t stream);
 
 /*
+ * Anchor ring: the per-token pooled Keys of each request's most recent
+ * tokens, kept as the tokens are written, so that a decode step forms
+ * v_anchor from W rows of head_dim floats instead of re-reading W tokens'
+ * Keys of every layer and head from the cache. The anchor is a mean over
+ * tokens of a weighted sum over (layer, head) [KK §5.2 step 1], so it can
+ * be summed token by token:
+ *   rows[r][t % slots][d] = sum_{l,h} w[l,h] * K[l, page(t), h, t % bs, d]
+ *   pos[r][t % slots]     = t      (-1: the slot holds no token)
+ * with w = head_w[r][l*H+h] when the ring is written with head weights, else
+ * 1. kk_anchor_ring_fill writes it from the cache (for example after a
+ * prefill); kk_append_tokens keeps it current token by token. A ring written
+ * with head weights must be read with the same head weights.
+ * rows: device float [R][slots][head_dim], 16-byte aligned (else
+ * KK_ERR_UNSUPPORTED); pos: device int32 [R][slots]; 1 <= slots <= 1024. The
+ * ring belongs to the caller.
+ */
+typedef struct kk_anchor_ring {
+  float* rows;
+  int32_t* pos;
+  int32_t slots;
+} kk_anchor_ring;
+
+/*
+ * Writes the anchor ring of every request from the K cache: for request r
+ * with T = seq_lens[r], the tokens t in [T - min(slots, T), T) (slot
+ * t % slots), and pos = -1 in every other slot. head_w: nullable device
+ * [R][L*H] (the weights the ring carries).
+ */
+kk_status kk_anchor_ring_fill(const kk_kcache_desc* kc, const kk_block_table* bt, const float* head_w,
+                              const kk_anchor_ring* ring, cudaStream_t stream);
+
+/*
+ * Options of the decode-step calls (the whole struct may be NULL):
+ *  - ring (kk_select_step and kk_select_step_stable only; nullable): take
+ *    v_anchor from this ring instead of from the K cache:
+ *      va[r] = (1/W') * sum_{T-W' <= t < T} rows[r][t % slots]   (/ (L*H) when head_w is NULL)
+ *    The result is kk_anchor's, summed in another order. W <= slots. A slot
+ *    whose pos is not the token expected there counts as zero and is
+ *    reported through the device error word (KK_ERR_BAD_INDEX).
+ *  - workspace, workspace_bytes (nullable): device memory, 16-byte aligned,
+ *    of at least kk_select_step_workspace_bytes(R, max_blocks, K) bytes. With
+ *    it, a few very long requests are each split over several clusters of
+ *    CTAs (more SMs per request); the clusters of a request meet at a counter
+ *    in the workspace, which the last of them sets back to zero. Zero the
+ *    workspace once before its first use (cudaMemsetAsync), and again after a
+ *    call that did not run to completion (a CUDA error); a counter found past
+ *    its bound is reported as KK_ERR_BAD_INDEX. Without a workspace, every
+ *    request is served by one cluster. Calls that may run at once need
+ *    separate workspaces.
+ */
+typedef struct kk_step_options {
+  const kk_anchor_ring* ring;
+  void* workspace;
+  size_t workspace_bytes;
+} kk_step_options;
+
+/* Workspace bytes that let the decode-step calls split long requests (0:
+ * tables of at most max_blocks blocks per request are never split). */
+size_t kk_select_step_workspace_bytes(int32_t R, int32_t max_blocks, int32_t K);
+
+/*
  * kk_topk - top-K selection [KK §5.2 step 4]. For each request r, among
  * scores[offsets[r] .. offsets[r+1]) the K largest, ordered by score
  * descending, equal scores by lower index. idx[r][k] is the logical index
@@ -195,13 +273,13 @@ kk_status kk_score(const float* vb, int32_t D, int32_t num_pages, const kk_block
  * offsets: device [R+1]; max_n bounds every range; 1 <= K <= 256.
  */
 kk_status kk_topk(const float* scores, const int32_t* offsets, int32_t R, int32_t max_n, int32_t K,
-                  int32_t* idx, float* top_scores, cudaStream_t stream);
+                  int32_t* idx, float* top_scores, const kk_step_options* opt, cudaStream_t stream);
 
 /* kk_score followed by kk_topk in one launch; `scores` (nullable) receives
  * the full score vector as kk_score would. */
 kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                         const float* va, int32_t K, int32_t* idx, float* top_scores, float* scores,
-                        cudaStream_t stream);
+                        const kk_step_options* opt, cudaStream_t stream);
 
 /*
  * One decode step of the selector in one launch: kk_anchor, kk_score and
@@ -210,7 +288,7 @@ kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_
  */
 kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
                          const float* head_w, const float* vb, int32_t K, float* va, int32_t* idx,
-                         float* top_scores, float* scores, cudaStream_t stream);
+                         float* top_scores, float* scores, const kk_step_options* opt, cudaStream_t stream);
 
 /*
  * Stability filter [KK §5.3] fused into scoring: kk_score_topk and
@@ -231,11 +309,12 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
 kk_status kk_score_topk_stable(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                                const float* va, int32_t K, int32_t stab_window, float theta,
                                uint32_t* hist, float* stab, int32_t* idx, float* top_scores, float* scores,
-                               cudaStream_t stream);
+                               const kk_step_options* opt, cudaStream_t stream);
 kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
                                 const float* head_w, const float* vb, int32_t K, int32_t stab_window,
                                 float theta, uint32_t* hist, float* stab, float* va, int32_t* idx,
-                                float* top_scores, float* scores, cudaStream_t stream);
+                                float* top_scores, float* scores, const kk_step_options* opt,
+                                cudaStream_t stream);
 
 /*
  * The selected blocks as a table for the attention kernel [KK §5.2 step 4]
@@ -266,10 +345,13 @@ kk_status kk_compact_table(const int32_t* idx, int32_t K, const kk_block_table* 
  * [num_pages][D], caller-owned state carried from token to token; vb: the
  * v_b table of kk_pool_blocks. A request whose table disagrees with seq_lens
  * or holds a bad page is skipped and reported through the device error word.
- * Blocks must not be shared between the requests of one call.
+ * Blocks must not be shared between the requests of one call. ring
+ * (nullable): the token's pooled Keys also go to its anchor ring slot
+ * ((seq_lens[r] - 1) % slots, with its position), weighted as block_sum is.
  */
 kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, const void* k_new,
-                           const float* head_w, float* block_sum, float* vb, cudaStream_t stream);
+                           const float* head_w, float* block_sum, float* vb, const kk_anchor_ring* ring,
+                           cudaStream_t stream);
 
 /*
  * Hierarchical selection Grid -> Chunk -> Page [KK §5.1]. A Chunk is
@@ -283,7 +365,8 @@ kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, c
  *                      (device float [R][C_max][D], C_max = ceil(max_blocks / chunk_pages))
  *   grid_reps[r][g]  = mean of chunk_reps[r][c], c in Grid g
  *                      (device float [R][G_max][D], G_max = ceil(C_max / grid_chunks))
- * Levels past a request's end are zero. Call it when blocks change (write time).
+ * Levels past a request's end are zero. Call it when blocks change (write
+ * time). vb must be 16-byte aligned (else KK_ERR_UNSUPPORTED).
  *
  * kk_hier_select scores the levels against the anchor va (device float
  * [R][D]) with the affinity of kk_score and keeps, level by level,
@@ -370,7 +453,8 @@ kk_status kk_hier_select_pool(const uint16_t* A, const uint16_t* M, const uint32
  * mean of its children's): for request r and group g,
  *   out[r][g][d] = mean over j in [g*group, min((g+1)*group, nb_r)) of vb[pages[offsets[r]+j]][d]
  * out: device [R][ceil(max_blocks/group)][D]; groups past a request's last
- * block are written as zero. D in {32, 64, 128, 256}, group >= 1.
+ * block are written as zero. D in {32, 64, 128, 256}, group >= 1; vb
+ * 16-byte aligned (else KK_ERR_UNSUPPORTED).
  */
 kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                           int32_t group, float* out, cudaStream_t stream);

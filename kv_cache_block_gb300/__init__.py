@@ -11,7 +11,8 @@ _BINDING = (
     "BlockTable", "KKError", "kcache_desc", "kk_anchor", "kk_coarse_means", "kk_device_error",
     "kk_head_variance", "kk_head_variance_workspace_bytes", "kk_pool_blocks", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static",
     "kk_score", "kk_score_pool_batched", "kk_score_pool_batched_workspace_bytes", "kk_score_topk",
-    "kk_select_step", "kk_topk",
+    "kk_select_step", "kk_topk", "AnchorRing", "kk_anchor_ring_fill", "kk_append_tokens",
+    "kk_select_step_workspace_bytes",
 )
 __all__ = ["kk", *_BINDING]
 

@@ -1,11 +1,13 @@
 // C ABI of the selector (include/kk.h): argument checks on the host, then
 // launches. Nothing here allocates device memory.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
 #include "../../include/kk.h"
 
+#include "kk_device.cuh"
 #include "kk_internal.h"
 
 namespace {
@@ -28,6 +30,11 @@ int* error_word() {
 }
 
 kk_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KK_OK : KK_ERR_CUDA; }
+
+// Limit of every bounded wait, and the one-shot request to leave a pool copy
+// out (failure-detection tests), both set by the diagnostic calls below.
+std::atomic<unsigned long long> g_wait_ns{kk::kDefaultWaitNs};
+std::atomic<long long> g_skip_box{-1};
 
 bool dim_supported(int dtype, int D) {
   if (D != 32 && D != 64 && D != 128 && D != 256) return false;
@@ -89,6 +96,17 @@ VarWorkspace carve(void* ws, int LH, int D, long long total_blocks) {
 }  // namespace
 
 extern "C" {
+
+kk_status kk_debug_set_wait_limit(uint64_t ns) {
+  g_wait_ns = ns ? (unsigned long long)ns : kk::kDefaultWaitNs;
+  return KK_OK;
+}
+
+kk_status kk_debug_skip_pool_copy(int64_t box) {
+  if (box < -1) return KK_ERR_INVALID;
+  g_skip_box = (long long)box;
+  return KK_OK;
+}
 
 const char* kk_status_str(kk_status s) {
   switch (s) {
@@ -173,6 +191,36 @@ kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table
   return variance_common(kc, bt, total_blocks, head_w_out, vb, workspace, workspace_bytes, stream);
 }
 
+// Decode-step options: the anchor ring (select steps only) and the split
+// workspace.
+static kk_status step_options(const kk_step_options* opt, bool allow_ring, kk::StepParams* p) {
+  if (!opt) return KK_OK;
+  if (opt->ring) {
+    const kk_anchor_ring* g = opt->ring;
+    if (!allow_ring || !g->rows || !g->pos || g->slots < 1 || g->slots > kk::kMaxW || p->W > g->slots)
+      return KK_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(g->rows) % 16 || reinterpret_cast<uintptr_t>(g->pos) % 4)
+      return KK_ERR_UNSUPPORTED;
+    p->ring_rows = g->rows;
+    p->ring_pos = g->pos;
+    p->ring_slots = g->slots;
+  }
+  if (opt->workspace) {
+    const size_t need = kk::step_workspace_bytes(p->bt.R, p->bt.max_blocks, p->K);
+    if (opt->workspace_bytes < need) return KK_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(opt->workspace) % 16) return KK_ERR_UNSUPPORTED;
+    const int cap = kk::step_split_cap(p->bt.max_blocks, p->K);
+    if (need > 0 && cap >= 2) {
+      char* w = static_cast<char*>(opt->workspace);
+      p->split_ctr = reinterpret_cast<unsigned long long*>(w);
+      p->split_keys = reinterpret_cast<uint64_t*>(w + (((size_t)p->bt.R * sizeof(unsigned long long) + 255) &
+                                                        ~size_t(255)));
+      p->split_cap = cap;
+    }
+  }
+  return KK_OK;
+}
+
 static kk_status step_common(kk::StepParams& p, cudaStream_t stream) {
   int* err = error_word();
   if (!err) return KK_ERR_CUDA;
@@ -220,8 +268,13 @@ kk_status kk_score(const float* vb, int32_t D, int32_t num_pages, const kk_block
   return step_common(p, stream);
 }
 
+size_t kk_select_step_workspace_bytes(int32_t R, int32_t max_blocks, int32_t K) {
+  if (R < 0 || max_blocks < 0 || K < 1 || K > kk::kMaxK) return 0;
+  return kk::step_workspace_bytes(R, max_blocks, K);
+}
+
 kk_status kk_topk(const float* scores, const int32_t* offsets, int32_t R, int32_t max_n, int32_t K,
-                  int32_t* idx, float* top_scores, cudaStream_t stream) {
+                  int32_t* idx, float* top_scores, const kk_step_options* opt, cudaStream_t stream) {
   if (R < 0 || R > 65535 || max_n < 0 || K < 1 || K > kk::kMaxK) return KK_ERR_INVALID;
   if (R == 0) return KK_OK;
   if (!scores || !offsets || !idx) return KK_ERR_INVALID;
@@ -233,12 +286,14 @@ kk_status kk_topk(const float* scores, const int32_t* offsets, int32_t R, int32_
   p.idx_out = idx;
   p.top_out = top_scores;
   p.flags = kk::kStepTopK | kk::kStepTopKFromScores;
+  kk_status st = step_options(opt, false, &p);
+  if (st != KK_OK) return st;
   return step_common(p, stream);
 }
 
 kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                         const float* va, int32_t K, int32_t* idx, float* top_scores, float* scores,
-                        cudaStream_t stream) {
+                        const kk_step_options* opt, cudaStream_t stream) {
   kk::StepParams p = {};
   kk_status st = score_args(vb, D, num_pages, bt, va, &p);
   if (st != KK_OK) return st;
@@ -248,12 +303,13 @@ kk_status kk_score_topk(const float* vb, int32_t D, int32_t num_pages, const kk_
   p.top_out = top_scores;
   p.scores_out = scores;
   p.flags = kk::kStepScore | kk::kStepTopK;
+  if ((st = step_options(opt, false, &p)) != KK_OK) return st;
   return step_common(p, stream);
 }
 
 kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
                          const float* head_w, const float* vb, int32_t K, float* va, int32_t* idx,
-                         float* top_scores, float* scores, cudaStream_t stream) {
+                         float* top_scores, float* scores, const kk_step_options* opt, cudaStream_t stream) {
   kk::StepParams p = {};
   kk_status st = check_kcache(kc, &p.kc);
   if (st != KK_OK) return st;
@@ -271,6 +327,7 @@ kk_status kk_select_step(const kk_kcache_desc* kc, const kk_block_table* bt, int
   p.top_out = top_scores;
   p.scores_out = scores;
   p.flags = kk::kStepAnchor | kk::kStepScore | kk::kStepTopK;
+  if ((st = step_options(opt, true, &p)) != KK_OK) return st;
   return step_common(p, stream);
 }
 
@@ -290,7 +347,7 @@ static kk_status stability_args(int32_t stab_window, float theta, uint32_t* hist
 kk_status kk_score_topk_stable(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                                const float* va, int32_t K, int32_t stab_window, float theta,
                                uint32_t* hist, float* stab, int32_t* idx, float* top_scores, float* scores,
-                               cudaStream_t stream) {
+                               const kk_step_options* opt, cudaStream_t stream) {
   kk::StepParams p = {};
   kk_status st = score_args(vb, D, num_pages, bt, va, &p);
   if (st != KK_OK) return st;
@@ -301,13 +358,15 @@ kk_status kk_score_topk_stable(const float* vb, int32_t D, int32_t num_pages, co
   p.top_out = top_scores;
   p.scores_out = scores;
   p.flags = kk::kStepScore | kk::kStepTopK;
+  if ((st = step_options(opt, false, &p)) != KK_OK) return st;
   return step_common(p, stream);
 }
 
 kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* bt, int32_t W,
                                 const float* head_w, const float* vb, int32_t K, int32_t stab_window,
                                 float theta, uint32_t* hist, float* stab, float* va, int32_t* idx,
-                                float* top_scores, float* scores, cudaStream_t stream) {
+                                float* top_scores, float* scores, const kk_step_options* opt,
+                                cudaStream_t stream) {
   kk::StepParams p = {};
   kk_status st = check_kcache(kc, &p.kc);
   if (st != KK_OK) return st;
@@ -326,6 +385,7 @@ kk_status kk_select_step_stable(const kk_kcache_desc* kc, const kk_block_table* 
   p.top_out = top_scores;
   p.scores_out = scores;
   p.flags = kk::kStepAnchor | kk::kStepScore | kk::kStepTopK;
+  if ((st = step_options(opt, true, &p)) != KK_OK) return st;
   return step_common(p, stream);
 }
 
@@ -340,8 +400,18 @@ kk_status kk_compact_table(const int32_t* idx, int32_t K, const kk_block_table* 
   return from_cuda(kk::launch_compact_table(idx, K, t, sel_pages, sel_logical, sel_count, err, stream));
 }
 
+// The anchor ring's pointers and size, checked on the host.
+static kk_status ring_args(const kk_anchor_ring* ring, kk::Ring* out) {
+  if (!ring || !ring->rows || !ring->pos || ring->slots < 1 || ring->slots > kk::kMaxW) return KK_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(ring->rows) % 16 || reinterpret_cast<uintptr_t>(ring->pos) % 4)
+    return KK_ERR_UNSUPPORTED;
+  *out = kk::Ring{ring->rows, ring->pos, ring->slots};
+  return KK_OK;
+}
+
 kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, const void* k_new,
-                           const float* head_w, float* block_sum, float* vb, cudaStream_t stream) {
+                           const float* head_w, float* block_sum, float* vb, const kk_anchor_ring* ring,
+                           cudaStream_t stream) {
   kk::KCache c;
   kk_status st = check_kcache(kc, &c);
   if (st != KK_OK) return st;
@@ -349,9 +419,25 @@ kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, c
   if ((st = check_table(bt, true, &t)) != KK_OK) return st;
   if (t.R > 0 && (!k_new || !block_sum || !vb)) return KK_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(k_new) % 16) return KK_ERR_UNSUPPORTED;
+  kk::Ring g = {};
+  if (ring && (st = ring_args(ring, &g)) != KK_OK) return st;
   int* err = error_word();
   if (!err) return KK_ERR_CUDA;
-  return from_cuda(kk::launch_append(c, t, k_new, head_w, block_sum, vb, err, stream));
+  return from_cuda(kk::launch_append(c, t, k_new, head_w, block_sum, vb, ring ? &g : nullptr, err, stream));
+}
+
+kk_status kk_anchor_ring_fill(const kk_kcache_desc* kc, const kk_block_table* bt, const float* head_w,
+                              const kk_anchor_ring* ring, cudaStream_t stream) {
+  kk::KCache c;
+  kk_status st = check_kcache(kc, &c);
+  if (st != KK_OK) return st;
+  kk::Table t;
+  if ((st = check_table(bt, true, &t)) != KK_OK) return st;
+  kk::Ring g;
+  if ((st = ring_args(ring, &g)) != KK_OK) return st;
+  int* err = error_word();
+  if (!err) return KK_ERR_CUDA;
+  return from_cuda(kk::launch_ring_fill(c, t, head_w, g, err, stream));
 }
 
 // Sizes of the hierarchical levels for a table whose longest request has
@@ -377,7 +463,7 @@ kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_b
   if (st != KK_OK) return st;
   if (!vb || !chunk_reps || !grid_reps || chunk_pages < 1 || grid_chunks < 1 || num_pages <= 0)
     return KK_ERR_INVALID;
-  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  if (!dim_supported(KK_BF16, D) || reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
   const long long C = ((long long)t.max_blocks + chunk_pages - 1) / chunk_pages;
   const long long G = (C + grid_chunks - 1) / grid_chunks;
   int* err = error_word();
@@ -489,7 +575,7 @@ kk_status kk_coarse_means(const float* vb, int32_t D, int32_t num_pages, const k
   kk_status st = check_table(bt, false, &t);
   if (st != KK_OK) return st;
   if (!vb || !out || group < 1 || num_pages <= 0) return KK_ERR_INVALID;
-  if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  if (!dim_supported(KK_BF16, D) || reinterpret_cast<uintptr_t>(vb) % 16) return KK_ERR_UNSUPPORTED;
   int* err = error_word();
   if (!err) return KK_ERR_CUDA;
   return from_cuda(kk::launch_coarse(vb, D, num_pages, t, group, out, err, stream));
@@ -512,5 +598,9 @@ kk_status check_weighted_args(const kk_kcache_desc* kc, const kk_block_table* bt
 }
 
 int* device_error_word() { return error_word(); }
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
+
+long long take_skip_box() { return g_skip_box.exchange(-1); }
 
 }  // namespace kk

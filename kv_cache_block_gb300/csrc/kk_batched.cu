@@ -58,6 +58,7 @@ struct GemmArgs {
   int mtiles;          // block tiles (128 pool blocks each)
   uint64_t* keys;      // [R][N] each anchor's candidate keys, contiguous, in pool order
   int mask_vec;     // mask rows allow 16-byte loads of a tile's four words
+  unsigned long long wait_ns;  // limit of every bounded wait
   int* err;
 };
 
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (i >= range_len(gg)) continue;
         const int j = range_lo(gg) + i;
         const int st = q % kStages;
-        if (q >= kStages && !mbar_wait_bounded(&empty[st], ((q / kStages) & 1) ^ 1, kWaitLimitNs)) {
+        if (q >= kStages && !mbar_wait_bounded(&empty[st], ((q / kStages) & 1) ^ 1, g.wait_ns)) {
           fail(kErrTimeout);
           break;
         }
@@ -211,13 +212,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-      if (!mbar_wait_bounded(bar_a, 0, kWaitLimitNs)) fail(kErrTimeout);
+      if (!mbar_wait_bounded(bar_a, 0, g.wait_ns)) fail(kErrTimeout);
       for (int k = 0, q = 0; q < ntiles && !*abort_flag; ++k) {
         const int gg = k % kGroups, i = k / kGroups;
         if (i >= range_len(gg)) continue;
         const int st = q % kStages;
-        if (!mbar_wait_bounded(&full[st], (q / kStages) & 1, kWaitLimitNs) ||
-            (i >= 1 && !mbar_wait_bounded(&acc_empty[gg], (i - 1) & 1, kWaitLimitNs))) {
+        if (!mbar_wait_bounded(&full[st], (q / kStages) & 1, g.wait_ns) ||
+            (i >= 1 && !mbar_wait_bounded(&acc_empty[gg], (i - 1) & 1, g.wait_ns))) {
           fail(kErrTimeout);
           break;
         }
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t w_next[4];
     int o_next;
     mask_load(len > 0 ? lo : ntiles, w_next, o_next);
-    bool ok = mbar_wait_bounded(bar_a, 0, kWaitLimitNs);
+    bool ok = mbar_wait_bounded(bar_a, 0, g.wait_ns);
     if (!ok) fail(kErrTimeout);
     const float inv_a = ok ? inv_norm(row_sq(sA, row)) : 0.f;
     for (int i = 0; i < len; ++i) {
@@ -311,12 +312,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // V-row norms of this tile (one row per thread), then release the
       // ring stage. The group leaves the loop together (a lone warp leaving
       // would strand the others at the named barrier).
-      ok = !*abort_flag && mbar_wait_bounded(&full[st], (q / kStages) & 1, kWaitLimitNs);
+      ok = !*abort_flag && mbar_wait_bounded(&full[st], (q / kStages) & 1, g.wait_ns);
       float* inv_v = inv_v_grp + (i & 1) * kBN;
       inv_v[row] = ok ? inv_norm(row_sq(sV + st * kTileBytes, row)) : 0.f;
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      ok = ok && mbar_wait_bounded(&acc_full[grp], i & 1, kWaitLimitNs);
+      ok = ok && mbar_wait_bounded(&acc_full[grp], i & 1, g.wait_ns);
       if (named_sync_or(bar_id, kGroupThreads, !ok)) {  // also orders the inv_v writes before the reads
         if (!ok) fail(kErrTimeout);
         break;
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (!mbar_wait_bounded(epi_done, 0, kWaitLimitNs)) flag_error(g.err, kErrTimeout);
+    if (!mbar_wait_bounded(epi_done, 0, g.wait_ns)) flag_error(g.err, kErrTimeout);
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -905,7 +906,7 @@ cudaError_t launch_pool_gemm(const uint16_t* A, const uint16_t* V, int rows, con
     CUtensorMap ma, mv;
     if (!make_map(&ma, A, R) || !make_map(&mv, V, rows)) return cudaErrorInvalidValue;
     GemmArgs g{mask, R, N, mask_words, L.tiles, coarse_rows, (rows - N) / kBN, coarse, offsets, L.mtiles, keys,
-               mask_vec, err};
+               mask_vec, wait_limit_ns(), err};
     // programmatic dependent launch: the GEMM's producer and MMA start while
     // the offsets kernel runs; the epilogue waits for it (griddepcontrol.wait)
     cudaLaunchConfig_t cfg = {};

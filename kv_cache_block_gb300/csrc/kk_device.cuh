@@ -208,6 +208,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
+// Every spin on an mbarrier is bounded: kernels take the limit as an
+// argument (1 s unless a diagnostic call set another; the host side keeps it).
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 }  // namespace kk

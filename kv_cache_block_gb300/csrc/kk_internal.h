@@ -76,10 +76,26 @@ struct StepParams {
   float* stab_out;
   int stab_w;
   float stab_theta;
+  // anchor ring (nullable rows): the anchor is the mean of the W' newest
+  // rows[r][t % ring_slots], checked against pos
+  const float* ring_rows;
+  const int* ring_pos;
+  int ring_slots;
+  // split scratch (nullable): per-request counters of the clusters done
+  // (zero between calls) and each cluster's sorted list, split_cap lists a
+  // request
+  unsigned long long* split_ctr;
+  uint64_t* split_keys;
+  int split_cap;
+  unsigned long long wait_ns;  // limit of every bounded wait
   int* err;
   int splits;  // clusters per request (set by the launcher; > 1 for very long requests)
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
+// Lists a request may be split into (a power of two), and the workspace that
+// holds them for R requests of at most max_blocks blocks (0: never split).
+int step_split_cap(int max_blocks, int K);
+size_t step_workspace_bytes(int R, int max_blocks, int K);
 
 // kk_batched.cu
 // Shared-pool GEMM (kk_batched.cu): each anchor's candidate keys (score,
@@ -115,8 +131,15 @@ cudaError_t launch_score_pool_batched(const uint16_t* A, const uint16_t* V, cons
 // kk_write.cu
 cudaError_t launch_compact_table(const int* idx, int K, const Table& bt, int* out_pages, int* out_logical,
                                  int* out_count, int* err, cudaStream_t s);
+struct Ring {
+  float* rows;  // [R][slots][D]
+  int* pos;     // [R][slots]
+  int slots;
+};
 cudaError_t launch_append(const KCache& kc, const Table& bt, const void* k_new, const float* head_w,
-                          float* block_sum, float* vb, int* err, cudaStream_t s);
+                          float* block_sum, float* vb, const Ring* ring, int* err, cudaStream_t s);
+cudaError_t launch_ring_fill(const KCache& kc, const Table& bt, const float* head_w, const Ring& ring, int* err,
+                             cudaStream_t s);
 
 // kk_hier.cu: members of one level of the hierarchical selection held in
 // shared memory at once (Grids, active Chunks, active blocks of a request)
@@ -145,6 +168,12 @@ cudaError_t launch_pool_tma_slices(const KCache& kc, const Table& bt, long long 
 
 // kk_api.cu (used by kk_static.cu)
 int* device_error_word();
+// kk_api.cu: the limit of every bounded wait (kDefaultWaitNs unless a
+// diagnostic call set another), and a one-shot request, for failure-detection
+// tests, that the next persistent pool launch leave TMA box `box` of its first
+// CTA uncopied (-1: none; taking it clears it).
+unsigned long long wait_limit_ns();
+long long take_skip_box();
 
 // kk_coarse.cu
 cudaError_t launch_coarse(const float* vb, int D, int num_pages, const Table& bt, int group,

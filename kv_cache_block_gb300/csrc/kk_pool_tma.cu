@@ -50,6 +50,8 @@ struct PoolTmaArgs {
   int nhb, nlb;       // boxes per block along heads and layers
   int pos[4];         // tensor-map position (1..4) of each Dim
   int ext[5];         // box extent at each tensor-map position
+  unsigned long long wait_ns;  // limit of every bounded wait
+  long long skip_box;          // failure-detection tests: CTA 0 leaves this box uncopied (-1: none)
   int* err;
 };
 
@@ -132,12 +134,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           for (int hbi = 0; hbi < a.nhb && alive; ++hbi)
             for (int tbi = 0; tbi < nt; ++tbi) {
               const int st = (int)(k % kStages);
-              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, kWaitLimitNs)) ||
+              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, a.wait_ns)) ||
                   *abort_flag) {
                 if (!*abort_flag) flag_error(a.err, kErrTimeout);
                 *abort_flag = 1;
                 alive = false;
                 break;
+              }
+              if (blockIdx.x == 0 && (long long)k == a.skip_box) {
+                ++k;  // no copy and no arrival: the consumers' wait for this box runs out
+                continue;
               }
               const int ct = tbi * a.tb, ch = hbi * a.hb, cl = lbi * a.lb;
               mbar_arrive_expect_tx(&full[st], box_bytes);
@@ -147,12 +153,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               ++k;
             }
       }
-      // no copy may still be writing shared memory when the CTA exits
+      // no copy may still be writing shared memory when the CTA exits: every
+      // box of the last kStages is waited for, each wait bounded (a box whose
+      // wait runs out does not end the drain of the ones after it)
       for (uint32_t j = k > (uint32_t)kStages ? k - kStages : 0; j < k; ++j)
-        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, kWaitLimitNs)) {
-          flag_error(a.err, kErrTimeout);
-          break;
-        }
+        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, a.wait_ns)) flag_error(a.err, kErrTimeout);
     }
     return;
   }
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         for (int tbi = 0; tbi < nt; ++tbi, ++k) {
           if (!alive) continue;
           const int st = (int)(k % kStages);
-          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, kWaitLimitNs);
+          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, a.wait_ns);
           ok = __all_sync(kFull, ok);
           if (!ok) {
             if (lane == 0 && !*abort_flag) flag_error(a.err, kErrTimeout);
@@ -278,6 +283,7 @@ struct SliceTmaArgs {
   int pos[4];
   float* S;
   float* Q;
+  unsigned long long wait_ns;
   int* err;
 };
 
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           for (int hbi = 0; hbi < a.nhb && alive; ++hbi)
             for (int tbi = 0; tbi < nt; ++tbi) {
               const int st = (int)(k % kStages);
-              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, kWaitLimitNs)) ||
+              if ((k >= kStages && !mbar_wait_bounded(&empty[st], ((k / kStages) & 1) ^ 1, a.wait_ns)) ||
                   *abort_flag) {
                 if (!*abort_flag) flag_error(a.err, kErrTimeout);
                 *abort_flag = 1;
@@ -379,10 +385,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             }
       }
       for (uint32_t j = k > (uint32_t)kStages ? k - kStages : 0; j < k; ++j)
-        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, kWaitLimitNs)) {
-          flag_error(a.err, kErrTimeout);
-          break;
-        }
+        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, a.wait_ns)) flag_error(a.err, kErrTimeout);
     }
     return;
   }
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         for (int tbi = 0; tbi < nt; ++tbi, ++k) {
           if (!alive) continue;
           const int st = (int)(k % kStages);
-          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, kWaitLimitNs);
+          bool ok = !*abort_flag && mbar_wait_bounded(&full[st], (k / kStages) & 1, a.wait_ns);
           ok = __all_sync(kFull, ok);
           if (!ok) {
             if (lane == 0 && !*abort_flag) flag_error(a.err, kErrTimeout);
@@ -612,6 +615,8 @@ cudaError_t launch_pool_tma(const KCache& kc, const int* pages, const int* n_val
   a.nhb = kc.H / pl.hb;
   a.nlb = kc.L / pl.lb;
   a.err = err;
+  a.wait_ns = wait_limit_ns();
+  a.skip_box = take_skip_box();
   for (int i = 0; i < 4; ++i) a.pos[i] = pl.pos[i];
   for (int i = 0; i < 5; ++i) a.ext[i] = pl.ext[i];
   const int grid = std::min(n, sms);
@@ -643,6 +648,7 @@ cudaError_t launch_pool_tma_slices(const KCache& kc, const Table& bt, long long 
   a.S = S;
   a.Q = Q;
   a.err = err;
+  a.wait_ns = wait_limit_ns();
   const int grid = (int)std::min<long long>(total_blocks, sms);
   if (kc.dtype == 1) {
     switch (kc.D) {

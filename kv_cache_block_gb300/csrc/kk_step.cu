@@ -18,6 +18,7 @@
 #include <type_traits>
 
 #include "kk_device.cuh"
+#include "kk_pdl.cuh"
 #include "kk_internal.h"
 #include "kk_warp.cuh"
 
@@ -25,19 +26,18 @@ namespace kk {
 namespace {
 
 // Very long requests are split over several clusters: each writes its sorted
-// top-K list here, and the last one to finish (a per-request counter) merges
-// the lists into the request's output and resets the counter. Calls that
-// split a request share this scratch, so they must not run concurrently.
-constexpr int kSplitKeys = 65536;  // requests x splits x Kp
-constexpr int kSplitReq = 64;      // requests
-constexpr int kSplitPerWarp = 8;   // lists each warp folds in the final merge of K <= 32
-__device__ uint64_t g_split_keys[kSplitKeys];
-__device__ int g_split_count[kSplitReq];
+// top-K list to the caller's workspace, and the last one to count itself in
+// (a per-request counter in the workspace) merges the lists into the
+// request's output and sets the counter back to zero.
+constexpr int kSplitPerWarp = 8;     // lists each warp folds in the final merge of K <= 32
+constexpr int kSplitMinBlocks = 256;  // blocks per CTA below which a request is not split further
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kThreads;  // candidates per top-K tile
+constexpr int kMaxSplits = kSplitPerWarp * kThreads / 32;  // lists the final fold of K <= 32 takes
 constexpr int kStage = 64;  // v_b rows staged in shared memory by bulk copies
+static_assert(kMaxW * 8 >= kThreads * 16, "ring-mode partial rows fit the token-offset table");
 static_assert(kMergeSlots % kThreads == 0, "the split merge holds kMergeSlots / kThreads keys a thread");
 static_assert(kSplitPerWarp * 32 * kWarps <= kMergeSlots, "the final fold stages its lists in the merge buffer");
 
@@ -47,7 +47,7 @@ struct StepSmem {
   float part[kMaxCluster][D];  // anchor partial of each CTA of the cluster
   float wpart[kWarps][D];
   float va[D];
-  long long tok[kMaxW];  // byte offset of each anchor token row (page, slot)
+  alignas(16) long long tok[kMaxW];  // byte offset of each anchor token row (page, slot); ring mode: sums
   float w[kMaxLH];
   int pg[kTile];
   uint64_t keys[kTile];
@@ -153,6 +153,13 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   const int K = p.K;
   const int Kp = K <= 1 ? 1 : 1 << (32 - __clz(K - 1));  // next power of two >= K
 
+  // launched early behind the previous kernel of the stream (for example the
+  // decode step's append): wait for it before touching global memory. The
+  // next kernel is not let in early: a following step kernel's clusters,
+  // parked on the SMs, would keep this one's clusters from being placed
+  // (measured: 32 requests x 8 CTAs back to back, 15.8 -> 20.8 us per step).
+  pdl_wait();
+
   // The first remote shared-memory access must follow a cluster barrier that
   // every CTA has arrived at; arrive now, wait just before that access.
   bool start_waited = true;
@@ -186,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   // ---- prefetch: one round of page-id loads for the anchor's token rows and
   // the first tile's blocks, then bulk copies of that tile's v_b rows -------
   constexpr bool kAnchorFits = D <= 32 * Vec16<T>::kElems;  // a row is at most 32 vectors
+  const bool ring = p.ring_rows != nullptr;                 // anchor from the anchor ring
   const int w_eff = min(p.W, T_r);
-  if (kAnchorFits && do_anchor) {
+  if (kAnchorFits && do_anchor && !ring) {
     constexpr int ES = elem_bytes<T>();
     for (int i = tid; i < w_eff; i += kThreads) {
       const int pos = T_r - w_eff + i;
@@ -234,7 +242,60 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   }
 
   // ---- stage 1: anchor -----------------------------------------------------
-  if (kAnchorFits && do_anchor) {
+  if (do_anchor && ring) {
+    // Every CTA sums the W' newest ring rows itself (W' * D floats, mostly
+    // from L2): thread (rr, c4) takes the 16-byte column c4 of rows rr,
+    // rr + RP, ..., loading each row's slot position and values together (one
+    // round trip a batch); a row whose slot does not hold the expected token
+    // counts as zero and is reported. The RP partial rows are then added
+    // through shared memory (the token-offset table is not used in this mode).
+    constexpr int V4 = D / 4, RP = kThreads / V4;
+    constexpr int kRowUnroll = 4;
+    const int c4 = tid % V4, rr = tid / V4;
+    const long long rbase = (long long)r * p.ring_slots;
+    const float4* rows4 = reinterpret_cast<const float4*>(p.ring_rows);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = rr; i0 < w_eff; i0 += RP * kRowUnroll) {
+      float4 v[kRowUnroll];
+      int ps[kRowUnroll], tt[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int i = i0 + u * RP;
+        const bool valid = i < w_eff;
+        tt[u] = T_r - 1 - i;
+        const long long slot = rbase + (valid ? tt[u] % p.ring_slots : 0);
+        ps[u] = valid ? __ldg(p.ring_pos + slot) : -2;
+        v[u] = valid ? __ldg(rows4 + slot * V4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        if (ps[u] == tt[u]) {
+          acc.x += v[u].x;
+          acc.y += v[u].y;
+          acc.z += v[u].z;
+          acc.w += v[u].w;
+        } else if (ps[u] != -2 && c4 == 0) {
+          flag_error(p.err, kErrBadIndex);
+        }
+      }
+    }
+    float4* red = reinterpret_cast<float4*>(sm.tok);
+    red[tid] = acc;
+    __syncthreads();
+    const int LH = p.kc.L * p.kc.H;
+    const float scale =
+        w_eff > 0 ? (p.head_w ? 1.f / (float)w_eff : 1.f / ((float)w_eff * (float)LH)) : 0.f;
+    if (tid < D) {
+      const float* redf = reinterpret_cast<const float*>(red);
+      float v = 0.f;
+#pragma unroll 8
+      for (int q = 0; q < RP; ++q) v += redf[(q * V4 + tid / 4) * 4 + (tid & 3)];
+      v *= scale;
+      sm.va[tid] = v;
+      if (crank == 0 && sp == 0 && p.va_out) p.va_out[(long long)r * D + tid] = v;
+    }
+    __syncthreads();
+  } else if (kAnchorFits && do_anchor) {
     constexpr int EPV = Vec16<T>::kElems;
     constexpr int V16 = kAnchorFits ? D / EPV : 32;
     constexpr int RPW = 32 / V16;
@@ -351,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
 #pragma unroll
       for (int e = 0; e < RowSlice<D>::kPer; ++e) t = fmaf(a.v[e], a.v[e], t);
       na2 = warp_sum(t);
-      if (nstage > 0 && !mbar_wait_bounded(&sm.bar, 0, kWaitLimitNs)) {
+      if (nstage > 0 && !mbar_wait_bounded(&sm.bar, 0, p.wait_ns)) {
         staged_ok = false;
         if (tid == 0) flag_error(p.err, kErrTimeout);
       }
@@ -503,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     float* top_out = p.top_out ? p.top_out + (long long)r * K : nullptr;
     // the place of a ranked key: the request's output, or (a split request)
     // this cluster's sorted list in the scratch
-    uint64_t* slist = S > 1 ? g_split_keys + ((long long)r * S + sp) * Kp : nullptr;
+    uint64_t* slist = S > 1 ? p.split_keys + ((long long)r * p.split_cap + sp) * Kp : nullptr;
     auto emit = [&](int rank, uint64_t k) {
       if (slist) {
         slist[rank] = k;
@@ -618,11 +679,18 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         __syncthreads();
       }
       if (crank == 0) {
-        if (tid == 0) sm.wn[0] = atomicAdd(&g_split_count[r], 1) == S - 1 ? 1 : 0;
+        // count this cluster in; the last one merges and sets the counter
+        // back to zero for the next call (a count at or past S means the
+        // workspace was not zeroed before its first use: reported)
+        if (tid == 0) {
+          const unsigned long long seen = atomicAdd(p.split_ctr + r, 1ull);
+          if (seen >= (unsigned long long)S) flag_error(p.err, kErrBadIndex);
+          sm.wn[0] = seen == (unsigned long long)(S - 1) ? 1 : 0;
+        }
         __syncthreads();
         if (sm.wn[0]) {
           __threadfence();
-          const uint64_t* lists = g_split_keys + (long long)r * S * Kp;
+          const uint64_t* lists = p.split_keys + (long long)r * p.split_cap * Kp;
           if (Kp <= 32) {
             // each warp folds lists warp, warp + 8, ... (up to kSplitPerWarp,
             // loaded together into its shared-memory slots) into one
@@ -657,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
                   top_out[lane] = acc ? (stab ? stab_key_score(acc) : key_score(acc)) : -__int_as_float(0x7f800000);
               }
             }
-            if (tid == 0) g_split_count[r] = 0;
+            if (tid == 0) p.split_ctr[r] = 0ull;  // ready for the next call (and graph replays)
           } else {
             for (int f = tid; f < S * Kp; f += kThreads) sm.merge[f] = __ldcg(lists + f);
             __syncthreads();
@@ -694,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
               idx_out[i] = k ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
               if (top_out) top_out[i] = k ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
             }
-            if (tid == 0) g_split_count[r] = 0;
+            if (tid == 0) p.split_ctr[r] = 0ull;
           }
         }
       }
@@ -780,14 +848,10 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
 // (every cluster recomputes the anchor), within the scratch and the final
 // merge buffer.
 int pick_splits(const StepParams& p, const ClusterCaps& caps, int CL) {
-  constexpr int kSplitMinBlocks = 256;
-  if (!(p.flags & (kStepScore | kStepTopK)) || p.bt.R > kSplitReq) return 1;
-  const int Kp = p.K <= 1 ? 1 : 1 << (32 - __builtin_clz(p.K - 1));
+  if (!(p.flags & (kStepScore | kStepTopK)) || !p.split_ctr || p.split_cap < 2) return 1;
   int S = caps.active[CL] / p.bt.R;
   S = std::min(S, p.bt.max_blocks / (CL * kSplitMinBlocks));
-  S = std::min(S, kMergeSlots / Kp);
-  S = std::min(S, kSplitKeys / (p.bt.R * Kp));
-  S = std::min(S, kSplitPerWarp * kWarps);
+  S = std::min(S, p.split_cap);
   return std::max(S, 1);
 }
 
@@ -797,6 +861,7 @@ cudaError_t launch_typed(const StepParams& p0, cudaStream_t s) {
   cudaError_t e = setup_device<T, D>(&caps);
   if (e != cudaSuccess) return e;
   StepParams p = p0;
+  p.wait_ns = wait_limit_ns();
   const int CL = pick_cluster(p, caps);
   p.splits = pick_splits(p, caps, CL);
   cudaLaunchConfig_t cfg = {};
@@ -804,17 +869,34 @@ cudaError_t launch_typed(const StepParams& p0, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = sizeof(StepSmem<D>);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, step_kernel<T, D>, p);
 }
 
 }  // namespace
+
+int step_split_cap(int max_blocks, int K) {
+  const int Kp = K <= 1 ? 1 : 1 << (32 - __builtin_clz(K - 1));
+  int cap = std::min(kMergeSlots / Kp, kMaxSplits);
+  cap = std::min(cap, max_blocks / kSplitMinBlocks);
+  return cap >= 2 ? cap : 0;
+}
+
+size_t step_workspace_bytes(int R, int max_blocks, int K) {
+  const int cap = step_split_cap(max_blocks, K);
+  if (cap == 0 || R <= 0) return 0;
+  const int Kp = K <= 1 ? 1 : 1 << (32 - __builtin_clz(K - 1));
+  const size_t words = ((size_t)R * sizeof(unsigned long long) + 255) & ~size_t(255);
+  return words + (size_t)R * cap * Kp * sizeof(uint64_t);
+}
 
 cudaError_t launch_step(const StepParams& p, cudaStream_t s) {
   if (p.bt.R == 0) return cudaSuccess;

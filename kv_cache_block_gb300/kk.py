@@ -54,14 +54,26 @@ class kk_block_table(ctypes.Structure):
     ]
 
 
+class kk_anchor_ring(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("slots", ctypes.c_int32)]
+
+
+class kk_step_options(ctypes.Structure):
+    _fields_ = [("ring", ctypes.POINTER(kk_anchor_ring)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with `python -m kv_cache_block_gb300.build`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     KC, BT = ctypes.POINTER(kk_kcache_desc), ctypes.POINTER(kk_block_table)
+    RG, OP = ctypes.POINTER(kk_anchor_ring), ctypes.POINTER(kk_step_options)
     sig = {
         "kk_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "kk_debug_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64]),
+        "kk_debug_skip_pool_copy": (ctypes.c_int, [I64]),
         "kk_device_error": (ctypes.c_int, [P, ctypes.POINTER(I32)]),
         "kk_pool_blocks": (ctypes.c_int, [KC, P, P, I32, P, I32, P, P, P]),
         "kk_head_variance_workspace_bytes": (SZ, [KC, I32, I32]),
@@ -70,15 +82,17 @@ def _load():
         "kk_pool_blocks_weighted_static": (ctypes.c_int, [KC, BT, I32, P, P, P]),
         "kk_anchor": (ctypes.c_int, [KC, BT, I32, P, P, P]),
         "kk_score": (ctypes.c_int, [P, I32, I32, BT, P, P, P]),
-        "kk_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
-        "kk_score_topk": (ctypes.c_int, [P, I32, I32, BT, P, I32, P, P, P, P]),
-        "kk_select_step": (ctypes.c_int, [KC, BT, I32, P, P, I32, P, P, P, P, P]),
-        "kk_score_topk_stable": (ctypes.c_int, [P, I32, I32, BT, P, I32, I32, F, P, P, P, P, P, P]),
-        "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, P]),
+        "kk_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, OP, P]),
+        "kk_score_topk": (ctypes.c_int, [P, I32, I32, BT, P, I32, P, P, P, OP, P]),
+        "kk_select_step": (ctypes.c_int, [KC, BT, I32, P, P, I32, P, P, P, P, OP, P]),
+        "kk_score_topk_stable": (ctypes.c_int, [P, I32, I32, BT, P, I32, I32, F, P, P, P, P, P, OP, P]),
+        "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, OP, P]),
         "kk_compact_table": (ctypes.c_int, [P, I32, BT, P, P, P, P]),
         "kk_hier_reps": (ctypes.c_int, [P, I32, I32, BT, I32, I32, P, P, P]),
         "kk_hier_select": (ctypes.c_int, [P, I32, I32, BT, P, P, P, I32, I32, I32, I32, I32, I32, P, P, P, P]),
-        "kk_append_tokens": (ctypes.c_int, [KC, BT, P, P, P, P, P]),
+        "kk_append_tokens": (ctypes.c_int, [KC, BT, P, P, P, P, RG, P]),
+        "kk_anchor_ring_fill": (ctypes.c_int, [KC, BT, P, RG, P]),
+        "kk_select_step_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched_workspace_bytes": (SZ, [I32, I32, I32]),
         "kk_score_pool_batched": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
         "kk_coarse_means": (ctypes.c_int, [P, I32, I32, BT, I32, P, P]),
@@ -92,7 +106,7 @@ def _load():
         f = getattr(lib, name)
         f.restype = res
         f.argtypes = args
-    del F, I64
+    del F
     return lib
 
 
@@ -100,10 +114,11 @@ _lib = _load()
 
 #: the C entry points declared in include/kk.h
 EXPORTS = (
-    "kk_status_str", "kk_device_error", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
+    "kk_status_str", "kk_device_error", "kk_debug_set_wait_limit", "kk_debug_skip_pool_copy", "kk_pool_blocks", "kk_head_variance_workspace_bytes",
     "kk_head_variance", "kk_pool_blocks_weighted", "kk_pool_blocks_weighted_static", "kk_anchor", "kk_score", "kk_topk",
     "kk_score_topk", "kk_select_step", "kk_score_topk_stable", "kk_select_step_stable",
-    "kk_compact_table", "kk_append_tokens", "kk_hier_reps", "kk_hier_select",
+    "kk_compact_table", "kk_append_tokens", "kk_anchor_ring_fill", "kk_select_step_workspace_bytes",
+    "kk_hier_reps", "kk_hier_select",
     "kk_score_pool_batched_workspace_bytes",
     "kk_score_pool_batched", "kk_coarse_means", "kk_hier_pool_coarse_rows", "kk_hier_pool_reps",
     "kk_hier_select_pool_workspace_bytes", "kk_hier_select_pool",
@@ -169,7 +184,49 @@ class BlockTable:
         return self.c.num_requests
 
 
+class AnchorRing:
+    """A caller-owned anchor ring on the device: ``rows`` float32 [R][slots][D]
+    and ``pos`` int32 [R][slots] (see kk_anchor_ring in include/kk.h)."""
+
+    def __init__(self, R: int, slots: int, D: int, device="cuda"):
+        self.rows = torch.zeros((R, slots, D), dtype=torch.float32, device=device)
+        self.pos = torch.full((R, slots), -1, dtype=torch.int32, device=device)
+        self.c = kk_anchor_ring(self.rows.data_ptr(), self.pos.data_ptr(), slots)
+
+    @property
+    def slots(self) -> int:
+        return self.c.slots
+
+
+def _options(ring=None, workspace=None):
+    """kk_step_options for a call (None when neither is given); the returned
+    objects must stay alive until the call returns."""
+    if ring is None and workspace is None:
+        return None
+    o = kk_step_options()
+    if ring is not None:
+        o.ring = ctypes.pointer(ring.c)
+    if workspace is not None:
+        o.workspace = _ptr(workspace, name="workspace")
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    return ctypes.byref(o), o
+
+
+def _opt(o):
+    return None if o is None else o[0]
+
+
 # ---- entry points --------------------------------------------------------
+
+
+def kk_debug_set_wait_limit(ns: int):
+    """Limit (ns) of every bounded wait of the launches that follow; 0 restores 1 s."""
+    _check("kk_debug_set_wait_limit", _lib.kk_debug_set_wait_limit(int(ns)))
+
+
+def kk_debug_skip_pool_copy(box: int):
+    """The next persistent pool launch leaves TMA box ``box`` of its first CTA uncopied (-1 cancels)."""
+    _check("kk_debug_skip_pool_copy", _lib.kk_debug_skip_pool_copy(int(box)))
 
 
 def kk_device_error(stream=None) -> int:
@@ -223,45 +280,58 @@ def kk_score(vb, bt: BlockTable, va, scores, stream=None):
                                      _stream(stream)))
 
 
-def kk_topk(scores, offsets, max_n: int, K: int, idx, top_scores=None, stream=None):
+def kk_select_step_workspace_bytes(R: int, max_blocks: int, K: int) -> int:
+    return _lib.kk_select_step_workspace_bytes(R, max_blocks, K)
+
+
+def kk_topk(scores, offsets, max_n: int, K: int, idx, top_scores=None, workspace=None, stream=None):
+    o = _options(workspace=workspace)
     _check("kk_topk", _lib.kk_topk(_ptr(scores, torch.float32, "scores"), _ptr(offsets, torch.int32, "offsets"),
                                    offsets.numel() - 1, max_n, K, _ptr(idx, torch.int32, "idx"),
-                                   _ptr(top_scores, torch.float32, "top_scores"), _stream(stream)))
+                                   _ptr(top_scores, torch.float32, "top_scores"), _opt(o), _stream(stream)))
 
 
-def kk_score_topk(vb, bt: BlockTable, va, K: int, idx, top_scores=None, scores=None, stream=None):
+def kk_score_topk(vb, bt: BlockTable, va, K: int, idx, top_scores=None, scores=None, workspace=None, stream=None):
+    o = _options(workspace=workspace)
     _check("kk_score_topk", _lib.kk_score_topk(
         _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c), _ptr(va, torch.float32, "va"),
         K, _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"),
-        _ptr(scores, torch.float32, "scores"), _stream(stream)))
+        _ptr(scores, torch.float32, "scores"), _opt(o), _stream(stream)))
 
 
 def kk_select_step(kc, bt: BlockTable, W: int, vb, K: int, idx, top_scores=None, va=None, scores=None,
-                   head_w=None, stream=None):
+                   head_w=None, ring=None, workspace=None, stream=None):
+    """``ring``: an :class:`AnchorRing` to take the anchor from (else the K cache)."""
+    o = _options(ring, workspace)
     _check("kk_select_step", _lib.kk_select_step(
         ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
         _ptr(vb, torch.float32, "vb"), K, _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
-        _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _stream(stream)))
+        _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _opt(o),
+        _stream(stream)))
 
 
 def kk_score_topk_stable(vb, bt: BlockTable, va, K: int, stab_window: int, theta: float, hist, idx,
-                         stab=None, top_scores=None, scores=None, stream=None):
+                         stab=None, top_scores=None, scores=None, workspace=None, stream=None):
     """``hist``: int32 tensor [offsets[R]] holding the uint32 history words (updated in place)."""
+    o = _options(workspace=workspace)
     _check("kk_score_topk_stable", _lib.kk_score_topk_stable(
         _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c), _ptr(va, torch.float32, "va"),
         K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"), _ptr(stab, torch.float32, "stab"),
         _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"),
-        _ptr(scores, torch.float32, "scores"), _stream(stream)))
+        _ptr(scores, torch.float32, "scores"), _opt(o), _stream(stream)))
 
 
 def kk_select_step_stable(kc, bt: BlockTable, W: int, vb, K: int, stab_window: int, theta: float, hist, idx,
-                          stab=None, top_scores=None, va=None, scores=None, head_w=None, stream=None):
+                          stab=None, top_scores=None, va=None, scores=None, head_w=None, ring=None, workspace=None,
+                          stream=None):
     """``hist``: int32 tensor [offsets[R]] holding the uint32 history words (updated in place)."""
+    o = _options(ring, workspace)
     _check("kk_select_step_stable", _lib.kk_select_step_stable(
         ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
         _ptr(vb, torch.float32, "vb"), K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"),
         _ptr(stab, torch.float32, "stab"), _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
-        _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _stream(stream)))
+        _ptr(top_scores, torch.float32, "top_scores"), _ptr(scores, torch.float32, "scores"), _opt(o),
+        _stream(stream)))
 
 
 def kk_compact_table(idx, bt: BlockTable, sel_pages, sel_logical=None, sel_count=None, stream=None):
@@ -270,13 +340,21 @@ def kk_compact_table(idx, bt: BlockTable, sel_pages, sel_logical=None, sel_count
         _ptr(sel_logical, torch.int32, "sel_logical"), _ptr(sel_count, torch.int32, "sel_count"), _stream(stream)))
 
 
-def kk_append_tokens(kc, bt: BlockTable, k_new, block_sum, vb, head_w=None, stream=None):
-    """``k_new``: [R][L][H][D] tensor of the cache's element type (int16 bf16 bits or float32)."""
+def kk_append_tokens(kc, bt: BlockTable, k_new, block_sum, vb, head_w=None, ring=None, stream=None):
+    """``k_new``: [R][L][H][D] tensor of the cache's element type (int16 bf16 bits or float32);
+    ``ring``: an :class:`AnchorRing` that also receives each token's pooled Keys."""
     if not k_new.is_cuda or not k_new.is_contiguous():
         raise ValueError("k_new must be a contiguous CUDA tensor")
     _check("kk_append_tokens", _lib.kk_append_tokens(
         ctypes.byref(kc), ctypes.byref(bt.c), ctypes.c_void_p(k_new.data_ptr()), _ptr(head_w, torch.float32, "head_w"),
-        _ptr(block_sum, torch.float32, "block_sum"), _ptr(vb, torch.float32, "vb"), _stream(stream)))
+        _ptr(block_sum, torch.float32, "block_sum"), _ptr(vb, torch.float32, "vb"),
+        None if ring is None else ctypes.byref(ring.c), _stream(stream)))
+
+
+def kk_anchor_ring_fill(kc, bt: BlockTable, ring: AnchorRing, head_w=None, stream=None):
+    _check("kk_anchor_ring_fill", _lib.kk_anchor_ring_fill(
+        ctypes.byref(kc), ctypes.byref(bt.c), _ptr(head_w, torch.float32, "head_w"), ctypes.byref(ring.c),
+        _stream(stream)))
 
 
 def kk_hier_reps(vb, bt: BlockTable, chunk_pages: int, grid_chunks: int, chunk_reps, grid_reps, stream=None):

@@ -90,30 +90,54 @@ def test_host_argument_errors(kk):
     assert lib.kk_score(None, 128, 8, B(t), 16, 16, None) == kk.KK_ERR_INVALID
     assert lib.kk_score(16, 128, 8, B(t), 16, None, None) == kk.KK_ERR_INVALID
     assert lib.kk_score(20, 128, 8, B(t), 16, 16, None) == kk.KK_ERR_UNSUPPORTED
-    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 0, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 257, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 0, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 257, 16, None, None, None, None) == kk.KK_ERR_INVALID
     # kk_topk: K range, R range, empty
-    assert lib.kk_topk(16, 16, 1, 4, 0, 16, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_topk(16, 16, 1, 4, 300, 16, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_topk(16, 16, -1, 4, 4, 16, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_topk(None, None, 0, 4, 4, None, None, None) == kk.KK_OK
+    assert lib.kk_topk(16, 16, 1, 4, 0, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_topk(16, 16, 1, 4, 300, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_topk(16, 16, -1, 4, 4, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_topk(None, None, 0, 4, 4, None, None, None, None) == kk.KK_OK
     # kk_select_step
-    assert lib.kk_select_step(B(d), B(t), 8, None, None, 4, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_select_step(B(d), B(t), 8, None, 16, 0, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_select_step(B(d), B(t), 8, None, None, 4, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_select_step(B(d), B(t), 8, None, 16, 0, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
     # stability filter: window, history words, threshold, table size
     f = float
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 0, f(0.5), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 33, f(0.5), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), None, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("nan"), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("inf"), 16, None, 16, None, None, None) == kk.KK_ERR_INVALID
-    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), 18, None, 16, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 0, f(0.5), 16, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 33, f(0.5), 16, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), None, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("nan"), 16, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f("inf"), 16, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
+    assert lib.kk_score_topk_stable(16, 128, 8, B(t), 16, 4, 20, f(0.5), 18, None, 16, None, None, None, None) == kk.KK_ERR_INVALID
     assert lib.kk_score_topk_stable(16, 128, 8, B(_table(kk, max_blocks=1 << 27)), 16, 4, 20, f(0.5), 16, None, 16,
-                                    None, None, None) == kk.KK_ERR_UNSUPPORTED
-    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 0, f(0.5), 16, None, None, 16, None, None,
+                                    None, None, None, None) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 0, f(0.5), 16, None, None, 16, None, None, None,
                                      None) == kk.KK_ERR_INVALID
-    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 20, f(0.5), None, None, None, 16, None, None,
+    assert lib.kk_select_step_stable(B(d), B(t), 8, None, 16, 4, 20, f(0.5), None, None, None, 16, None, None, None,
                                      None) == kk.KK_ERR_INVALID
+    # decode-step options: workspace too small or misaligned, ring on a score-only call, bad rings
+    ws_need = lib.kk_select_step_workspace_bytes(1, 65536, 32)
+    assert ws_need > 0
+    assert lib.kk_select_step_workspace_bytes(1, 300, 32) == 0  # too short to split
+    assert lib.kk_select_step_workspace_bytes(1, 65536, 0) == 0
+    big = _table(kk, max_blocks=65536)
+    small_ws = kk.kk_step_options(None, 4096, ws_need - 8)
+    assert lib.kk_score_topk(16, 128, 8, B(big), 16, 32, 16, None, None, B(small_ws), None) == kk.KK_ERR_INVALID
+    odd_ws = kk.kk_step_options(None, 4100, ws_need)
+    assert lib.kk_score_topk(16, 128, 8, B(big), 16, 32, 16, None, None, B(odd_ws), None) == kk.KK_ERR_UNSUPPORTED
+    ring = kk.kk_anchor_ring(4096, 4096, 16)
+    with_ring = kk.kk_step_options(ctypes.pointer(ring), None, 0)
+    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 4, 16, None, None, B(with_ring), None) == kk.KK_ERR_INVALID
+    assert lib.kk_topk(16, 16, 1, 4, 4, 16, None, B(with_ring), None) == kk.KK_ERR_INVALID
+    # W above the ring's slots, empty ring, missing positions
+    assert lib.kk_select_step(B(d), B(t), 17, None, 16, 4, None, 16, None, None, B(with_ring), None) == \
+        kk.KK_ERR_INVALID
+    for bad in (kk.kk_anchor_ring(4096, 4096, 0), kk.kk_anchor_ring(4096, None, 16),
+                kk.kk_anchor_ring(None, 4096, 16), kk.kk_anchor_ring(4096, 4096, 1025)):
+        o = kk.kk_step_options(ctypes.pointer(bad), None, 0)
+        assert lib.kk_select_step(B(d), B(t), 8, None, 16, 4, None, 16, None, None, B(o), None) == kk.KK_ERR_INVALID
+        assert lib.kk_anchor_ring_fill(B(d), B(t), None, B(bad), None) == kk.KK_ERR_INVALID
+        assert lib.kk_append_tokens(B(d), B(t), 16, None, 16, 16, B(bad), None) == kk.KK_ERR_INVALID
+    assert lib.kk_anchor_ring_fill(B(d), B(t), None, None, None) == kk.KK_ERR_INVALID
     # kk_head_variance: workspace too small / missing output
     assert lib.kk_head_variance(B(d), B(t), 4, 16, 256, 1, None) == kk.KK_ERR_INVALID
     assert lib.kk_head_variance(B(d), B(t), 4, None, 256, 1 << 30, None) == kk.KK_ERR_INVALID

@@ -70,12 +70,15 @@ def _check_planted(dev, idx):
 
 
 def _step(kk, dev, vb, head_w=None):
+    """One select step, with the workspace that lets long requests split."""
     sp = dev.spec
     idx = torch.zeros((sp.R, sp.K), dtype=torch.int32, device="cuda")
     top = torch.zeros((sp.R, sp.K), device="cuda")
     va = torch.zeros((sp.R, sp.D), device="cuda")
     scores = torch.zeros(sp.total_blocks, device="cuda")
-    kk.kk_select_step(dev.desc, dev.bt, sp.W, vb, sp.K, idx, top, va=va, scores=scores, head_w=head_w)
+    nws = kk.kk_select_step_workspace_bytes(sp.R, max(sp.nb), sp.K)
+    ws = torch.zeros(max(nws, 16), dtype=torch.uint8, device="cuda")
+    kk.kk_select_step(dev.desc, dev.bt, sp.W, vb, sp.K, idx, top, va=va, scores=scores, head_w=head_w, workspace=ws)
     assert kk.kk_device_error() == 0
     return idx.cpu().numpy(), top.cpu().numpy(), va.cpu().numpy(), scores.cpu().numpy()
 

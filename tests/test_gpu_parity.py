@@ -208,10 +208,14 @@ def test_topk_split_long_requests(kk, sizes):
     off_gpu = torch.from_numpy(offsets).cuda()
     for K in (1, 100, 256):
         want = [ko.topk(scores[offsets[r]:offsets[r + 1]], K) for r in range(len(sizes))]
-        for rep in range(3):
+        nws = kk.kk_select_step_workspace_bytes(len(sizes), max(sizes), K)
+        assert nws > 0
+        ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+        for rep in range(4):
             idx = torch.full((len(sizes), K), 7, dtype=torch.int32, device="cuda")
             top = torch.zeros((len(sizes), K), device="cuda")
-            kk.kk_topk(s_gpu, off_gpu, max(sizes), K, idx, top)
+            # the last call without a workspace: every request on one cluster
+            kk.kk_topk(s_gpu, off_gpu, max(sizes), K, idx, top, workspace=ws if rep < 3 else None)
             assert kk.kk_device_error() == 0
             for r in range(len(sizes)):
                 np.testing.assert_array_equal(idx.cpu().numpy()[r], want[r][0], err_msg=f"r={r} K={K} call {rep}")

@@ -168,11 +168,12 @@ def test_score_topk_stable_long_request_split(kk):
     scores = torch.zeros(n, device="cuda")
     idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
     top = torch.zeros((R, K), device="cuda")
+    ws = torch.zeros(kk.kk_select_step_workspace_bytes(R, max(sizes), K), dtype=torch.uint8, device="cuda")
     g_hist = []
     for t in range(steps):
         va_np = (rng.standard_normal((R, D)) + 2.0 * rows.cs[rng.integers(0, 6, R)]).astype(np.float32)
         kk.kk_score_topk_stable(vb, bt, torch.from_numpy(va_np).cuda(), K, W, theta, hist, idx, stab=stab,
-                                top_scores=top, scores=scores)
+                                top_scores=top, scores=scores, workspace=ws)
         assert kk.kk_device_error() == 0
         g_sc, g_idx, g_top, g_stab = scores.cpu().numpy(), idx.cpu().numpy(), top.cpu().numpy(), stab.cpu().numpy()
         g_hist.append(g_sc)
