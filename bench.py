@@ -601,26 +601,48 @@ def main_extras(args, run, dev, stream, peak_gbs):
                                  top_scores=run.top, head_w=run.head_w, ring=ring, workspace=run.step_ws)
 
     out["stable_us"] = b2b_us(select_stable, dev, stream)
-    # hierarchical Grid -> Chunk -> Page (64 blocks a Chunk, 8 Chunks a Grid,
-    # 50 / 20 / 10 %) against the same anchors, coarse levels built once
-    va_h = torch.zeros((sp.R, sp.D), device=dev)
-    kk.kk_anchor(run.desc, run.bt, sp.W, va_h, head_w=run.head_w)
+    out["hier"] = hier_record(run, dev, stream)
+    out["decode_step_us"] = decode_step_us(run, dev, stream)
+    if kk.kk_device_error() != 0:
+        raise RuntimeError("device error in the selector legs")
+    return out
+
+
+def hier_record(run, dev, stream):
+    """Hierarchical Grid -> Chunk -> Page selection (64 blocks a Chunk, 8
+    Chunks a Grid, 50 / 20 / 10 %; coarse levels built once, at write time)
+    against the flat selection (kk_score_topk) on the same anchors, back to
+    back and as CUDA graphs."""
+    import torch
+
+    from kv_cache_block_gb300 import kk
+
+    sp = run.spec
+    va = torch.zeros((sp.R, sp.D), device=dev)
+    kk.kk_anchor(run.desc, run.bt, sp.W, va, head_w=run.head_w)
     c_max = -(-max(sp.nb) // 64)
     g_max = -(-c_max // 8)
     chunk_reps = torch.zeros((sp.R, c_max, sp.D), device=dev)
     grid_reps = torch.zeros((sp.R, g_max, sp.D), device=dev)
     kk.kk_hier_reps(run.vb, run.bt, 64, 8, chunk_reps, grid_reps)
     h_idx = torch.zeros((sp.R, sp.K), dtype=torch.int32, device=dev)
+    f_idx = torch.zeros((sp.R, sp.K), dtype=torch.int32, device=dev)
     h_kept = torch.zeros(sp.R, dtype=torch.int32, device=dev)
 
     def hier_select():
-        kk.kk_hier_select(run.vb, run.bt, chunk_reps, grid_reps, va_h, 64, 8, (500, 200, 100), h_idx, kept=h_kept)
+        kk.kk_hier_select(run.vb, run.bt, chunk_reps, grid_reps, va, 64, 8, (500, 200, 100), h_idx, kept=h_kept,
+                          workspace=run.step_ws)
 
-    out["hier_us"] = b2b_us(hier_select, dev, stream)
-    out["hier_kept"] = int(h_kept.sum().item())
-    out["decode_step_us"] = decode_step_us(run, dev, stream)
+    def flat_select():
+        kk.kk_score_topk(run.vb, run.bt, va, sp.K, f_idx, workspace=run.step_ws)
+
+    out = {"hier_us_back_to_back": b2b_us(hier_select, dev, stream),
+           "hier_us_cuda_graph": graph_time_us(hier_select, dev, stream),
+           "flat_us_back_to_back": b2b_us(flat_select, dev, stream),
+           "flat_us_cuda_graph": graph_time_us(flat_select, dev, stream),
+           "blocks_kept": int(h_kept.sum().item()), "blocks": sp.total_blocks}
     if kk.kk_device_error() != 0:
-        raise RuntimeError("device error in the selector legs")
+        raise RuntimeError("device error in the hierarchy leg")
     return out
 
 
@@ -724,6 +746,8 @@ def record_paged(name, dev, stream, peak_gbs, steps, warmup, flush, coarse=False
     rec["select"] = select_record(run, dev, stream, peak_gbs)
     rec["select_ring"] = select_record(run, dev, stream, peak_gbs, ring=True)
     rec["decode_step_us_cuda_graph"] = decode_step_us(run, dev, stream)
+    if spec.total_blocks >= 2048:
+        rec["hier_select"] = hier_record(run, dev, stream)
     if coarse:
         for group in (64, 512):
             out = torch.zeros((spec.R, -(-max(spec.nb) // group), spec.D), device=dev)
@@ -936,7 +960,7 @@ def main():
         "anchor_then_score_topk_us_cuda_graph": res["two_launch_us"],
         "score_topk_stable_us_back_to_back": res["stable_us"],
         "decode_step_us_cuda_graph": res["decode_step_us"],
-        "hier_select_us_back_to_back": res["hier_us"], "hier_blocks_kept": res["hier_kept"],
+        "hier_select": res["hier"],
         "pool_ms_per_step": res["pool_ms"], "clocks": res["clocks"], "gpu_launches": res["launches"],
         "e2e": None,
     }

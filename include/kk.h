@@ -374,10 +374,15 @@ kk_status kk_append_tokens(const kk_kcache_desc* kc, const kk_block_table* bt, c
  * 500 / 200 / 100 keep 1 % of the blocks), where only the Chunks of kept
  * Grids and the blocks of kept Chunks are active (ties to the lower index).
  * The kept blocks of request r are written to idx[r][0..K) in kk_topk order
- * (logical indices, -1 / -inf padding; at most K of them) and their number
- * to kept[r] (nullable, device int32 [R]; may exceed K). 1 <= K <= 16384.
- * Returns KK_ERR_UNSUPPORTED when a level of the table's longest request
- * could hold more than 16384 members. D in {32, 64, 128, 256}.
+ * (logical indices, -1 / -inf padding; at most K of them: the best min(K,
+ * kept) blocks of the block level) and their number to kept[r] (nullable,
+ * device int32 [R]; may exceed K). 1 <= K <= 256. Returns
+ * KK_ERR_UNSUPPORTED when the Grid level, or the Chunks of the kept Grids, of
+ * the table's longest request could hold more than 32 * D members, or more
+ * than 2048 Chunks could be kept. D in {32, 64, 128, 256}; vb, chunk_reps and
+ * grid_reps 16-byte aligned. opt (nullable): the workspace of
+ * kk_step_options lets the blocks of a few very long requests' kept Chunks be
+ * scored by several clusters (no ring: the anchor is given).
  */
 kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                        int32_t chunk_pages, int32_t grid_chunks, float* chunk_reps, float* grid_reps,
@@ -385,7 +390,8 @@ kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_b
 kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                          const float* chunk_reps, const float* grid_reps, const float* va, int32_t chunk_pages,
                          int32_t grid_chunks, int32_t permille_grid, int32_t permille_chunk, int32_t permille_page,
-                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, cudaStream_t stream);
+                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, const kk_step_options* opt,
+                         cudaStream_t stream);
 
 /*
  * Shared-pool scoring [KK §5.1] (every representation against the anchors

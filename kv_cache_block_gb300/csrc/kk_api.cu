@@ -441,9 +441,11 @@ kk_status kk_anchor_ring_fill(const kk_kcache_desc* kc, const kk_block_table* bt
 }
 
 // Sizes of the hierarchical levels for a table whose longest request has
-// max_blocks blocks, and whether the worst case fits the kernel.
-static bool hier_dims(int32_t max_blocks, int32_t chunk_pages, int32_t grid_chunks, const int32_t* permille,
-                      int* c_max, int* g_max) {
+// max_blocks blocks, and whether the worst case fits the step kernel's
+// hierarchical mode (Grids and active Chunks held in shared memory at once,
+// kept Chunks listed per request).
+static bool hier_dims(int32_t max_blocks, int32_t D, int32_t chunk_pages, int32_t grid_chunks,
+                      const int32_t* permille, int* c_max, int* g_max) {
   const long long C = ((long long)max_blocks + chunk_pages - 1) / chunk_pages;
   const long long G = (C + grid_chunks - 1) / grid_chunks;
   *c_max = (int)C;
@@ -451,8 +453,8 @@ static bool hier_dims(int32_t max_blocks, int32_t chunk_pages, int32_t grid_chun
   const long long kg = (G * permille[0] + 999) / 1000;
   const long long ac = std::min(C, kg * grid_chunks);
   const long long kc = (ac * permille[1] + 999) / 1000;
-  const long long ap = std::min((long long)max_blocks, kc * chunk_pages);
-  return C <= kk::kHierMax && G <= kk::kHierMax && ac <= kk::kHierMax && ap <= kk::kHierMax;
+  const long long cap = kk::step_hier_level_cap(D);
+  return G <= cap && ac <= cap && kc <= kk::kHierKeptChunks && C < (1ll << 31);
 }
 
 kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
@@ -477,23 +479,32 @@ kk_status kk_hier_reps(const float* vb, int32_t D, int32_t num_pages, const kk_b
 kk_status kk_hier_select(const float* vb, int32_t D, int32_t num_pages, const kk_block_table* bt,
                          const float* chunk_reps, const float* grid_reps, const float* va, int32_t chunk_pages,
                          int32_t grid_chunks, int32_t permille_grid, int32_t permille_chunk, int32_t permille_page,
-                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, cudaStream_t stream) {
+                         int32_t K, int32_t* idx, float* top_scores, int32_t* kept, const kk_step_options* opt,
+                         cudaStream_t stream) {
   kk::Table t;
   kk_status st = check_table(bt, false, &t);
   if (st != KK_OK) return st;
   const int32_t pm[3] = {permille_grid, permille_chunk, permille_page};
   if (!vb || !chunk_reps || !grid_reps || !va || !idx || chunk_pages < 1 || grid_chunks < 1 || num_pages <= 0 ||
-      K < 1 || K > kk::kHierMax)
+      K < 1 || K > kk::kMaxK)
     return KK_ERR_INVALID;
   for (int32_t q : pm)
     if (q < 1 || q > 1000) return KK_ERR_INVALID;
   if (!dim_supported(KK_BF16, D)) return KK_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(vb) % 16 || reinterpret_cast<uintptr_t>(chunk_reps) % 16 ||
+      reinterpret_cast<uintptr_t>(grid_reps) % 16)
+    return KK_ERR_UNSUPPORTED;
   int c_max = 0, g_max = 0;
-  if (!hier_dims(t.max_blocks, chunk_pages, grid_chunks, pm, &c_max, &g_max)) return KK_ERR_UNSUPPORTED;
+  if (!hier_dims(t.max_blocks, D, chunk_pages, grid_chunks, pm, &c_max, &g_max)) return KK_ERR_UNSUPPORTED;
+  kk::StepParams sp = {};  // only the split workspace is taken from the options
+  sp.bt = t;
+  sp.K = K;
+  if ((st = step_options(opt, false, &sp)) != KK_OK) return st;
   int* err = error_word();
   if (!err) return KK_ERR_CUDA;
   return from_cuda(kk::launch_hier_select(vb, D, num_pages, t, chunk_reps, grid_reps, c_max, g_max, va,
-                                          chunk_pages, grid_chunks, pm, K, idx, top_scores, kept, err, stream));
+                                          chunk_pages, grid_chunks, pm, K, idx, top_scores, kept, sp.split_ctr,
+                                          sp.split_keys, sp.split_cap, err, stream));
 }
 
 size_t kk_score_pool_batched_workspace_bytes(int32_t R, int32_t N, int32_t K) {

@@ -87,6 +87,14 @@ struct StepParams {
   unsigned long long* split_ctr;
   uint64_t* split_keys;
   int split_cap;
+  // hierarchical selection (nullable hier_grid): the Grid and Chunk levels
+  // pick the Chunks whose blocks are scored; kept[r] (nullable) receives the
+  // number of blocks the block level keeps, and at most that many are output
+  const float* hier_grid;   // [R][g_max][D]
+  const float* hier_chunk;  // [R][c_max][D]
+  int g_max, c_max, chunk_pages, grid_chunks;
+  int permille[3];
+  int* kept;
   unsigned long long wait_ns;  // limit of every bounded wait
   int* err;
   int splits;  // clusters per request (set by the launcher; > 1 for very long requests)
@@ -96,6 +104,10 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t s);
 // holds them for R requests of at most max_blocks blocks (0: never split).
 int step_split_cap(int max_blocks, int K);
 size_t step_workspace_bytes(int R, int max_blocks, int K);
+// Members of a coarse level the step kernel's hierarchical mode holds at once
+// (Grids, or the active Chunks), and kept Chunks of a request.
+int step_hier_level_cap(int D);
+constexpr int kHierKeptChunks = 2048;
 
 // kk_batched.cu
 // Shared-pool GEMM (kk_batched.cu): each anchor's candidate keys (score,
@@ -141,15 +153,15 @@ cudaError_t launch_append(const KCache& kc, const Table& bt, const void* k_new, 
 cudaError_t launch_ring_fill(const KCache& kc, const Table& bt, const float* head_w, const Ring& ring, int* err,
                              cudaStream_t s);
 
-// kk_hier.cu: members of one level of the hierarchical selection held in
-// shared memory at once (Grids, active Chunks, active blocks of a request)
-constexpr int kHierMax = 16384;
+// kk_hier.cu: the Grid level from the Chunk level, and the hierarchical
+// selection (a mode of the step kernel, see StepParams)
 cudaError_t launch_grid_reps(const float* chunk, int D, int c_max, int g_max, const Table& bt, int chunk_pages,
                              int grid_chunks, float* grid, cudaStream_t s);
 cudaError_t launch_hier_select(const float* vb, int D, int vb_rows, const Table& bt, const float* chunk,
                                const float* grid, int c_max, int g_max, const float* va, int chunk_pages,
                                int grid_chunks, const int* permille, int K, int* idx, float* top, int* kept,
-                               int* err, cudaStream_t s);
+                               unsigned long long* split_ctr, uint64_t* split_keys, int split_cap, int* err,
+                               cudaStream_t s);
 
 // kk_host.cu
 void* tensor_map_encoder();  // cuTensorMapEncodeTiled (driver ABI 12.0), or null

@@ -135,6 +135,124 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// The smallest key T such that exactly k of keys[0..n) (distinct, in shared
+// memory) are >= T, k in [1, n]. Up to one key a thread: T is the key with
+// k - 1 keys above it (one counting pass). Longer lists: a radix select on
+// 8-bit digits from just below the bits every key shares, stopping as soon as
+// a digit's bucket holds exactly the keys still needed. hist: 256 ints of
+// shared memory; scal: 2 * kWarps + 3 words of shared memory.
+__device__ __forceinline__ uint64_t block_kth_largest(const uint64_t* keys, int n, int k, int* hist,
+                                                      uint64_t* scal) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t* s_lo = scal;
+  uint64_t* s_hi = scal + kWarps;
+  uint64_t* s_res = scal + 2 * kWarps;
+  int* s_sel = reinterpret_cast<int*>(scal + 2 * kWarps + 1);
+  if (n <= kThreads) {
+    if (tid < n) {
+      const uint64_t key = keys[tid];
+      int above = 0;
+#pragma unroll 8
+      for (int q = 0; q < n; ++q) above += keys[q] > key ? 1 : 0;
+      if (above == k - 1) *s_res = key;
+    }
+    __syncthreads();
+    const uint64_t res = *s_res;
+    __syncthreads();
+    return res;
+  }
+  uint64_t lo = ~0ull, hi = 0ull;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint64_t key = keys[i];
+    lo = key < lo ? key : lo;
+    hi = key > hi ? key : hi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t x = __shfl_xor_sync(kFull, lo, o), y = __shfl_xor_sync(kFull, hi, o);
+    lo = x < lo ? x : lo;
+    hi = y > hi ? y : hi;
+  }
+  if (lane == 0) {
+    s_lo[warp] = lo;
+    s_hi[warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = s_lo[w] < lo ? s_lo[w] : lo;
+    hi = s_hi[w] > hi ? s_hi[w] : hi;
+  }
+  __syncthreads();  // s_lo / s_hi may be rewritten by the next call
+  if (lo == hi) return lo;
+  const int common = __clzll(lo ^ hi);
+  uint64_t pmask = common == 0 ? 0ull : ~0ull << (64 - common);
+  uint64_t prefix = hi & pmask;
+  int need = k;
+  for (int shift = 56 - common;; shift -= 8) {
+    const int sh = shift < 0 ? 0 : shift;  // the last digit may overlap bits already fixed
+    for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint64_t key = keys[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(int)((key >> sh) & 255)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int local = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) local += hist[lane * 8 + b];
+      int sfx = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, sfx, o);
+        if (lane + o < 32) sfx += y;
+      }
+      int above = sfx - local;
+      for (int b = 7; b >= 0; --b) {
+        const int hb = hist[lane * 8 + b];
+        if (above < need && above + hb >= need) {
+          s_sel[0] = lane * 8 + b;
+          s_sel[1] = above;
+        }
+        above += hb;
+      }
+    }
+    __syncthreads();
+    const int b = s_sel[0];
+    need -= s_sel[1];
+    prefix = (prefix & ~((uint64_t)0xFF << sh)) | ((uint64_t)b << sh);
+    pmask |= (uint64_t)0xFF << sh;
+    const bool exact = hist[b] == need;  // every key of this bucket is needed
+    __syncthreads();
+    if (exact || sh == 0) break;
+  }
+  return prefix;
+}
+
+// Block-wide exclusive prefix sum of one count a thread; returns this
+// thread's offset and writes the total to *total. wsum: kWarps ints.
+__device__ __forceinline__ int block_scan(int cnt, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    before += w < warp ? wsum[w] : 0;
+    tot += wsum[w];
+  }
+  __syncthreads();  // wsum may be rewritten by the next call
+  *total = tot;
+  return before + incl - cnt;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -150,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   const bool do_topk = p.flags & kStepTopK;
   const bool from_scores = p.flags & kStepTopKFromScores;
   const bool stab = p.hist != nullptr;  // keys ranked by stability (score mode only)
+  const bool hier = p.hier_grid != nullptr;  // hierarchical selection (score mode, one cluster a request)
   const int K = p.K;
   const int Kp = K <= 1 ? 1 : 1 << (32 - __clz(K - 1));  // next power of two >= K
 
@@ -211,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       for (int s = tid; s < p.kc.L * p.kc.H; s += kThreads)
         sm.w[s] = p.head_w[(long long)r * p.kc.L * p.kc.H + s];
   }
-  const int nstage = do_score ? min(kStage, j1 - j0) : 0;
+  const int nstage = (do_score && !hier) ? min(kStage, j1 - j0) : 0;
   if (do_score) {
-    const int t0count = min(kTile, j1 - j0);
+    const int t0count = hier ? 0 : min(kTile, j1 - j0);  // hier: the blocks are known after its levels
     int pg = -1;
     if (tid < t0count) {
       pg = p.bt.pages[off + j0 + tid];
@@ -393,13 +512,135 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     __syncthreads();
   }
 
+  // ---- hierarchical selection: the Grid and Chunk levels -----------------
+  // Every CTA of the request's cluster runs both coarse levels itself (their
+  // rows are few), so they need no exchange between the CTAs: score every
+  // Grid, keep the best share; list the Chunks of the kept Grids, score them,
+  // keep the best share. The blocks of the kept Chunks are then scored and
+  // ranked below as the table of stage 2, each CTA of the request (all its
+  // clusters) taking every (S * CL)-th kept Chunk. The block level keeps kp = ceil(n * permille / 1000) of its n
+  // blocks; its best min(K, kp) are written.
+  int hn = 0;    // hier: kept Chunks of this CTA (ids ascending in hchunks)
+  int Kout = K;  // output slots filled with blocks
+  int* hchunks = reinterpret_cast<int*>(sm.tok);
+  if (hier) {
+    const int NT = S * CL, gi = sp * CL + crank;  // CTAs of the request, and this one's place among them
+    const int cp = p.chunk_pages, gc = p.grid_chunks;
+    const int C = nb > 0 ? (nb + cp - 1) / cp : 0;
+    const int G = C > 0 ? (C + gc - 1) / gc : 0;
+    uint64_t* mk = reinterpret_cast<uint64_t*>(&sm.stage[0][0]);  // member list / keys of a level
+    uint32_t* gbits = reinterpret_cast<uint32_t*>(&sm.wl[0][0]);  // kept Grids
+    int* hist = reinterpret_cast<int*>(&sm.run[0][0]);
+    uint64_t* scal = &sm.run[1][0];
+    int* wsum = reinterpret_cast<int*>(&sm.run[1][64]);
+    RowSlice<D> av;
+    av.load(sm.va, lane);
+    float t2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < RowSlice<D>::kPer; ++e) t2 = fmaf(av.v[e], av.v[e], t2);
+    const float na2 = warp_sum(t2), na = sqrtf(na2);
+    // keys of members [0, n): mk[i] holds the member's id (low half), or for
+    // the Grid level nothing (the id is i); kR rows a warp per transposed
+    // reduction
+    auto score_level = [&](int n, const float* rows, long long row_base, bool ids_in_list) {
+      constexpr int kR = D <= 128 ? 16 : 8;
+      for (int base = warp * kR; base < n; base += kWarps * kR) {
+        RowSlice<D> b[kR];
+        uint32_t id[kR];
+#pragma unroll
+        for (int u = 0; u < kR; ++u) {
+          const int i = base + u;
+          id[u] = i < n ? (ids_in_list ? (uint32_t)mk[i] : (uint32_t)i) : 0u;
+          b[u].load_global(rows + (row_base + (i < n ? id[u] : 0)) * D, lane);
+        }
+        float part[2 * kR];
+#pragma unroll
+        for (int u = 0; u < kR; ++u) {
+          float dot = 0.f, n2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < RowSlice<D>::kPer; ++e) {
+            dot = fmaf(av.v[e], b[u].v[e], dot);
+            n2 = fmaf(b[u].v[e], b[u].v[e], n2);
+          }
+          part[u] = dot;
+          part[kR + u] = n2;
+        }
+        warp_sum_transpose<2 * kR>(part, lane);
+        const float n2 = __shfl_down_sync(kFull, part[0], kR);
+        uint32_t my_id = 0u;
+#pragma unroll
+        for (int u = 0; u < kR; ++u) my_id = lane == u ? id[u] : my_id;
+        __syncwarp();  // every lane has read its ids before any key overwrites them
+        if (lane < kR && base + lane < n) {
+          float cosv = 0.f;
+          if (na2 > 0.f && n2 > 0.f) cosv = part[0] / (na * sqrtf(n2));
+          cosv = fminf(1.f, fmaxf(-1.f, cosv));
+          mk[base + lane] = make_key(fmaf(0.5f, cosv, 0.5f), my_id);
+        }
+      }
+      __syncthreads();
+    };
+    // Grid level
+    score_level(G, p.hier_grid, (long long)r * p.g_max, false);
+    const int kg = (int)(((long long)G * p.permille[0] + 999) / 1000);
+    const uint64_t thr_g = G > 0 ? block_kth_largest(mk, G, kg, hist, scal) : ~0ull;
+    for (int w = tid; w < (G + 31) / 32; w += kThreads) {
+      uint32_t bits = 0u;
+      for (int b = 0; b < 32 && w * 32 + b < G; ++b) bits |= (mk[w * 32 + b] >= thr_g ? 1u : 0u) << b;
+      gbits[w] = bits;
+    }
+    __syncthreads();
+    // Chunk level: the Chunks of the kept Grids, ascending
+    int nc = 0;
+    for (int g0 = 0; g0 < G; g0 += kThreads) {
+      const int g = g0 + tid;
+      const int cnt = (g < G && ((gbits[g >> 5] >> (g & 31)) & 1u)) ? min(gc, C - g * gc) : 0;
+      int tot;
+      const int at = nc + block_scan(cnt, wsum, &tot);
+      for (int c = 0; c < cnt; ++c) mk[at + c] = (uint64_t)(uint32_t)(g * gc + c);
+      nc += tot;
+    }
+    __syncthreads();
+    score_level(nc, p.hier_chunk, (long long)r * p.c_max, true);
+    const int kc = (int)(((long long)nc * p.permille[1] + 999) / 1000);
+    const uint64_t thr_c = nc > 0 ? block_kth_largest(mk, nc, kc, hist, scal) : ~0ull;
+    // the kept Chunks in id order: every CL-th to this CTA; and the blocks they hold
+    int nkept = 0, nact = 0;
+    for (int i0 = 0; i0 < nc; i0 += kThreads) {
+      const int i = i0 + tid;
+      const bool keep = i < nc && mk[i] >= thr_c;
+      const int c = keep ? (int)key_index(mk[i]) : 0;
+      int tot;
+      const int at = nkept + block_scan(keep ? 1 : 0, wsum, &tot);
+      if (keep && at % NT == gi) hchunks[at / NT] = c;
+      int tb;
+      block_scan(keep ? min(cp, nb - c * cp) : 0, wsum, &tb);
+      nact += tb;
+      nkept += tot;
+    }
+    hn = nkept > gi ? (nkept - gi + NT - 1) / NT : 0;
+    const int kp = (int)(((long long)nact * p.permille[2] + 999) / 1000);
+    Kout = min(K, kp);
+    if (sp == 0 && crank == 0 && tid == 0 && p.kept) p.kept[r] = kp;
+    __syncthreads();
+  }
+  // stage 2's table: blocks [j0, j1) of the request, or (hier) this CTA's
+  // kept Chunks' blocks, position v -> block hier_block(v) (-1 past the end)
+  const int t_lo = hier ? 0 : j0;
+  const int t_hi = hier ? hn * p.chunk_pages : j1;
+  auto hier_block = [&](int v) {
+    const int q = v / p.chunk_pages;
+    const int j = hchunks[q] * p.chunk_pages + (v - q * p.chunk_pages);
+    return j < nb ? j : -1;
+  };
+
   // ---- stage 2: scores and the CTA's top-K over its share of the blocks --
   // Running top-K list: sm.run[cur][0..Kp), descending, zero-padded.
   int run_n = 0, cur = 0;
   // Few blocks per CTA: no per-CTA list; stage 3 all-gathers the raw keys
   // and every CTA ranks its own by counting.
   constexpr int kDirectMax = 64;
-  const bool direct = do_topk && CL > 1 && S == 1 && chunk <= kDirectMax;
+  const bool direct = do_topk && CL > 1 && S == 1 && chunk <= kDirectMax && !hier;
   if (do_topk)
     for (int i = tid; i < Kp; i += kThreads) sm.run[0][i] = 0ull;
   if (do_score || from_scores) {
@@ -418,17 +659,20 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       }
     }
     const float na = sqrtf(na2);
-    for (int tile0 = j0; tile0 < j1; tile0 += kTile) {
-      const int tcount = min(kTile, j1 - tile0);
-      const bool first = tile0 == j0;
+    for (int tile0 = t_lo; tile0 < t_hi; tile0 += kTile) {
+      const int tcount = min(kTile, t_hi - tile0);
+      const bool first = tile0 == t_lo;
       if (do_score) {
-        if (!first) {
+        if (!first || hier) {
           int pg = -1;
           if (tid < tcount) {
-            pg = p.bt.pages[off + tile0 + tid];
-            if (pg < 0 || pg >= p.vb_rows) {
-              flag_error(p.err, kErrBadIndex);
-              pg = -1;
+            const int jt = hier ? hier_block(tile0 + tid) : tile0 + tid;
+            if (jt >= 0) {
+              pg = p.bt.pages[off + jt];
+              if (pg < 0 || pg >= p.vb_rows) {
+                flag_error(p.err, kErrBadIndex);
+                pg = -1;
+              }
             }
           }
           sm.pg[tid] = pg;
@@ -480,8 +724,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
               if (na2 > 0.f && n2 > 0.f) cosv = dot / (na * sqrtf(n2));
               cosv = fminf(1.f, fmaxf(-1.f, cosv));
               const float sc = fmaf(0.5f, cosv, 0.5f);
-              const int j = tile0 + slot;
-              if (p.scores_out) p.scores_out[off + j] = sc;
+              const int j = hier ? hier_block(tile0 + slot) : tile0 + slot;
+              if (p.scores_out && j >= 0) p.scores_out[off + j] = sc;
               uint64_t key = 0ull;
               if (sm.pg[slot] >= 0) {
                 if (p.hist) {
@@ -584,8 +828,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       }
     };
     if (CL == 1) {
-      for (int i = tid; i < run_n; i += kThreads) emit(i, sm.run[cur][i]);
-      pad(run_n);
+      const int nout = min(run_n, Kout);
+      for (int i = tid; i < nout; i += kThreads) emit(i, sm.run[cur][i]);
+      pad(nout);
     } else if (direct) {
       if (!start_waited) {
         cluster_wait_acquire();
@@ -655,12 +900,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         const uint64_t k = have ? sm.merge[crank * Kp + c] : ~0ull;
         int cnt = count_greater_pow2(&sm.merge[list * Kp], Kp, k);
         for (int o = 1; o < CL; o <<= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
-        if (have && list == 0 && cnt < K) emit(cnt, k);
+        if (have && list == 0 && cnt < Kout) emit(cnt, k);
       }
       if (crank == 0) {
         int total = 0;
         for (int q = 0; q < CL; ++q) total += sm.mcount[q];
-        pad(min(total, K));
+        pad(min(total, Kout));
       }
     }
     if (S > 1) {
@@ -720,9 +965,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
             }
             if (warp == 0) {
               if (lane < K) {
-                idx_out[lane] = acc ? (int)(stab ? stab_key_index(acc) : key_index(acc)) : -1;
+                const bool have = acc != 0ull && lane < Kout;
+                idx_out[lane] = have ? (int)(stab ? stab_key_index(acc) : key_index(acc)) : -1;
                 if (top_out)
-                  top_out[lane] = acc ? (stab ? stab_key_score(acc) : key_score(acc)) : -__int_as_float(0x7f800000);
+                  top_out[lane] = have ? (stab ? stab_key_score(acc) : key_score(acc)) : -__int_as_float(0x7f800000);
               }
             }
             if (tid == 0) p.split_ctr[r] = 0ull;  // ready for the next call (and graph replays)
@@ -758,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
               __syncthreads();
             }
             for (int i = tid; i < K; i += kThreads) {
-              const uint64_t k = sm.merge[i];
+              const uint64_t k = i < Kout ? sm.merge[i] : 0ull;
               idx_out[i] = k ? (int)(stab ? stab_key_index(k) : key_index(k)) : -1;
               if (top_out) top_out[i] = k ? (stab ? stab_key_score(k) : key_score(k)) : -__int_as_float(0x7f800000);
             }
@@ -769,6 +1015,17 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     }
   }
   if (!start_waited) cluster_wait_acquire();
+}
+
+// Blocks a request's clusters score: its table, or (hierarchy) the blocks of
+// the kept Chunks, about max_blocks * permille_grid * permille_chunk / 10^6
+// of them plus a Chunk.
+long long hier_work(const StepParams& p) {
+  long long work = p.bt.max_blocks;
+  if (p.hier_grid)
+    work = std::min<long long>(work, (long long)p.bt.max_blocks * p.permille[0] / 1000 * p.permille[1] / 1000 +
+                                         p.chunk_pages);
+  return work;
 }
 
 // Per-device launch setup of one instantiation: dynamic shared memory above
@@ -832,11 +1089,12 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
   // splitting over several clusters instead (one request of 65536 blocks:
   // 28.5 us at 16 CTAs x 16 clusters, 24.1 at 8 x 32).
   const int cap = 8;
+  const long long work = hier_work(p);
   int best = 1;
   for (int cl = 2; cl <= cap; cl <<= 1) {
     if (caps.active[cl] < p.bt.R) break;
     if (cl * Kp > kMergeSlots / 2) break;
-    if ((long long)cl * per_cta_min > (long long)p.bt.max_blocks + per_cta_min) break;
+    if ((long long)cl * per_cta_min > work + per_cta_min) break;
     best = cl;
   }
   return best;
@@ -850,7 +1108,7 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
 int pick_splits(const StepParams& p, const ClusterCaps& caps, int CL) {
   if (!(p.flags & (kStepScore | kStepTopK)) || !p.split_ctr || p.split_cap < 2) return 1;
   int S = caps.active[CL] / p.bt.R;
-  S = std::min(S, p.bt.max_blocks / (CL * kSplitMinBlocks));
+  S = std::min<long long>(S, hier_work(p) / (CL * kSplitMinBlocks));
   S = std::min(S, p.split_cap);
   return std::max(S, 1);
 }
@@ -882,6 +1140,8 @@ cudaError_t launch_typed(const StepParams& p0, cudaStream_t s) {
 }
 
 }  // namespace
+
+int step_hier_level_cap(int D) { return kStage * D / 2; }
 
 int step_split_cap(int max_blocks, int K) {
   const int Kp = K <= 1 ? 1 : 1 << (32 - __builtin_clz(K - 1));

@@ -89,7 +89,7 @@ def _load():
         "kk_select_step_stable": (ctypes.c_int, [KC, BT, I32, P, P, I32, I32, F, P, P, P, P, P, P, OP, P]),
         "kk_compact_table": (ctypes.c_int, [P, I32, BT, P, P, P, P]),
         "kk_hier_reps": (ctypes.c_int, [P, I32, I32, BT, I32, I32, P, P, P]),
-        "kk_hier_select": (ctypes.c_int, [P, I32, I32, BT, P, P, P, I32, I32, I32, I32, I32, I32, P, P, P, P]),
+        "kk_hier_select": (ctypes.c_int, [P, I32, I32, BT, P, P, P, I32, I32, I32, I32, I32, I32, P, P, P, OP, P]),
         "kk_append_tokens": (ctypes.c_int, [KC, BT, P, P, P, P, RG, P]),
         "kk_anchor_ring_fill": (ctypes.c_int, [KC, BT, P, RG, P]),
         "kk_select_step_workspace_bytes": (SZ, [I32, I32, I32]),
@@ -364,14 +364,15 @@ def kk_hier_reps(vb, bt: BlockTable, chunk_pages: int, grid_chunks: int, chunk_r
 
 
 def kk_hier_select(vb, bt: BlockTable, chunk_reps, grid_reps, va, chunk_pages: int, grid_chunks: int, permille,
-                   idx, top_scores=None, kept=None, stream=None):
+                   idx, top_scores=None, kept=None, workspace=None, stream=None):
     pg, pc, pp = (int(x) for x in permille)
+    o = _options(workspace=workspace)
     _check("kk_hier_select", _lib.kk_hier_select(
         _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c),
         _ptr(chunk_reps, torch.float32, "chunk_reps"), _ptr(grid_reps, torch.float32, "grid_reps"),
         _ptr(va, torch.float32, "va"), chunk_pages, grid_chunks, pg, pc, pp, idx.shape[1],
         _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"), _ptr(kept, torch.int32, "kept"),
-        _stream(stream)))
+        _opt(o), _stream(stream)))
 
 
 def kk_score_pool_batched_workspace_bytes(R: int, N: int, K: int) -> int:

@@ -173,16 +173,16 @@ def test_hier_host_errors(kk):
     lib = kk._lib
     t = kk.kk_block_table(4096, 4096, None, 1, 4)
     B = __import__("ctypes").byref
-    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 64, 8, 0, 200, 100, 4, 16, None, None, None) == \
+    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 64, 8, 0, 200, 100, 4, 16, None, None, None, None) == \
         kk.KK_ERR_INVALID
-    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 64, 8, 500, 1001, 100, 4, 16, None, None, None) == \
+    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 64, 8, 500, 1001, 100, 4, 16, None, None, None, None) == \
         kk.KK_ERR_INVALID
-    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 0, 8, 500, 200, 100, 4, 16, None, None, None) == \
+    assert lib.kk_hier_select(16, 128, 8, B(t), 16, 16, 16, 0, 8, 500, 200, 100, 4, 16, None, None, None, None) == \
         kk.KK_ERR_INVALID
-    assert lib.kk_hier_select(16, 96, 8, B(t), 16, 16, 16, 64, 8, 500, 200, 100, 4, 16, None, None, None) == \
+    assert lib.kk_hier_select(16, 96, 8, B(t), 16, 16, 16, 64, 8, 500, 200, 100, 4, 16, None, None, None, None) == \
         kk.KK_ERR_UNSUPPORTED
     big = kk.kk_block_table(4096, 4096, None, 1, 1 << 22)
-    assert lib.kk_hier_select(16, 128, 8, B(big), 16, 16, 16, 64, 8, 1000, 1000, 1000, 4, 16, None, None, None) == \
+    assert lib.kk_hier_select(16, 128, 8, B(big), 16, 16, 16, 64, 8, 1000, 1000, 1000, 4, 16, None, None, None, None) == \
         kk.KK_ERR_UNSUPPORTED
 
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from oracle import kk_oracle as ko
-from tests.helpers import assert_scores_close, assert_vec_close
+from tests.helpers import assert_scores_close, assert_topk_valid, assert_vec_close
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def _cuts_are_clear(vb_l, va, cp, gc, pm):
 @pytest.mark.parametrize("cp,gc,pm,K", [
     (64, 8, (500, 200, 100), 64),
     (4, 3, (500, 200, 100), 16),
-    (8, 2, (700, 400, 250), 300),
+    (8, 2, (700, 400, 250), 256),
     (64, 8, (1000, 1000, 100), 128),
     (16, 4, (300, 300, 500), 5),
 ])
@@ -77,10 +77,9 @@ def test_hier_select(kk, cp, gc, pm, K):
     (64, 8, (500, 200, 100), 40, 41),
 ])
 def test_hier_select_long_requests(kk, cp, gc, pm, K, seed):
-    """Two long requests, so each is scored by a cluster of CTAs: with at
-    most 32 blocks out of a last level of thousands, every CTA folds its
-    share to a 32-key list for the leader (K 32, K 10, and a level that keeps
-    fewer blocks than K); with more, the leader's radix select (K 40)."""
+    """Two long requests, so each is scored by a cluster of CTAs, each CTA
+    taking every CL-th kept Chunk: K 32, K 10, a block level that keeps fewer
+    blocks than K, and K 40."""
     _check_hier(kk, [20000, 16000], 128, cp, gc, pm, K, seed)
 
 
@@ -149,3 +148,46 @@ def test_hier_everything_kept_is_plain_topk(kk):
     kk.kk_score_topk(vb_d, bt, va_d, K, i2, top_scores=t2)
     assert kk.kk_device_error() == 0
     assert torch.equal(i1, i2) and torch.equal(t1, t2)
+
+
+def test_hier_select_split_request(kk):
+    """One request of 70000 blocks whose kept Chunks hold ~35000 blocks: with
+    a workspace, their blocks are scored by several clusters, which meet in
+    the workspace. The Grid and Chunk cuts are clear, so the active blocks
+    are the oracle's; the output is the best K of them (ties within 1e-6 may
+    swap) and the kept count is exact."""
+    nb, D, cp, gc, pm, K = [70000], 128, 64, 8, (1000, 500, 100), 64
+    offsets, pages, vb, va = _case(nb, D, seed=71)
+    bt = kk.BlockTable(_i32(pages), _i32(offsets), None, nb[0])
+    C_max = -(-nb[0] // cp)
+    G_max = -(-C_max // gc)
+    vb_d = torch.from_numpy(vb).cuda()
+    chunk = torch.zeros((1, C_max, D), device="cuda")
+    grid = torch.zeros((1, G_max, D), device="cuda")
+    kk.kk_hier_reps(vb_d, bt, cp, gc, chunk, grid)
+    ws = torch.zeros(kk.kk_select_step_workspace_bytes(1, nb[0], K), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    vb_l = vb.astype(np.float64)[pages]
+    va0 = va[0].astype(np.float64)
+    chunks, grids = ko.hier_reps(vb_l, cp, gc)
+    _, _, want_kept, gk, ck = ko.hier_select(vb_l, va0, 1, cp, gc, pm)
+    ca = np.array([c for c in range(len(chunks)) if c // gc in set(gk.tolist())], dtype=np.int64)
+    sc = ko.affinity(chunks, va0)
+    drop = np.setdiff1d(ca, ck)
+    assert sc[ck].min() - sc[drop].max() > GAP, "the Chunk cut is a near-tie"
+    active = np.array([j for j in range(nb[0]) if j // cp in set(ck.tolist())], dtype=np.int64)
+    s = np.full(nb[0], -np.inf)  # blocks outside the kept Chunks are never candidates
+    s[active] = ko.affinity(vb_l, va0)[active]
+    for rep in range(3):
+        idx = torch.zeros((1, K), dtype=torch.int32, device="cuda")
+        top = torch.zeros((1, K), device="cuda")
+        kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kk.kk_hier_select(vb_d, bt, chunk, grid, torch.from_numpy(va).cuda(), cp, gc, pm, idx, top, kept,
+                          workspace=ws)
+        assert kk.kk_device_error() == 0
+        assert int(kept.item()) == want_kept
+        assert_topk_valid(idx.cpu().numpy()[0], top.cpu().numpy()[0], s, K, f"call {rep}")
+        # the indices are logical blocks of the active set
+        sel = idx.cpu().numpy()[0]
+        assert set(sel.tolist()) <= set(active.tolist())
+        assert ws[:8].cpu().numpy().view(np.uint64)[0] == 0
