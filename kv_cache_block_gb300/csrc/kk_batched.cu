@@ -452,7 +452,6 @@ constexpr int kSelStage = 6144;                    // keys of a row held in regi
 constexpr int kRegKeys = kSelStage / kSelThreads;  // 24 per thread
 constexpr int kBuckets = 2048;                     // linear buckets over a row's score range
 constexpr int kTieCap = 512;                       // boundary-bucket keys ranked exactly
-constexpr int kCandCap = 1024;                     // keys above a threshold round's cut kept for the next
 
 struct SelArgs {
   const uint64_t* keys;  // [R][cap] each anchor's candidate keys, contiguous
@@ -540,85 +539,6 @@ __global__ void __launch_bounds__(kSelThreads) select_rows_kernel(const SelArgs 
         hi = k > hi ? k : hi;
       }
     });
-  }
-  // ---- threshold rounds (rows held in registers): the m-th largest of the
-  // threads' maxima is a key T with at least m keys >= T (the maxima are keys
-  // of the row), and usually not many more. The keys >= T go to shared
-  // memory; at most 256 of them are ranked exactly by counting; up to 1024
-  // take one more round over them (four a thread). Anything else takes the
-  // bucket passes below.
-  if (staged && min(K, n) > 0) {
-    const int m = min(K, n);
-    __shared__ uint64_t s_max[kSelThreads];
-    __shared__ uint64_t s_cand[2][kCandCap];
-    __shared__ uint64_t s_thr;
-    __shared__ int s_cnt[2];
-    // T from this thread's candidate keys (0: none), then the keys >= T into
-    // s_cand[b]; returns their number (capped writes, exact count)
-    auto round = [&](const uint64_t* kk, int U, int b) -> int {
-      uint64_t tmax = 0ull;
-      for (int u = 0; u < U; ++u) tmax = kk[u] > tmax ? kk[u] : tmax;
-      s_max[tid] = tmax;
-      if (tid == 0) s_cnt[b] = 0;
-      __syncthreads();
-      if (tmax != 0ull) {
-        int above = 0;
-#pragma unroll 8
-        for (int q = 0; q < kSelThreads; ++q) above += s_max[q] > tmax ? 1 : 0;
-        if (above == m - 1) s_thr = tmax;
-      }
-      __syncthreads();
-      const uint64_t thr = s_thr;
-      const unsigned below_me = (1u << lane) - 1u;
-      for (int u = 0; u < U; ++u) {
-        const bool in = kk[u] != 0ull && kk[u] >= thr;
-        const unsigned bal = __ballot_sync(kFull, in);
-        int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&s_cnt[b], __popc(bal));
-        base = __shfl_sync(kFull, base, 0);
-        const int at = base + __popc(bal & below_me);
-        if (in && at < kCandCap) s_cand[b][at] = kk[u];
-      }
-      __syncthreads();
-      return s_cnt[b];
-    };
-    // exact: the m largest of c <= kSelThreads candidates, each at its rank
-    auto rank_out = [&](const uint64_t* cand, int c) {
-      int* io = a.idx + (long long)r * K;
-      float* to = a.top ? a.top + (long long)r * K : nullptr;
-      if (tid < c) {
-        const uint64_t mine = cand[tid];
-        int rank = 0;
-#pragma unroll 8
-        for (int q = 0; q < c; ++q) rank += cand[q] > mine ? 1 : 0;
-        if (rank < m) {
-          io[rank] = (int)key_index(mine);
-          if (to) to[rank] = key_score(mine);
-        }
-      }
-      for (int i = m + tid; i < K; i += kSelThreads) {
-        io[i] = -1;
-        if (to) to[i] = -__int_as_float(0x7f800000);
-      }
-    };
-    int c = round(key, kRegKeys, 0);
-    if (c <= kSelThreads) {
-      rank_out(s_cand[0], c);
-      return;
-    }
-    if (c <= kCandCap) {
-      uint64_t k4[kCandCap / kSelThreads];
-#pragma unroll
-      for (int u = 0; u < kCandCap / kSelThreads; ++u) {
-        const int i = tid + u * kSelThreads;
-        k4[u] = i < c ? s_cand[0][i] : 0ull;
-      }
-      c = round(k4, kCandCap / kSelThreads, 1);
-      if (c <= kSelThreads) {
-        rank_out(s_cand[1], c);
-        return;
-      }
-    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
