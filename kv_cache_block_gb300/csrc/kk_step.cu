@@ -140,7 +140,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 // k - 1 keys above it (one counting pass). Longer lists: a radix select on
 // 8-bit digits from just below the bits every key shares, stopping as soon as
 // a digit's bucket holds exactly the keys still needed. hist: 256 ints of
-// shared memory; scal: 2 * kWarps + 3 words of shared memory.
+// shared memory; scal: 2 * kWarps + 3 words of shared memory. (Ranking up to
+// two keys a thread from sorted warp runs by binary search was measured
+// slower here: its searches are chains of dependent loads.)
 __device__ __forceinline__ uint64_t block_kth_largest(const uint64_t* keys, int n, int k, int* hist,
                                                       uint64_t* scal) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -584,11 +586,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     score_level(G, p.hier_grid, (long long)r * p.g_max, false);
     const int kg = (int)(((long long)G * p.permille[0] + 999) / 1000);
     const uint64_t thr_g = G > 0 ? block_kth_largest(mk, G, kg, hist, scal) : ~0ull;
-    for (int w = tid; w < (G + 31) / 32; w += kThreads) {
-      uint32_t bits = 0u;
-      for (int b = 0; b < 32 && w * 32 + b < G; ++b) bits |= (mk[w * 32 + b] >= thr_g ? 1u : 0u) << b;
-      gbits[w] = bits;
-    }
+    for (int w = tid; w < (G + 31) / 32; w += kThreads) gbits[w] = 0u;
+    __syncthreads();
+    for (int i = tid; i < G; i += kThreads)
+      if (mk[i] >= thr_g) atomicOr(&gbits[i >> 5], 1u << (i & 31));
     __syncthreads();
     // Chunk level: the Chunks of the kept Grids, ascending
     int nc = 0;
@@ -605,19 +606,23 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     const int kc = (int)(((long long)nc * p.permille[1] + 999) / 1000);
     const uint64_t thr_c = nc > 0 ? block_kth_largest(mk, nc, kc, hist, scal) : ~0ull;
     // the kept Chunks in id order: every CL-th to this CTA; and the blocks they hold
-    int nkept = 0, nact = 0;
+    int* s_nact = wsum + kWarps;
+    if (tid == 0) *s_nact = 0;
+    int nkept = 0;
     for (int i0 = 0; i0 < nc; i0 += kThreads) {
       const int i = i0 + tid;
       const bool keep = i < nc && mk[i] >= thr_c;
       const int c = keep ? (int)key_index(mk[i]) : 0;
       int tot;
-      const int at = nkept + block_scan(keep ? 1 : 0, wsum, &tot);
-      if (keep && at % NT == gi) hchunks[at / NT] = c;
-      int tb;
-      block_scan(keep ? min(cp, nb - c * cp) : 0, wsum, &tb);
-      nact += tb;
+      const int at = nkept + block_scan(keep ? 1 : 0, wsum, &tot);  // its syncs also order s_nact's zeroing
+      if (keep) {
+        if (at % NT == gi) hchunks[at / NT] = c;
+        atomicAdd(s_nact, min(cp, nb - c * cp));
+      }
       nkept += tot;
     }
+    __syncthreads();
+    const int nact = *s_nact;
     hn = nkept > gi ? (nkept - gi + NT - 1) / NT : 0;
     const int kp = (int)(((long long)nact * p.permille[2] + 999) / 1000);
     Kout = min(K, kp);
