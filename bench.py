@@ -651,8 +651,9 @@ def decode_step_us(run, dev, stream):
     written into its block with v_b and the anchor ring kept current
     (kk_append_tokens), the stability-filtered selection with the anchor from
     the ring (kk_select_step_stable) and the table of selected pages
-    (kk_compact_table). The token is written at position seq_len - 1 (its
-    block exists in this fixed-size cache)."""
+    (kk_compact_table); as three launches and as the one fused launch
+    (kk_step_options k_new and sel_pages). The token is written at position
+    seq_len - 1 (its block exists in this fixed-size cache)."""
     import torch
 
     from kv_cache_block_gb300 import kk
@@ -672,8 +673,14 @@ def decode_step_us(run, dev, stream):
                                  top_scores=run.top, head_w=run.head_w, ring=run.ring, workspace=run.step_ws)
         kk.kk_compact_table(run.idx, run.bt, sel_pages, sel_count=sel_count)
 
+    def decode_step_fused():
+        kk.kk_select_step_stable(run.desc, run.bt, sp.W, run.vb, sp.K, 20, 0.5, hist, run.idx, stab=stab,
+                                 top_scores=run.top, head_w=run.head_w, ring=run.ring, workspace=run.step_ws,
+                                 append=(k_new, block_sum), compact=(sel_pages, None, sel_count))
+
     run.fill_ring()
-    return graph_time_us(decode_step, dev, stream)
+    return {"three_launches": graph_time_us(decode_step, dev, stream),
+            "fused": graph_time_us(decode_step_fused, dev, stream)}
 
 
 def e2e_leg(args, run, dev, stream):

@@ -253,11 +253,29 @@ kk_status kk_anchor_ring_fill(const kk_kcache_desc* kc, const kk_block_table* bt
  *    its bound is reported as KK_ERR_BAD_INDEX. Without a workspace, every
  *    request is served by one cluster. Calls that may run at once need
  *    separate workspaces.
+ *  - k_new, block_sum (kk_select_step and kk_select_step_stable only, with a
+ *    ring; nullable together): the decode token of every request is first
+ *    written as kk_append_tokens(kc, bt, k_new, head_w, block_sum, vb, ring)
+ *    would write it (cache slot, running sum, v_b, ring slot), in the same
+ *    launch, and the step then selects on the updated v_b and ring; vb is
+ *    written, with the same bits as the two calls write. The page that
+ *    receives a request's token must be in no other request's table (that
+ *    request would read its v_b row while it is written). k_new: device,
+ *    16-byte aligned, [R][L][H][D] of the cache's element type; fp32 caches
+ *    with D = 256 are not supported (KK_ERR_UNSUPPORTED).
+ *  - sel_pages, sel_logical, sel_count (not kk_topk; sel_pages nullable, the
+ *    other two nullable): the step also writes the table of the selected
+ *    blocks as kk_compact_table(idx, K, bt, ...) would, in the same launch.
  */
 typedef struct kk_step_options {
   const kk_anchor_ring* ring;
   void* workspace;
   size_t workspace_bytes;
+  const void* k_new;
+  float* block_sum;
+  int32_t* sel_pages;
+  int32_t* sel_logical;
+  int32_t* sel_count;
 } kk_step_options;
 
 /* Workspace bytes that let the decode-step calls split long requests (0:

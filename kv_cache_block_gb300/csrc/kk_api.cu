@@ -195,6 +195,21 @@ kk_status kk_pool_blocks_weighted(const kk_kcache_desc* kc, const kk_block_table
 // workspace.
 static kk_status step_options(const kk_step_options* opt, bool allow_ring, kk::StepParams* p) {
   if (!opt) return KK_OK;
+  if ((opt->k_new == nullptr) != (opt->block_sum == nullptr)) return KK_ERR_INVALID;
+  if (opt->k_new) {
+    // the fused write side: select steps with an anchor ring only
+    if (!allow_ring || !opt->ring) return KK_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(opt->k_new) % 16) return KK_ERR_UNSUPPORTED;
+    if (p->kc.dtype != 1 && p->kc.D > 128) return KK_ERR_UNSUPPORTED;  // as kk_append_tokens
+    p->k_new = opt->k_new;
+    p->block_sum = opt->block_sum;
+  }
+  if (opt->sel_pages) {
+    if (!p->bt.pages) return KK_ERR_INVALID;  // kk_topk has no block table
+    p->sel_pages = opt->sel_pages;
+    p->sel_logical = opt->sel_logical;
+    p->sel_count = opt->sel_count;
+  }
   if (opt->ring) {
     const kk_anchor_ring* g = opt->ring;
     if (!allow_ring || !g->rows || !g->pos || g->slots < 1 || g->slots > kk::kMaxW || p->W > g->slots)

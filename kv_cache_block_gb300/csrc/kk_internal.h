@@ -87,6 +87,14 @@ struct StepParams {
   unsigned long long* split_ctr;
   uint64_t* split_keys;
   int split_cap;
+  // fused write side (nullable k_new): the decode token of every request is
+  // appended (kk_append_tokens, with head_w and the ring) before the step;
+  // fused compact table (nullable sel_pages): kk_compact_table of the output
+  const void* k_new;
+  float* block_sum;
+  int* sel_pages;
+  int* sel_logical;
+  int* sel_count;
   // hierarchical selection (nullable hier_grid): the Grid and Chunk levels
   // pick the Chunks whose blocks are scored; kept[r] (nullable) receives the
   // number of blocks the block level keeps, and at most that many are output
@@ -100,6 +108,8 @@ struct StepParams {
   int splits;  // clusters per request (set by the launcher; > 1 for very long requests)
 };
 cudaError_t launch_step(const StepParams& p, cudaStream_t s);
+// launch_step's instantiations with the decode token's append fused in (k_new)
+cudaError_t launch_step_fused(const StepParams& p, cudaStream_t s);
 // Lists a request may be split into (a power of two), and the workspace that
 // holds them for R requests of at most max_blocks blocks (0: never split).
 int step_split_cap(int max_blocks, int K);

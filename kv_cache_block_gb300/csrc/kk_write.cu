@@ -11,6 +11,7 @@
 //    CTA (the anchor of §5.2 step 1 is a mean of these per-token rows).
 #include <utility>
 
+#include "kk_append.cuh"
 #include "kk_device.cuh"
 #include "kk_pdl.cuh"
 #include "kk_internal.h"
@@ -69,70 +70,22 @@ __global__ void __launch_bounds__(kThreads) compact_table_kernel(const int* idx,
   if (t == 0 && out_count) out_count[r] = n;
 }
 
-// One CTA per request. The new token's Keys k_new[r] ([L][H][D], the cache's
-// element type) are copied 16 bytes at a time into slot (T-1) % bs of the
-// block holding position T-1, and summed over (layer, head) with the
-// request's weights (uniform when head_w is null); the block's running sum
-// restarts at its first token, and v_b = sum / n (/ (L*H) unweighted).
+// One CTA per request: the append of request blockIdx.x's decode token
+// (kk_append.cuh).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(KCache kc, Table bt, const void* k_new, const float* head_w,
                                                           float* block_sum, float* vb, Ring ring, int* err) {
-  constexpr int EPV = Vec16<T>::kElems;
-  constexpr int V16 = D / EPV;  // 16-byte vectors per row
-  constexpr int RSTEP = kThreads / V16;
-  constexpr int ES = elem_bytes<T>();
-  static_assert(V16 >= 1 && V16 <= 32 && (32 % V16) == 0, "row must be 16..512 bytes");
-  __shared__ float s_red[RSTEP][D];
+  __shared__ float s_red[kThreads * Vec16<T>::kElems];
+  __shared__ float s_x[D];
   pdl_launch_dependents();
   pdl_wait();
-  const int r = blockIdx.x, tid = threadIdx.x;
-  const int off = bt.offsets[r];
-  const int nb = bt.offsets[r + 1] - off;
-  const int T_r = bt.seq_lens[r];
-  if (T_r < 1 || nb > bt.max_blocks || nb != (T_r + kc.bs - 1) / kc.bs) {
-    if (tid == 0) flag_error(err, kErrBadIndex);
-    return;
-  }
-  const int t = T_r - 1, slot = t % kc.bs;
-  const int page = bt.pages[off + t / kc.bs];
-  if (page < 0 || page >= kc.num_pages) {
-    if (tid == 0) flag_error(err, kErrBadIndex);
-    return;
-  }
-  const int LH = kc.L * kc.H;
-  const int vec = tid % V16, s0 = tid / V16;
-  const char* src = static_cast<const char*>(k_new) + (long long)r * LH * D * ES;  // byte offsets: T is a tag
-  char* base = reinterpret_cast<char*>(const_cast<void*>(kc.base));
-  float acc[EPV];
-#pragma unroll
-  for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
-  for (int s = s0; s < LH; s += RSTEP) {
-    const int l = s / kc.H, h = s - l * kc.H;
-    const uint4 x = *reinterpret_cast<const uint4*>(src + ((long long)s * D + vec * EPV) * ES);
-    char* dst = base + ((long long)l * kc.sL + (long long)page * kc.sP + (long long)h * kc.sH +
-                        (long long)slot * kc.sT + vec * EPV) * ES;
-    *reinterpret_cast<uint4*>(dst) = x;
-    float f[EPV];
-    Vec16<T>::unpack(x, f);
-    const float w = head_w ? head_w[(long long)r * LH + s] : 1.f;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) acc[e] = fmaf(w, f[e], acc[e]);
-  }
-#pragma unroll
-  for (int e = 0; e < EPV; ++e) s_red[s0][vec * EPV + e] = acc[e];
-  __syncthreads();
-  const float scale = head_w ? 1.f / (float)(slot + 1) : 1.f / ((float)(slot + 1) * (float)LH);
-  const long long rslot = ring.rows ? (long long)r * ring.slots + t % ring.slots : 0;
-  for (int d = tid; d < D; d += kThreads) {
-    float x = 0.f;
-    for (int q = 0; q < RSTEP; ++q) x += s_red[q][d];
-    float* sum = block_sum + (long long)page * D + d;
-    const float total = slot == 0 ? x : *sum + x;
-    *sum = total;
-    vb[(long long)page * D + d] = total * scale;
-    if (ring.rows) ring.rows[rslot * D + d] = x;
-  }
-  if (ring.rows && tid == 0) ring.pos[rslot] = t;
+  const int r = blockIdx.x;
+  int t;
+  const int page = append_page(kc, bt, r, &t, err, true);
+  if (page < 0) return;
+  const float old = load_old_sum(block_sum, page, t, kc.bs, D);
+  pool_token<T, D, kThreads>(kc, r, k_new, head_w, page, t % kc.bs, 0, 1, s_red, s_x);
+  commit_token(r, page, t, kc.bs, kc.L * kc.H, head_w != nullptr, D, old, s_x, block_sum, vb, ring);
 }
 
 // CTA (i, r): slot of token t = T - 1 - i of request r when i < min(slots, T)

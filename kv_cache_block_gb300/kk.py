@@ -60,7 +60,8 @@ class kk_anchor_ring(ctypes.Structure):
 
 class kk_step_options(ctypes.Structure):
     _fields_ = [("ring", ctypes.POINTER(kk_anchor_ring)), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("k_new", ctypes.c_void_p), ("block_sum", ctypes.c_void_p),
+                ("sel_pages", ctypes.c_void_p), ("sel_logical", ctypes.c_void_p), ("sel_count", ctypes.c_void_p)]
 
 
 def _load():
@@ -198,10 +199,12 @@ class AnchorRing:
         return self.c.slots
 
 
-def _options(ring=None, workspace=None):
-    """kk_step_options for a call (None when neither is given); the returned
-    objects must stay alive until the call returns."""
-    if ring is None and workspace is None:
+def _options(ring=None, workspace=None, append=None, compact=None):
+    """kk_step_options for a call (None when nothing is given); the returned
+    objects must stay alive until the call returns. ``append``: (k_new,
+    block_sum) of the fused write side; ``compact``: (sel_pages, sel_logical,
+    sel_count) of the fused table (the last two may be None)."""
+    if ring is None and workspace is None and append is None and compact is None:
         return None
     o = kk_step_options()
     if ring is not None:
@@ -209,6 +212,17 @@ def _options(ring=None, workspace=None):
     if workspace is not None:
         o.workspace = _ptr(workspace, name="workspace")
         o.workspace_bytes = workspace.numel() * workspace.element_size()
+    if append is not None:
+        k_new, block_sum = append
+        if not k_new.is_cuda or not k_new.is_contiguous():
+            raise ValueError("k_new must be a contiguous CUDA tensor")
+        o.k_new = k_new.data_ptr()
+        o.block_sum = _ptr(block_sum, torch.float32, "block_sum")
+    if compact is not None:
+        sp, sl, sc = compact
+        o.sel_pages = _ptr(sp, torch.int32, "sel_pages")
+        o.sel_logical = _ptr(sl, torch.int32, "sel_logical")
+        o.sel_count = _ptr(sc, torch.int32, "sel_count")
     return ctypes.byref(o), o
 
 
@@ -291,8 +305,9 @@ def kk_topk(scores, offsets, max_n: int, K: int, idx, top_scores=None, workspace
                                    _ptr(top_scores, torch.float32, "top_scores"), _opt(o), _stream(stream)))
 
 
-def kk_score_topk(vb, bt: BlockTable, va, K: int, idx, top_scores=None, scores=None, workspace=None, stream=None):
-    o = _options(workspace=workspace)
+def kk_score_topk(vb, bt: BlockTable, va, K: int, idx, top_scores=None, scores=None, workspace=None, compact=None,
+                  stream=None):
+    o = _options(workspace=workspace, compact=compact)
     _check("kk_score_topk", _lib.kk_score_topk(
         _ptr(vb, torch.float32, "vb"), vb.shape[1], vb.shape[0], ctypes.byref(bt.c), _ptr(va, torch.float32, "va"),
         K, _ptr(idx, torch.int32, "idx"), _ptr(top_scores, torch.float32, "top_scores"),
@@ -300,9 +315,10 @@ def kk_score_topk(vb, bt: BlockTable, va, K: int, idx, top_scores=None, scores=N
 
 
 def kk_select_step(kc, bt: BlockTable, W: int, vb, K: int, idx, top_scores=None, va=None, scores=None,
-                   head_w=None, ring=None, workspace=None, stream=None):
-    """``ring``: an :class:`AnchorRing` to take the anchor from (else the K cache)."""
-    o = _options(ring, workspace)
+                   head_w=None, ring=None, workspace=None, append=None, compact=None, stream=None):
+    """``ring``: an :class:`AnchorRing` to take the anchor from (else the K cache);
+    ``append`` / ``compact``: the fused write side and table (see kk_step_options)."""
+    o = _options(ring, workspace, append, compact)
     _check("kk_select_step", _lib.kk_select_step(
         ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
         _ptr(vb, torch.float32, "vb"), K, _ptr(va, torch.float32, "va"), _ptr(idx, torch.int32, "idx"),
@@ -323,9 +339,9 @@ def kk_score_topk_stable(vb, bt: BlockTable, va, K: int, stab_window: int, theta
 
 def kk_select_step_stable(kc, bt: BlockTable, W: int, vb, K: int, stab_window: int, theta: float, hist, idx,
                           stab=None, top_scores=None, va=None, scores=None, head_w=None, ring=None, workspace=None,
-                          stream=None):
+                          append=None, compact=None, stream=None):
     """``hist``: int32 tensor [offsets[R]] holding the uint32 history words (updated in place)."""
-    o = _options(ring, workspace)
+    o = _options(ring, workspace, append, compact)
     _check("kk_select_step_stable", _lib.kk_select_step_stable(
         ctypes.byref(kc), ctypes.byref(bt.c), W, _ptr(head_w, torch.float32, "head_w"),
         _ptr(vb, torch.float32, "vb"), K, stab_window, float(theta), _ptr(hist, torch.int32, "hist"),
