@@ -6,8 +6,9 @@
 // together (two round trips per batch instead of two per row), in
 // compensated (Kahan) float32: a group may hold hundreds of rows, and float64
 // arithmetic runs at a small fraction of the float32 rate on this GPU. The RL
-// partial rows are added in float64 (a few dozen additions per output).
-// Groups of 256 rows or more take 1024 threads.
+// partial rows are added the same way (measured: adding them and dividing in
+// float64 made the kernel 4 times slower than its HBM time). Groups of 256
+// rows or more take 1024 threads.
 #include "kk_device.cuh"
 #include "kk_internal.h"
 
@@ -21,7 +22,7 @@ __global__ void __launch_bounds__(kThreads) coarse_kernel(const float* vb, int n
   constexpr int V4 = D / 4;            // 16-byte columns of a row
   constexpr int RL = kThreads / V4;    // rows summed side by side
   static_assert(kThreads % V4 == 0, "whole rows per pass");
-  __shared__ double s_acc[RL][D];
+  __shared__ float s_acc[RL][D];
   const int g = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
   const int off = offsets[r];
   int nb = offsets[r + 1] - off;
@@ -63,13 +64,18 @@ __global__ void __launch_bounds__(kThreads) coarse_kernel(const float* vb, int n
     }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) s_acc[k][c4 * 4 + e] = (double)acc[e] - (double)cmp[e];
+  for (int e = 0; e < 4; ++e) s_acc[k][c4 * 4 + e] = acc[e] - cmp[e];
   __syncthreads();
   const int cnt = j1 - j0;
   for (int d = tid; d < D; d += kThreads) {
-    double s = 0.0;
-    for (int q = 0; q < RL; ++q) s += s_acc[q][d];
-    out[((long long)r * ng_max + g) * D + d] = cnt > 0 ? (float)(s / cnt) : 0.f;
+    float s = 0.f, c = 0.f;
+    for (int q = 0; q < RL; ++q) {
+      const float y = s_acc[q][d] - c;
+      const float t = s + y;
+      c = (t - s) - y;
+      s = t;
+    }
+    out[((long long)r * ng_max + g) * D + d] = cnt > 0 ? (s - c) / (float)cnt : 0.f;
   }
 }
 
