@@ -278,3 +278,70 @@ def test_fused_split_request(kk, K, stable):
             pg, lg, n = _compact_expected(outs["fus"]["idx"][r], tables[r])
             np.testing.assert_array_equal(outs["fus"]["sp"][r], pg, err_msg=f"{what} r={r} sel_pages")
             np.testing.assert_array_equal(outs["fus"]["sl"][r], lg, err_msg=f"{what} r={r} sel_logical")
+
+
+def test_split_score_topk_compact_table(kk):
+    """kk_score_topk with a workspace on a request long enough to split over
+    clusters: the table the merging cluster writes is kk_compact_table's."""
+    spec = synth.qwen7b(L=1, H=2, D=128, bs=16, seq_lens=[16 * 12000, 16 * 40], num_topics=8, W=16, K=64,
+                        shuffle_pages=True)
+    dev = DeviceCache(spec)
+    vb = torch.zeros((spec.num_pages, spec.D), device="cuda")
+    kk.kk_pool_blocks(dev.desc, dev.pages, dev.n_valid, vb)
+    va = torch.randn((spec.R, spec.D), device="cuda")
+    R, K = spec.R, spec.K
+    res = []
+    for fused in (False, True):
+        ws = torch.zeros(kk.kk_select_step_workspace_bytes(R, max(spec.nb), K), dtype=torch.uint8, device="cuda")
+        idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+        sp, sl, sc = (torch.full((R, K), 9, dtype=torch.int32, device="cuda"),
+                      torch.full((R, K), 9, dtype=torch.int32, device="cuda"),
+                      torch.full((R,), 9, dtype=torch.int32, device="cuda"))
+        if fused:
+            kk.kk_score_topk(vb, dev.bt, va, K, idx, workspace=ws, compact=(sp, sl, sc))
+        else:
+            kk.kk_score_topk(vb, dev.bt, va, K, idx, workspace=ws)
+            kk.kk_compact_table(idx, dev.bt, sp, sl, sc)
+        assert kk.kk_device_error() == 0
+        assert np.any(ws.cpu().numpy()[256:] != 0), "the request was split"
+        res.append([t.cpu().numpy() for t in (idx, sp, sl, sc)])
+    for a, b in zip(*res):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_fused_bad_token_page_is_reported(kk):
+    """A request whose token block holds an out-of-range page: the fused call
+    reports it on the device error word and leaves the other requests'
+    outputs and state as the separate calls leave them."""
+    spec = SPECS["short"]()
+    R, D, K, W = spec.R, spec.D, spec.K, spec.W
+    sep, fus = _State(kk, spec, None, W + 3), _State(kk, spec, None, W + 3)
+    for st in (sep, fus):
+        _prefill(kk, st, spec, None, None)
+    # requests whose next token fits in their last block take one; the others
+    # take none this step (their table and length stay as they are)
+    grow = [r for r in range(R) if spec.seq_lens[r] % spec.bs]
+    lens = [spec.seq_lens[r] + (1 if r in grow else 0) for r in range(R)]
+    pages = np.array(spec.pages, dtype=np.int32)
+    bad_r = grow[0]
+    pages[spec.offsets[bad_r + 1] - 1] = spec.num_pages + 7  # the token's block
+    bt = kk.BlockTable(_i32(pages), _i32(spec.offsets), _i32(lens), max(spec.nb))
+    kn = torch.from_numpy(synth.bf16_rne(np.random.default_rng(3).standard_normal((R, spec.L, spec.H, D))
+                                         .astype(np.float32)).view(np.int16)).cuda()
+    outs = {}
+    for tag, st in (("sep", sep), ("fus", fus)):
+        idx = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+        va = torch.zeros((R, D), device="cuda")
+        if tag == "sep":
+            kk.kk_append_tokens(st.dev.desc, bt, kn, st.block_sum, st.vb, ring=st.ring)
+            kk.kk_select_step(st.dev.desc, bt, W, st.vb, K, idx, va=va, ring=st.ring)
+        else:
+            kk.kk_select_step(st.dev.desc, bt, W, st.vb, K, idx, va=va, ring=st.ring, append=(kn, st.block_sum))
+        assert kk.kk_device_error() == kk.KK_ERR_BAD_INDEX, tag
+        outs[tag] = (idx.cpu().numpy(), va.cpu().numpy())
+    ok = [r for r in range(R) if r != bad_r]
+    np.testing.assert_array_equal(outs["fus"][0][ok], outs["sep"][0][ok])
+    np.testing.assert_array_equal(outs["fus"][1][ok], outs["sep"][1][ok])
+    for a, b in ((fus.vb, sep.vb), (fus.block_sum, sep.block_sum), (fus.dev.storage, sep.dev.storage)):
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    assert kk.kk_device_error() == 0  # the word was cleared by the read
