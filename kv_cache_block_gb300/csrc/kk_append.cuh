@@ -1,5 +1,5 @@
 // The write of one decode token, shared by kk_append_tokens (kk_write.cu)
-// and the decode step that fuses it (kk_step.cu). Request r's decode token
+// and the decode step that fuses it (kk_step.cuh). Request r's decode token
 // sits at position t = T - 1 (T = seq_lens[r]; the table already holds its
 // block); its Keys k_new[r] ([L][H][D], the cache's element type) go into
 // slot t % bs of the block's page, their sum over (layer, head) with the

@@ -1,7 +1,7 @@
 // Hierarchical Grid -> Chunk -> Page selection ("Key-Key Semantic Affinity"
 // page, §5.1). The Chunk level's representations are kk_coarse_means over the
 // blocks; grid_reps_kernel builds the Grid level from them. The selection
-// itself is a mode of the decode-step kernel (kk_step.cu): every CTA of a
+// itself is a mode of the decode-step kernel (kk_step.cuh): every CTA of a
 // request's cluster runs the Grid and Chunk levels itself, then the blocks of
 // the kept Chunks are scored and ranked like a request's table.
 #include "kk_internal.h"
