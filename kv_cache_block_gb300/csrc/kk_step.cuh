@@ -39,6 +39,7 @@ namespace {
 // request's output and sets the counter back to zero.
 constexpr int kSplitPerWarp = 8;     // lists each warp folds in the final merge of K <= 32
 constexpr int kSplitMinBlocks = 256;  // blocks per CTA below which a request is not split further
+constexpr int kHierSplitMinBlocks = 64;  // the same for the hierarchy's block level
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -586,11 +587,16 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
   // Grid, keep the best share; list the Chunks of the kept Grids, score them,
   // keep the best share. The blocks of the kept Chunks are then scored and
   // ranked below as the table of stage 2, each CTA of the request (all its
-  // clusters) taking every (S * CL)-th kept Chunk. The block level keeps kp = ceil(n * permille / 1000) of its n
-  // blocks; its best min(K, kp) are written.
-  int hn = 0;    // hier: kept Chunks of this CTA (ids ascending in hchunks)
+  // clusters) taking an equal run of their block positions (a few kept
+  // Chunks are then spread over every CTA: measured, 32 requests x 1024
+  // blocks, dealing whole Chunks left 2 of a request's 8 CTAs scoring 64
+  // blocks each while the others waited). The block level keeps
+  // kp = ceil(n * permille / 1000) of its n blocks; its best min(K, kp) are
+  // written.
+  int h_lo = 0, h_hi = 0;  // hier: this CTA's block positions in the kept Chunks (ids ascending in hchunks)
   int Kout = K;  // output slots filled with blocks
   int* hchunks = reinterpret_cast<int*>(sm.tok);
+  static_assert(sizeof(sm.tok) >= kHierKeptChunks * sizeof(int), "every kept Chunk of a request is listed");
   if (hier) {
     const int NT = S * CL, gi = sp * CL + crank;  // CTAs of the request, and this one's place among them
     const int cp = p.chunk_pages, gc = p.grid_chunks;
@@ -607,19 +613,25 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
 #pragma unroll
     for (int e = 0; e < RowSlice<D>::kPer; ++e) t2 = fmaf(av.v[e], av.v[e], t2);
     const float na2 = warp_sum(t2), na = sqrtf(na2);
-    // keys of members [0, n): mk[i] holds the member's id (low half), or for
-    // the Grid level nothing (the id is i); kR rows a warp per transposed
-    // reduction
-    auto score_level = [&](int n, const float* rows, long long row_base, bool ids_in_list) {
-      constexpr int kR = D <= 128 ? 16 : 8;
+    // keys of members [0, n) into mk[0, n): member(i, &row, &id) names the
+    // member's representation row and its id (for the Chunk list, mk[i]
+    // holds the id until its key overwrites it); kR rows a warp per
+    // transposed reduction
+    constexpr int kR = D <= 128 ? 16 : 8;
+    auto score_level = [&](int n, auto&& member) {
       for (int base = warp * kR; base < n; base += kWarps * kR) {
         RowSlice<D> b[kR];
         uint32_t id[kR];
 #pragma unroll
         for (int u = 0; u < kR; ++u) {
           const int i = base + u;
-          id[u] = i < n ? (ids_in_list ? (uint32_t)mk[i] : (uint32_t)i) : 0u;
-          b[u].load_global(rows + (row_base + (i < n ? id[u] : 0)) * D, lane);
+          // slots past n load a fixed valid row (their result is dropped);
+          // member() is asked only for real members, since a slot's id may
+          // already have been overwritten by its key in the Chunk-list mode
+          const float* row = p.hier_grid;
+          id[u] = 0u;
+          if (i < n) member(i, &row, &id[u]);
+          b[u].load_global(row, lane);
         }
         float part[2 * kR];
 #pragma unroll
@@ -648,8 +660,23 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       }
       __syncthreads();
     };
-    // Grid level
-    score_level(G, p.hier_grid, (long long)r * p.g_max, false);
+    const float* grid_rows = p.hier_grid + (long long)r * p.g_max * D;
+    const float* chunk_rows = p.hier_chunk + (long long)r * p.c_max * D;
+    // Grid level. When the Grids and every Chunk fit in one round of row
+    // loads, the Chunks are scored with the Grids (keys at mk[G + c]) and
+    // those outside the kept Grids are dropped afterwards: one round trip
+    // less than scoring the kept Grids' Chunks after the Grid selection.
+    const bool all_chunks = G + C <= kWarps * kR;
+    if (all_chunks)
+      score_level(G + C, [&](int i, const float** row, uint32_t* id) {
+        *id = (uint32_t)(i < G ? i : i - G);
+        *row = (i < G ? grid_rows : chunk_rows) + (long long)*id * D;
+      });
+    else
+      score_level(G, [&](int i, const float** row, uint32_t* id) {
+        *id = (uint32_t)i;
+        *row = grid_rows + (long long)i * D;
+      });
     const int kg = (int)(((long long)G * p.permille[0] + 999) / 1000);
     const uint64_t thr_g = G > 0 ? block_kth_largest(mk, G, kg, hist, scal) : ~0ull;
     for (int w = tid; w < (G + 31) / 32; w += kThreads) gbits[w] = 0u;
@@ -657,48 +684,70 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     for (int i = tid; i < G; i += kThreads)
       if (mk[i] >= thr_g) atomicOr(&gbits[i >> 5], 1u << (i & 31));
     __syncthreads();
-    // Chunk level: the Chunks of the kept Grids, ascending
-    int nc = 0;
-    for (int g0 = 0; g0 < G; g0 += kThreads) {
-      const int g = g0 + tid;
-      const int cnt = (g < G && ((gbits[g >> 5] >> (g & 31)) & 1u)) ? min(gc, C - g * gc) : 0;
-      int tot;
-      const int at = nc + block_scan(cnt, wsum, &tot);
-      for (int c = 0; c < cnt; ++c) mk[at + c] = (uint64_t)(uint32_t)(g * gc + c);
-      nc += tot;
+    // Chunk level: the Chunks of the kept Grids (ids ascending), nc of them,
+    // their keys ck[0, ncand)
+    int nc = 0, ncand = 0;
+    uint64_t* ck = mk;
+    if (all_chunks) {
+      ck = mk + G;
+      ncand = C;
+      bool in = false;
+      for (int c = tid; c < C; c += kThreads) {  // C <= kWarps * kR <= kThreads: one pass
+        const int g = c / gc;
+        in = (gbits[g >> 5] >> (g & 31)) & 1u;
+        if (!in) ck[c] = 0ull;  // below every key
+      }
+      nc = __syncthreads_count(in);
+    } else {
+      for (int g0 = 0; g0 < G; g0 += kThreads) {
+        const int g = g0 + tid;
+        const int cnt = (g < G && ((gbits[g >> 5] >> (g & 31)) & 1u)) ? min(gc, C - g * gc) : 0;
+        int tot;
+        const int at = nc + block_scan(cnt, wsum, &tot);
+        for (int c = 0; c < cnt; ++c) mk[at + c] = (uint64_t)(uint32_t)(g * gc + c);
+        nc += tot;
+      }
+      __syncthreads();
+      score_level(nc, [&](int i, const float** row, uint32_t* id) {
+        *id = (uint32_t)mk[i];
+        *row = chunk_rows + (long long)*id * D;
+      });
+      ncand = nc;
     }
-    __syncthreads();
-    score_level(nc, p.hier_chunk, (long long)r * p.c_max, true);
     const int kc = (int)(((long long)nc * p.permille[1] + 999) / 1000);
-    const uint64_t thr_c = nc > 0 ? block_kth_largest(mk, nc, kc, hist, scal) : ~0ull;
-    // the kept Chunks in id order: every CL-th to this CTA; and the blocks they hold
+    const uint64_t thr_c = nc > 0 ? block_kth_largest(ck, ncand, kc, hist, scal) : ~0ull;
+    // the kept Chunks in id order, and the blocks they hold
     int* s_nact = wsum + kWarps;
     if (tid == 0) *s_nact = 0;
     int nkept = 0;
-    for (int i0 = 0; i0 < nc; i0 += kThreads) {
+    for (int i0 = 0; i0 < ncand; i0 += kThreads) {
       const int i = i0 + tid;
-      const bool keep = i < nc && mk[i] >= thr_c;
-      const int c = keep ? (int)key_index(mk[i]) : 0;
+      const bool keep = i < ncand && ck[i] >= thr_c;
+      const int c = keep ? (int)key_index(ck[i]) : 0;
       int tot;
       const int at = nkept + block_scan(keep ? 1 : 0, wsum, &tot);  // its syncs also order s_nact's zeroing
       if (keep) {
-        if (at % NT == gi) hchunks[at / NT] = c;
+        hchunks[at] = c;  // at most kHierKeptChunks, checked by the caller
         atomicAdd(s_nact, min(cp, nb - c * cp));
       }
       nkept += tot;
     }
     __syncthreads();
     const int nact = *s_nact;
-    hn = nkept > gi ? (nkept - gi + NT - 1) / NT : 0;
+    const int ptot = nkept * cp;  // positions; those past the request's last block map to no block
+    const int span = (ptot + NT - 1) / NT;
+    h_lo = min(ptot, gi * span);
+    h_hi = min(ptot, h_lo + span);
     const int kp = (int)(((long long)nact * p.permille[2] + 999) / 1000);
     Kout = min(K, kp);
     if (sp == 0 && crank == 0 && tid == 0 && p.kept) p.kept[r] = kp;
     __syncthreads();
   }
-  // stage 2's table: blocks [j0, j1) of the request, or (hier) this CTA's
-  // kept Chunks' blocks, position v -> block hier_block(v) (-1 past the end)
-  const int t_lo = hier ? 0 : j0;
-  const int t_hi = hier ? hn * p.chunk_pages : j1;
+  // stage 2's table: blocks [j0, j1) of the request, or (hier) positions
+  // [h_lo, h_hi) of the kept Chunks' blocks, position v -> block
+  // hier_block(v) (-1 past the request's end)
+  const int t_lo = hier ? h_lo : j0;
+  const int t_hi = hier ? h_hi : j1;
   auto hier_block = [&](int v) {
     const int q = v / p.chunk_pages;
     const int j = hchunks[q] * p.chunk_pages + (v - q * p.chunk_pages);
@@ -1272,7 +1321,11 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
 int pick_splits(const StepParams& p, const ClusterCaps& caps, int CL) {
   if (!(p.flags & (kStepScore | kStepTopK)) || !p.split_ctr || p.split_cap < 2) return 1;
   int S = caps.active[CL] / p.bt.R;
-  S = std::min<long long>(S, hier_work(p) / (CL * kSplitMinBlocks));
+  // the hierarchy's coarse levels run in every CTA at once, so its few kept
+  // blocks are spread thinner (measured, one request of 65536 blocks: 24
+  // CTAs left 275 blocks each to the block level)
+  const int min_blocks = p.hier_grid ? kHierSplitMinBlocks : kSplitMinBlocks;
+  S = std::min<long long>(S, hier_work(p) / (CL * min_blocks));
   S = std::min(S, p.split_cap);
   return std::max(S, 1);
 }
