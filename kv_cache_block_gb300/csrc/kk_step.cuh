@@ -679,11 +679,13 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       });
     const int kg = (int)(((long long)G * p.permille[0] + 999) / 1000);
     const uint64_t thr_g = G > 0 ? block_kth_largest(mk, G, kg, hist, scal) : ~0ull;
-    for (int w = tid; w < (G + 31) / 32; w += kThreads) gbits[w] = 0u;
-    __syncthreads();
-    for (int i = tid; i < G; i += kThreads)
-      if (mk[i] >= thr_g) atomicOr(&gbits[i >> 5], 1u << (i & 31));
-    __syncthreads();
+    if (!all_chunks) {  // the kept Grids as bits (the single-round path reads the Grid keys instead)
+      for (int w = tid; w < (G + 31) / 32; w += kThreads) gbits[w] = 0u;
+      __syncthreads();
+      for (int i = tid; i < G; i += kThreads)
+        if (mk[i] >= thr_g) atomicOr(&gbits[i >> 5], 1u << (i & 31));
+      __syncthreads();
+    }
     // Chunk level: the Chunks of the kept Grids (ids ascending), nc of them,
     // their keys ck[0, ncand)
     int nc = 0, ncand = 0;
@@ -693,8 +695,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       ncand = C;
       bool in = false;
       for (int c = tid; c < C; c += kThreads) {  // C <= kWarps * kR <= kThreads: one pass
-        const int g = c / gc;
-        in = (gbits[g >> 5] >> (g & 31)) & 1u;
+        in = mk[c / gc] >= thr_g;  // its Grid is kept
         if (!in) ck[c] = 0ull;  // below every key
       }
       nc = __syncthreads_count(in);
