@@ -138,6 +138,24 @@ def test_host_argument_errors(kk):
         assert lib.kk_anchor_ring_fill(B(d), B(t), None, B(bad), None) == kk.KK_ERR_INVALID
         assert lib.kk_append_tokens(B(d), B(t), 16, None, 16, 16, B(bad), None) == kk.KK_ERR_INVALID
     assert lib.kk_anchor_ring_fill(B(d), B(t), None, None, None) == kk.KK_ERR_INVALID
+    # the fused write side and table: k_new needs block_sum and a ring (select steps only), 16-byte
+    # alignment, and no fp32 cache of D 256; a table needs a block table (not kk_topk)
+    O = kk.kk_step_options
+    rp = ctypes.pointer(ring)
+    assert lib.kk_select_step(B(d), B(t), 8, None, 16, 4, None, 16, None, None, B(O(rp, None, 0, 4096, None)),
+                              None) == kk.KK_ERR_INVALID
+    assert lib.kk_select_step(B(d), B(t), 8, None, 16, 4, None, 16, None, None, B(O(None, None, 0, 4096, 4096)),
+                              None) == kk.KK_ERR_INVALID
+    assert lib.kk_select_step(B(d), B(t), 8, None, 16, 4, None, 16, None, None, B(O(rp, None, 0, 4100, 4096)),
+                              None) == kk.KK_ERR_UNSUPPORTED
+    d256 = _desc(kk, dtype=kk.KK_F32, head_dim=256, stride_layer=8 * 2 * 16 * 256, stride_page=2 * 16 * 256,
+                 stride_head=16 * 256, stride_token=256)
+    assert lib.kk_select_step(B(d256), B(t), 8, None, 16, 4, None, 16, None, None,
+                              B(O(ctypes.pointer(kk.kk_anchor_ring(4096, 4096, 16)), None, 0, 4096, 4096)),
+                              None) == kk.KK_ERR_UNSUPPORTED
+    assert lib.kk_score_topk(16, 128, 8, B(t), 16, 4, 16, None, None, B(O(None, None, 0, 4096, 4096)), None) == \
+        kk.KK_ERR_INVALID
+    assert lib.kk_topk(16, 16, 1, 4, 4, 16, None, B(O(None, None, 0, None, None, 4096)), None) == kk.KK_ERR_INVALID
     # kk_head_variance: workspace too small / missing output
     assert lib.kk_head_variance(B(d), B(t), 4, 16, 256, 1, None) == kk.KK_ERR_INVALID
     assert lib.kk_head_variance(B(d), B(t), 4, None, 256, 1 << 30, None) == kk.KK_ERR_INVALID
