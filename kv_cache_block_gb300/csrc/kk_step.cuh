@@ -662,11 +662,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
     };
     const float* grid_rows = p.hier_grid + (long long)r * p.g_max * D;
     const float* chunk_rows = p.hier_chunk + (long long)r * p.c_max * D;
-    // Grid level. When the Grids and every Chunk fit in one round of row
+    // Grid level. When the Grids and every Chunk fit in two rounds of row
     // loads, the Chunks are scored with the Grids (keys at mk[G + c]) and
-    // those outside the kept Grids are dropped afterwards: one round trip
-    // less than scoring the kept Grids' Chunks after the Grid selection.
-    const bool all_chunks = G + C <= kWarps * kR;
+    // those outside the kept Grids are dropped afterwards: no wait for the
+    // Grid selection before the Chunks' rows are loaded, and no Chunk list.
+    const bool all_chunks = G + C <= 2 * kWarps * kR;
+    static_assert(2 * kWarps * 16 <= kThreads, "a thread a Chunk in the single pass below");
     if (all_chunks)
       score_level(G + C, [&](int i, const float** row, uint32_t* id) {
         *id = (uint32_t)(i < G ? i : i - G);
@@ -694,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
       ck = mk + G;
       ncand = C;
       bool in = false;
-      for (int c = tid; c < C; c += kThreads) {  // C <= kWarps * kR <= kThreads: one pass
+      for (int c = tid; c < C; c += kThreads) {  // C <= 2 * kWarps * kR <= kThreads: one pass
         in = mk[c / gc] >= thr_g;  // its Grid is kept
         if (!in) ck[c] = 0ull;  // below every key
       }
