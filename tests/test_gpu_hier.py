@@ -83,6 +83,15 @@ def test_hier_select_long_requests(kk, cp, gc, pm, K, seed):
     _check_hier(kk, [20000, 16000], 128, cp, gc, pm, K, seed)
 
 
+@pytest.mark.parametrize("D", [32, 64, 256])
+def test_hier_select_head_dims(kk, D):
+    """Other head dims, with requests whose Grids and Chunks are scored in
+    one round of row loads, in two, and through the Chunk list (700, 1200
+    and 3000 blocks at 8 blocks a Chunk, 4 Chunks a Grid; at D 256 a warp
+    takes 8 rows a round, so the 1200-block request takes the list)."""
+    _check_hier(kk, [700, 1200, 3000, 1, 150], D, 8, 4, (500, 300, 200), 24, seed=1)
+
+
 def _check_hier(kk, nb, D, cp, gc, pm, K, seed):
     offsets, pages, vb, va = _case(nb, D, seed=seed)
     R = len(nb)
