@@ -1302,9 +1302,11 @@ int pick_cluster(const StepParams& p, const ClusterCaps& caps) {
   // than the extra SMs return (7B: 10.5 us at 8 vs 11.3 at 16; 8 x 1024
   // blocks: 13.7 vs 18.5). A few very long requests take more SMs by
   // splitting over several clusters instead (one request of 65536 blocks:
-  // 28.5 us at 16 CTAs x 16 clusters, 24.1 at 8 x 32).
-  const int cap = 8;
+  // 28.5 us at 16 CTAs x 16 clusters, 24.1 at 8 x 32). Short tables of few
+  // requests do gain from 16 (one request of 256 blocks, anchor from the
+  // ring: 6.9 -> 6.5 us).
   const long long work = hier_work(p);
+  const int cap = work <= 512 ? 16 : 8;
   int best = 1;
   for (int cl = 2; cl <= cap; cl <<= 1) {
     if (caps.active[cl] < p.bt.R) break;
